@@ -1,0 +1,280 @@
+"""Plain CPU oracle: TIDE's packed-shard layout, two-level fp32 reduce-scatter
+and direct-landing all-gather, written from the pages' definitions.
+
+TEST INFRASTRUCTURE ONLY -- imported by the tests, by ``__graft_entry__.smoke``
+and by the CPU-baseline leg of ``bench.py``; never by the CUDA library, with
+which it shares no code.  Slow and obvious on purpose: numpy float32 arrays are
+used only for elementwise IEEE round-to-nearest-even adds across independent
+output elements; the order of the additions for each output element is exactly
+the one written out below, with no blocking, fusion or reordering.
+
+Sources (three web pages about the TIDE preprint, arXiv 2610.38228):
+
+[Endgame]  "The Endgame of FSDP Communication: Layout-Aware Collectives on Copy
+           Engines, RDMA, and NVSwitch" (explainer)
+[Richland] "TIDE gives FSDP2 layout-aware zero-copy collectives: up to 27.1%
+           faster steps on 64 GPUs, zero-SM all-gather, bf16->fp32
+           reduce-scatter" (news post)
+[Abstract] the preprint's abstract page with its figure captions and tables
+
+Notation follows [Abstract] Table 2 (Notation): M nodes, L GPUs per NVSwitch
+domain, N = M*L ranks, r = n*L + l; for parameter p, Rp padded per-rank rows,
+Kp row length, sp / op per-rank shard size and prefix offset (kept here in
+elements, not bytes), S per-rank packed shard size.
+
+Readings taken where the pages leave a step open (each is marked "Reading" at
+its use below):
+  R1  Rp = ceil(R_p / N); rank r owns global rows [r*Rp, (r+1)*Rp); rows at or
+      beyond R_p are zero padding.
+  R2  Kp = product of the dims after dim 0 (1 for a 1-D tensor; a 0-D tensor
+      is treated as shape [1]).
+  R3  op is the plain prefix sum of the per-rank piece sizes, no alignment gap.
+  R4  the reduction is a plain sum (no averaging), fp32 round-to-nearest-even,
+      every accumulator starting from +0.0.
+  R5  level 2 adds the node partials in landing-GPU order g = 0..L-1.
+  R6  slice s of a destination node is block s of each of its ranks' packed
+      shards, cut into L contiguous blocks of ceil(S / L) elements.
+  R8  level 1 adds the L local contributions in ascending local index l.
+  R9  the all-gather writes the padded [N*Rp, Kp] parameter-major block.
+"""
+
+from dataclasses import dataclass
+
+import numpy as np
+
+__all__ = [
+    "Geometry", "geometry", "rank_major_offset", "param_major_offset", "valid_elems",
+    "owner_of_row", "relative_index", "landing_gpu", "handled_slice", "slice_len",
+    "slice_of", "level2_order", "bf16_to_f32", "rs_reduce", "ag_place", "rs_element",
+    "ag_element",
+]
+
+
+# --------------------------------------------------------------------------
+# Layout: [Abstract] Table 2 (Notation); [Endgame] "What problem is it
+# actually solving?" (the hand-checkable example of rank-major vs
+# parameter-major offsets); [Abstract] Figure 1.
+# --------------------------------------------------------------------------
+
+@dataclass
+class Geometry:
+    N: int
+    P: int
+    rows: list   # R_p, the unpadded dim-0 size of parameter p
+    Kp: list     # row length of p (Reading R2)
+    Rp: list     # padded per-rank rows of p (Reading R1)
+    e: list      # per-rank piece of p in elements, Rp * Kp
+    o: list      # prefix offset op of p inside a packed shard, in elements (R3)
+    S: int       # per-rank packed shard size in elements
+
+
+def geometry(shapes, N):
+    """Per-parameter dim-0 shard geometry of a parameter group over N ranks."""
+    if N < 1:
+        raise ValueError("N must be >= 1")
+    rows, Kp, Rp, e, o = [], [], [], [], []
+    offset = 0
+    for shape in shapes:
+        shape = tuple(int(d) for d in shape) or (1,)          # Reading R2: 0-D as [1]
+        if any(d < 0 for d in shape):
+            raise ValueError("negative dimension")
+        k = 1
+        for d in shape[1:]:
+            k *= d                                            # Reading R2
+        r_pad = -(-shape[0] // N)                             # Reading R1: ceil(R_p / N)
+        rows.append(shape[0])
+        Kp.append(k)
+        Rp.append(r_pad)
+        e.append(r_pad * k)
+        o.append(offset)                                      # Reading R3
+        offset += r_pad * k
+    return Geometry(N=N, P=len(rows), rows=rows, Kp=Kp, Rp=Rp, e=e, o=o, S=offset)
+
+
+def rank_major_offset(geo, p, r):
+    """Element offset of rank r's piece of p in the flat rank-major buffer.
+
+    All of rank 0's pieces come first, then rank 1's, and so on
+    ([Endgame] "What problem is it actually solving?").
+    """
+    return r * geo.S + geo.o[p]
+
+
+def param_major_offset(geo, p, r):
+    """Element offset of rank r's piece of p when every parameter is one block.
+
+    Parameter p's block starts after the N full pieces of every earlier
+    parameter (N * op), and rank r's piece sits r pieces into it
+    ([Endgame] "What problem is it actually solving?"; [Abstract] Figure 1).
+    """
+    return geo.N * geo.o[p] + r * geo.e[p]
+
+
+def owner_of_row(geo, p, g):
+    """Rank that holds global row g of parameter p (Reading R1)."""
+    return g // geo.Rp[p]
+
+
+def valid_elems(geo, p, r):
+    """Elements of rank r's piece of p that come from real rows (the rest pad)."""
+    real_rows = min(geo.Rp[p], max(0, geo.rows[p] - r * geo.Rp[p]))
+    return real_rows * geo.Kp[p]
+
+
+# --------------------------------------------------------------------------
+# Latin-square placement: [Endgame] "Reduce-scatter: two levels of addition,
+# the last one done by NVSwitch"; [Abstract] Figure 6(b).
+# --------------------------------------------------------------------------
+
+def relative_index(n_dest, n_src, M):
+    """c = destination's node number minus the source's, modulo M."""
+    return (n_dest - n_src) % M
+
+
+def handled_slice(j, c, L):
+    """On a source node with relative index c, GPU j sums slice (j + c) mod L."""
+    return (j + c) % L
+
+
+def landing_gpu(s, c, L):
+    """Slice s from the source with relative index c lands on GPU (s - c) mod L.
+
+    GPU j of the source sends over line j to GPU j of the destination, and it
+    handles slice s = (j + c) mod L, so j = (s - c) mod L.
+    """
+    return (s - c) % L
+
+
+def slice_len(S, L):
+    """Elements per slice when a packed shard is cut into L blocks (Reading R6)."""
+    return -(-S // L) if S > 0 else 0
+
+
+def slice_of(x, S, L):
+    """Slice index of packed-shard position x (Reading R6)."""
+    return x // slice_len(S, L)
+
+
+def level2_order(s, n_dest, M, L):
+    """Source nodes of slice s in the order their partials are added (Reading R5).
+
+    The destination's GPUs are visited g = 0, 1, ..., L-1; GPU g holds the
+    partial of the source whose slice s lands on it.  With M < L some GPUs hold
+    nothing for slice s.  More than L sources need the batched scheme of the
+    same section, which this oracle does not cover.
+    """
+    if M > L:
+        raise NotImplementedError("more nodes than GPUs per node needs source batching")
+    order = []
+    for g in range(L):
+        for n_src in range(M):
+            if landing_gpu(s, relative_index(n_dest, n_src, M), L) == g:
+                order.append(n_src)
+    return order
+
+
+# --------------------------------------------------------------------------
+# Reduce-scatter: bf16 per-parameter gradients in, fp32 packed shards out.
+# [Endgame] "Reduce-scatter: two levels of addition, the last one done by
+# NVSwitch"; [Richland] "What shipped" (bf16 gradients consumed in place and
+# reduced into fp32 shards; fp32 node partials); [Endgame] "What problem is it
+# actually solving?" (sliced, zero-padded, upcast).
+# --------------------------------------------------------------------------
+
+def bf16_to_f32(bits):
+    """Exact bf16 -> fp32 widening: the 16 bits become the high half of fp32."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _node_partial(grad_slice_of, n_src, L, count):
+    """Level 1: fp32 sum of node n_src's L local bf16 copies, l = 0..L-1 (R8)."""
+    acc1 = np.zeros(count, dtype=np.float32)                 # Reading R4: start at +0.0
+    for l in range(L):
+        acc1 = acc1 + bf16_to_f32(grad_slice_of(n_src * L + l))
+    return acc1
+
+
+def rs_reduce(geo, grads, M, L):
+    """Reduce-scatter of grads[rank][p] (uint16 bf16 bits, R_p*Kp row-major).
+
+    Returns N float32 arrays of S elements: rank r's packed fp32 gradient shard.
+    """
+    N = geo.N
+    if N != M * L:
+        raise ValueError("N must equal M * L")
+    shards = []
+    for r in range(N):
+        n_dest = r // L
+        out = np.empty(geo.S, dtype=np.float32)
+        for p in range(geo.P):
+            e_p, o_p = geo.e[p], geo.o[p]
+            v = valid_elems(geo, p, r)
+            # Rows at or beyond R_p are zero padding (Reading R1).
+            out[o_p + v:o_p + e_p] = np.float32(0.0)
+            a = 0
+            while a < v:
+                s = slice_of(o_p + a, geo.S, L)
+                b = min(v, (s + 1) * slice_len(geo.S, L) - o_p)
+                src0 = r * e_p + a   # rank r's rows start at global row r*Rp
+
+                def grad_slice_of(src_rank, p=p, src0=src0, count=b - a):
+                    return grads[src_rank][p][src0:src0 + count]
+
+                acc2 = np.zeros(b - a, dtype=np.float32)      # Reading R4
+                for n_src in level2_order(s, n_dest, M, L):  # level 2, Reading R5
+                    acc2 = acc2 + _node_partial(grad_slice_of, n_src, L, b - a)
+                out[o_p + a:o_p + b] = acc2
+                a = b
+        shards.append(out)
+    return shards
+
+
+def rs_element(geo, M, L, r, x, grad_at):
+    """One element of rank r's packed fp32 shard at position x, from scratch.
+
+    ``grad_at(src_rank, p, idx)`` returns the bf16 bits of contributor
+    src_rank's gradient of p at flat indices idx.  Same arithmetic and order as
+    ``rs_reduce``; used for sampled checks at sizes the full oracle cannot hold.
+    """
+    p = next(q for q in range(geo.P) if geo.o[q] <= x < geo.o[q] + geo.e[q])
+    e = x - geo.o[p]
+    if e >= valid_elems(geo, p, r):
+        return np.float32(0.0)
+    s = slice_of(x, geo.S, L)
+    idx = np.array([r * geo.e[p] + e], dtype=np.int64)
+    acc2 = np.float32(0.0)
+    for n_src in level2_order(s, r // L, M, L):
+        acc1 = np.float32(0.0)
+        for l in range(L):
+            acc1 = np.float32(acc1 + bf16_to_f32(grad_at(n_src * L + l, p, idx))[0])
+        acc2 = np.float32(acc2 + acc1)
+    return acc2
+
+
+# --------------------------------------------------------------------------
+# All-gather with direct landing: each rank's packed shard piece is written
+# once, at its final parameter-major address.  [Endgame] "All-gather:
+# parameters land at their final address"; [Richland] "What shipped";
+# [Abstract] Figure 1 and Figure 5(b).
+# --------------------------------------------------------------------------
+
+def ag_place(geo, shards):
+    """All-gather of N packed shards (1-D arrays of S elements, any dtype).
+
+    Returns P arrays: parameter p as its padded N*Rp x Kp block, flattened
+    (Reading R9; the parameter proper is its first R_p rows).
+    """
+    params = []
+    for p in range(geo.P):
+        e_p, o_p = geo.e[p], geo.o[p]
+        block = np.empty(geo.N * e_p, dtype=shards[0].dtype)
+        for r in range(geo.N):
+            block[r * e_p:(r + 1) * e_p] = shards[r][o_p:o_p + e_p]
+        params.append(block)
+    return params
+
+
+def ag_element(geo, p, y, shard_at):
+    """Element y of parameter p's gathered block, from ``shard_at(r, idx)``."""
+    r, e = divmod(y, geo.e[p])
+    return shard_at(r, np.array([geo.o[p] + e], dtype=np.int64))[0]

@@ -1,0 +1,316 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each ``check_*`` raises AssertionError when the oracle disagrees with:
+* the pages' worked examples (``tests/golden/*.json``, each citing its page),
+* brute-force enumeration over full parameters on tiny groups,
+* exact integer arithmetic (integer-valued bf16 sums are exact in fp32),
+* the rigorous error bound of recursive fp32 summation against an fp64 sum,
+* structural invariants (bijections, zero padding, round trips).
+
+They are plain functions so that ``test_oracle_mutations`` can plant a
+mistake in the oracle and confirm that at least one check notices it.
+"""
+
+import itertools
+import json
+import os
+
+import numpy as np
+
+import oracle.tide_oracle as O
+from synth import gen
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- layout pins
+
+def check_hand_layout_example():
+    g = _golden("layout_example.json")
+    N = g["N"]
+    for unit in (1, 64):   # one unit = one row of `unit` elements
+        shapes = [(k * N, unit) for k in g["piece_units"]]
+        geo = O.geometry(shapes, N)
+        assert [x // unit for x in geo.e] == g["piece_units"]
+        assert geo.S // unit == g["units_per_rank"]
+        p, r = g["param"], g["rank"]
+        assert O.rank_major_offset(geo, p, r) == g["rank_major_offset_units"] * unit
+        assert O.param_major_offset(geo, p, r) == g["param_major_offset_units"] * unit
+
+
+def _tiny_groups():
+    """Small parameter groups with padding, 1-D/3-D/0-D shapes and rows < N."""
+    groups = [
+        ([(8, 64), (4, 64), (12, 64)], 1, 4),
+        ([(5, 3), (1,), (7, 2, 2), (), (3, 1)], 2, 2),
+        ([(13, 5), (2, 7), (17,), (6, 6)], 2, 3),
+        ([(1, 9), (16, 8), (31, 3)], 4, 4),
+        ([(11, 1), (3, 4)], 1, 1),
+        ([(9, 5), (40, 3), (2, 2)], 3, 4),
+        ([(16, 8)], 4, 4),
+        ([(23, 3), (5, 5), (0, 4)], 2, 3),
+    ]
+    return groups
+
+
+def check_bruteforce_index_maps():
+    """Row ownership and both offsets, enumerated element by element."""
+    for shapes, M, L in _tiny_groups():
+        N = M * L
+        geo = O.geometry(shapes, N)
+        seen_rank_major = np.zeros(N * geo.S, dtype=np.int64)
+        seen_param_major = np.zeros(N * geo.S, dtype=np.int64)
+        for p, shape in enumerate(shapes):
+            shape = tuple(shape) or (1,)
+            R = shape[0]
+            K = int(np.prod(shape[1:])) if len(shape) > 1 else 1
+            rp = -(-R // N)
+            assert geo.Rp[p] == rp and geo.Kp[p] == K and geo.rows[p] == R
+            for r in range(N):
+                # rank r's piece of p holds rows [r*rp, (r+1)*rp), real or padding
+                real = sum(1 for g in range(r * rp, (r + 1) * rp) if g < R)
+                assert O.valid_elems(geo, p, r) == real * K
+                for i in range(rp * K):
+                    seen_rank_major[O.rank_major_offset(geo, p, r) + i] += 1
+                    seen_param_major[O.param_major_offset(geo, p, r) + i] += 1
+            for g in range(R):
+                assert O.owner_of_row(geo, p, g) == g // rp
+        # both layouts tile [0, N*S) exactly once
+        assert (seen_rank_major == 1).all() and (seen_param_major == 1).all()
+        # parameters are contiguous and in order in the parameter-major layout
+        for p in range(geo.P):
+            assert O.param_major_offset(geo, p, 0) == N * sum(geo.e[:p])
+
+
+def check_no_padding_when_divisible():
+    for shapes, N in [([(8192, 8192), (1024, 8192), (8192,)], 8),
+                      ([(4096, 2048), (768, 2048), (2048,)], 16),
+                      ([(5120, 5120), (13824, 5120), (5120,)], 64)]:
+        geo = O.geometry(shapes, N)
+        G = sum(int(np.prod(s)) for s in shapes)
+        assert N * geo.S == G
+    geo = O.geometry([(49, 3)], 48)   # 49 rows over 48 ranks: 2 rows each, 47 padding
+    assert geo.Rp == [2] and 48 * geo.S - 49 * 3 == 47 * 3
+
+
+def check_pack_buffer_size_identity():
+    """Stock FSDP2's fp32 pack is twice the padded bf16 group (same element count)."""
+    for shapes, M, L in _tiny_groups():
+        N = M * L
+        geo = O.geometry(shapes, N)
+        padded_bf16_bytes = 2 * sum(N * geo.Rp[p] * geo.Kp[p] for p in range(geo.P))
+        assert 4 * N * geo.S == 2 * padded_bf16_bytes
+
+
+# ---------------------------------------------------------- Latin-square pins
+
+def check_latin_square_figure6():
+    g = _golden("latin_square_fig6.json")
+    L = g["L"]
+    for name, c in g["relative_index"].items():
+        assert O.landing_gpu(0, c, L) == g["slice0_landing_gpu"][name]
+    table = g["derived_by_hand"]["landing_gpu_by_slice_then_c"]
+    for s in range(L):
+        for c in range(g["M"]):
+            assert O.landing_gpu(s, c, L) == table[s][c]
+    # D, A, B, C numbered 0..3 as destination 0 and sources with indices 1..3
+    M = g["M"]
+    n_dest = 0
+    for name, c in g["relative_index"].items():
+        n_src = (n_dest - c) % M
+        assert O.relative_index(n_dest, n_src, M) == c
+
+
+def check_latin_property():
+    """Every row and column of the seating table holds each source exactly once,
+    and the source-side rule (GPU j sums slice (j+c) mod L and sends on line j)
+    agrees with the landing rule."""
+    for L in range(1, 9):
+        for M in range(1, L + 1):
+            for n_dest in range(M):
+                for s in range(L):
+                    gpus = [O.landing_gpu(s, O.relative_index(n_dest, n, M), L) for n in range(M)]
+                    assert len(set(gpus)) == M
+                for g in range(L):
+                    srcs = [n for n in range(M) for s in range(L)
+                            if O.landing_gpu(s, O.relative_index(n_dest, n, M), L) == g]
+                    # source c lands on GPU g for exactly one slice, (g + c) mod L
+                    assert sorted(srcs) == list(range(M))
+            for c in range(M):
+                for j in range(L):
+                    s = O.handled_slice(j, c, L)
+                    assert O.landing_gpu(s, c, L) == j
+
+
+def check_level2_order_cases():
+    cases = _golden("level2_order_cases.json")["cases"]
+    for case in cases:
+        for s, expect in enumerate(case["order_by_slice"]):
+            assert O.level2_order(s, case["n_dest"], case["M"], case["L"]) == expect
+
+
+def check_level2_order_cancellation():
+    """Order-sensitive sums whose fp32 results were worked out by hand."""
+    for g in _golden("level2_order_cases.json")["cancellations"]:
+        M, L = g["M"], g["L"]
+        N = M * L
+        R, K = g["shape"]
+        geo = O.geometry([(R, K)], N)
+        grads = [[np.zeros(R * K, dtype=np.uint16)] for _ in range(N)]
+        for n, v in enumerate(g["V"]):
+            bits = gen.f32_to_bf16_bits(np.full(K, v, dtype=np.float32))
+            for row in g["planted_rows"]:
+                grads[n * L][0][row * K:(row + 1) * K] = bits
+        out = O.rs_reduce(geo, grads, M, L)
+        for r in range(N):
+            expect = np.array(g["expected_shard"].get(str(r), [g["other_ranks"]] * geo.S),
+                              dtype=np.float32)
+            assert np.array_equal(out[r], expect), (r, out[r], expect)
+        # the single-element form agrees
+        for r in range(N):
+            for x in range(geo.S):
+                val = O.rs_element(geo, M, L, r, x, lambda k, p, idx: grads[k][p][idx])
+                assert val == out[r][x]
+
+
+# ----------------------------------------------------------- reduction pins
+
+def _int_grads(shapes, N, seed):
+    grads = []
+    for r in range(N):
+        row = []
+        for p, s in enumerate(shapes):
+            n = int(np.prod(s)) if len(s) else 1
+            row.append(gen.bf16_values(gen.tensor_key(seed, r, p),
+                                       np.arange(n, dtype=np.uint64), gen.INTEGER))
+        grads.append(row)
+    return grads
+
+
+def _bf16_as_float(bits):
+    """Independent widening for the checks: scale the bf16 fields directly."""
+    bits = np.asarray(bits, dtype=np.int64)
+    sign = np.where(bits >> 15, -1.0, 1.0)
+    exp = (bits >> 7) & 0xFF
+    man = bits & 0x7F
+    normal = sign * (1.0 + man / 128.0) * np.exp2(exp.astype(np.float64) - 127.0)
+    sub = sign * (man / 128.0) * 2.0 ** -126
+    return np.where(exp == 0, sub, normal)
+
+
+def check_exact_integer_sums_bruteforce():
+    """Integer-valued bf16 gradients: every output must be the exact integer sum,
+    whatever the summation order; every padding slot must be +0.0."""
+    for t, (shapes, M, L) in enumerate(_tiny_groups()):
+        N = M * L
+        geo = O.geometry(shapes, N)
+        grads = _int_grads(shapes, N, seed=77 + t)
+        out = O.rs_reduce(geo, grads, M, L)
+        covered = [np.zeros(geo.S, dtype=bool) for _ in range(N)]
+        for p, shape in enumerate(shapes):
+            shape = tuple(shape) or (1,)
+            R = shape[0]
+            K = int(np.prod(shape[1:])) if len(shape) > 1 else 1
+            rp = -(-R // N)
+            total = sum(_bf16_as_float(grads[k][p]) for k in range(N)) if R * K else None
+            for g in range(R):
+                owner = g // rp
+                for k in range(K):
+                    pos = geo.o[p] + (g - owner * rp) * K + k
+                    assert out[owner][pos] == total[g * K + k], (p, g, k)
+                    covered[owner][pos] = True
+        for r in range(N):
+            pad = out[r][~covered[r]]
+            assert (pad.view(np.uint32) == 0).all(), "padding must be +0.0"
+
+
+def check_fp64_error_bound():
+    """Random normal inputs: |oracle - fp64 sum| <= gamma_{(L-1)+(M-1)} * sum|x|."""
+    u = 2.0 ** -24
+    for shapes, M, L in [([(64, 33), (17, 5)], 2, 4), ([(128, 16)], 4, 4), ([(96, 7)], 1, 8),
+                         ([(50, 9)], 3, 3)]:
+        N = M * L
+        geo = O.geometry(shapes, N)
+        grads = [[gen.bf16_values(gen.tensor_key(5, r, p), np.arange(int(np.prod(s)), dtype=np.uint64),
+                                  gen.OUTLIER) for p, s in enumerate(shapes)] for r in range(N)]
+        out = O.rs_reduce(geo, grads, M, L)
+        k = (L - 1) + (M - 1)
+        gamma = k * u / (1 - k * u)
+        for p, s in enumerate(shapes):
+            R, K = s[0], int(np.prod(s[1:]))
+            rp = geo.Rp[p]
+            x = np.stack([_bf16_as_float(grads[r][p]) for r in range(N)])
+            exact = x.sum(axis=0)
+            mag = np.abs(x).sum(axis=0)
+            for g in range(R):
+                owner = g // rp
+                a = geo.o[p] + (g - owner * rp) * K
+                got = out[owner][a:a + K].astype(np.float64)
+                assert (np.abs(got - exact[g * K:(g + 1) * K]) <= gamma * mag[g * K:(g + 1) * K]).all()
+            # and the bound is not vacuous: the result is not just zero
+            assert np.abs(np.concatenate([o for o in out])).max() > 0
+
+
+def check_signed_zero_and_subnormals():
+    """-0.0 inputs sum to +0.0 (accumulators start at +0.0); bf16 subnormals are kept."""
+    N, M, L = 4, 2, 2
+    geo = O.geometry([(4, 2)], N)
+    neg0 = np.full(8, 0x8000, dtype=np.uint16)
+    grads = [[neg0.copy()] for _ in range(N)]
+    tiny = np.uint16(0x0001)            # smallest positive bf16 subnormal, 2^-133
+    grads[0][0][0] = tiny
+    grads[3][0][0] = tiny
+    out = O.rs_reduce(geo, grads, M, L)
+    assert out[0][0] == np.float32(2.0 ** -132)
+    for r in range(N):
+        rest = out[r].view(np.uint32)[1:] if r == 0 else out[r].view(np.uint32)
+        assert (rest == 0).all()
+
+
+# ---------------------------------------------------------------- AG pins
+
+def check_ag_bruteforce():
+    """Every element of every gathered parameter comes from the right rank/offset."""
+    for shapes, M, L in _tiny_groups():
+        N = M * L
+        geo = O.geometry(shapes, N)
+        shards = [np.arange(r * geo.S, (r + 1) * geo.S, dtype=np.int64) for r in range(N)]
+        params = O.ag_place(geo, shards)
+        hits = np.zeros(N * geo.S, dtype=np.int64)
+        for p, shape in enumerate(shapes):
+            shape = tuple(shape) or (1,)
+            K = int(np.prod(shape[1:])) if len(shape) > 1 else 1
+            rp = -(-shape[0] // N)
+            assert params[p].size == N * rp * K
+            for g in range(N * rp):
+                owner = g // rp
+                for k in range(K):
+                    src = owner * geo.S + geo.o[p] + (g - owner * rp) * K + k
+                    assert params[p][g * K + k] == src
+                    hits[src] += 1
+                    y = g * K + k
+                    assert O.ag_element(geo, p, y, lambda r, idx: shards[r][idx]) == src
+        assert (hits == 1).all()
+
+
+def check_ag_of_rs_round_trip():
+    """AG(RS(x)) in fp32 equals the full sum of x on real rows and 0 on padding."""
+    for t, (shapes, M, L) in enumerate(_tiny_groups()):
+        N = M * L
+        geo = O.geometry(shapes, N)
+        grads = _int_grads(shapes, N, seed=300 + t)
+        full = O.ag_place(geo, O.rs_reduce(geo, grads, M, L))
+        for p, shape in enumerate(shapes):
+            shape = tuple(shape) or (1,)
+            n = int(np.prod(shape))
+            total = sum(_bf16_as_float(grads[k][p]) for k in range(N)) if n else np.zeros(0)
+            assert np.array_equal(full[p][:n].astype(np.float64), total)
+            assert (full[p][n:].view(np.uint32) == 0).all()
+
+
+ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]
