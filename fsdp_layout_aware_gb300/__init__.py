@@ -1,0 +1,10 @@
+"""TIDE layout-aware FSDP2 collectives, single-GPU hot path for GB300 (sm_103a).
+
+``tide_rs_reduce`` and ``tide_ag_place`` run in hand-written CUDA kernels in
+``libtide.so`` (C ABI: include/tide.h); this package only binds them.
+"""
+
+from .tide import (  # noqa: F401
+    TideError, TidePlan, tide_ag_place, tide_plan_create, tide_plan_destroy, tide_plan_items, tide_plan_level2_order,
+    tide_plan_param_geometry, tide_plan_shard_elems, tide_rs_reduce, LIB_PATH,
+)

@@ -1,0 +1,239 @@
+// Compute entry points of libtide: device set-up of a plan, the per-call
+// pointer-table upload through an event-guarded pinned ring, and the kernel
+// launches on the caller's stream.
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "tide_internal.h"
+
+using namespace tide;
+
+namespace {
+
+tide_status cuda_fail(cudaError_t err, const char* what) {
+  return fail(err == cudaErrorMemoryAllocation ? TIDE_ERR_OUT_OF_MEMORY : TIDE_ERR_CUDA,
+              std::string(what) + ": " + cudaGetErrorString(err));
+}
+
+#define TIDE_CUDA(call, what)                          \
+  do {                                                 \
+    cudaError_t err_ = (call);                         \
+    if (err_ != cudaSuccess) return cuda_fail(err_, what); \
+  } while (0)
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Bytes of one per-call pointer table: RS needs [P][N] gradient pointers, [N]
+// shard pointers and [P] phase flags; AG needs [N] shard and [P] param pointers.
+size_t rs_table_bytes(const tide_plan* pl) {
+  return align_up((size_t)pl->P * pl->N * 8 + (size_t)pl->N * 8, 16) + align_up((size_t)pl->P, 16);
+}
+size_t ag_table_bytes(const tide_plan* pl) { return (size_t)pl->N * 8 + (size_t)pl->P * 8; }
+
+void release_device_state(tide_plan* pl) {
+  for (auto& s : pl->ring) {
+    if (s.done) {
+      if (s.in_flight) cudaEventSynchronize((cudaEvent_t)s.done);
+      cudaEventDestroy((cudaEvent_t)s.done);
+    }
+    if (s.host) cudaFreeHost(s.host);
+    if (s.dev) cudaFree(s.dev);
+    s = tide_plan::Slot();
+  }
+  if (pl->d_rs_items) cudaFree(pl->d_rs_items);
+  if (pl->d_ag_items) cudaFree(pl->d_ag_items);
+  pl->d_rs_items = nullptr;
+  pl->d_ag_items = nullptr;
+  pl->device = -1;
+}
+
+// First compute call: bind the plan to the current device, upload its work
+// lists and build the pointer-table ring.  Synchronous; allocates.
+tide_status ensure_device(tide_plan* pl) {
+  int dev = -1;
+  TIDE_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (pl->device >= 0) {
+    if (dev != pl->device)
+      return fail(TIDE_ERR_DEVICE_MISMATCH, "plan was set up on device " + std::to_string(pl->device) +
+                                                " but device " + std::to_string(dev) + " is current");
+    return TIDE_OK;
+  }
+  pl->device = dev;
+  tide_status st = TIDE_OK;
+  auto bail = [&](cudaError_t err, const char* what) {
+    st = cuda_fail(err, what);
+    release_device_state(pl);
+    return st;
+  };
+  cudaError_t err = cudaDeviceGetAttribute(&pl->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return bail(err, "cudaDeviceGetAttribute");
+  if (!pl->rs_items.empty()) {
+    const size_t bytes = pl->rs_items.size() * sizeof(RsItem);
+    if ((err = cudaMalloc(&pl->d_rs_items, bytes)) != cudaSuccess) return bail(err, "cudaMalloc(rs items)");
+    if ((err = cudaMemcpy(pl->d_rs_items, pl->rs_items.data(), bytes, cudaMemcpyHostToDevice)) != cudaSuccess)
+      return bail(err, "cudaMemcpy(rs items)");
+  }
+  if (!pl->ag_items.empty()) {
+    const size_t bytes = pl->ag_items.size() * sizeof(AgItem);
+    if ((err = cudaMalloc(&pl->d_ag_items, bytes)) != cudaSuccess) return bail(err, "cudaMalloc(ag items)");
+    if ((err = cudaMemcpy(pl->d_ag_items, pl->ag_items.data(), bytes, cudaMemcpyHostToDevice)) != cudaSuccess)
+      return bail(err, "cudaMemcpy(ag items)");
+  }
+  pl->slot_bytes = align_up(std::max(rs_table_bytes(pl), ag_table_bytes(pl)), 256);
+  for (auto& s : pl->ring) {
+    if ((err = cudaHostAlloc((void**)&s.host, pl->slot_bytes, cudaHostAllocDefault)) != cudaSuccess)
+      return bail(err, "cudaHostAlloc(pointer ring)");
+    if ((err = cudaMalloc((void**)&s.dev, pl->slot_bytes)) != cudaSuccess) return bail(err, "cudaMalloc(pointer ring)");
+    cudaEvent_t ev;
+    if ((err = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess)
+      return bail(err, "cudaEventCreate");
+    s.done = ev;
+  }
+  const int rs_occ = rs_blocks_per_sm(pl->L);
+  const int ag_occ = ag_blocks_per_sm();
+  if (rs_occ <= 0 || ag_occ <= 0) {
+    release_device_state(pl);
+    return fail(TIDE_ERR_CUDA, "occupancy query failed (is this an sm_103 device?)");
+  }
+  pl->rs_grid = (int)std::min<int64_t>((int64_t)pl->num_sms * rs_occ, std::max<int64_t>(1, pl->rs_items.size()));
+  pl->ag_grid = (int)std::min<int64_t>((int64_t)pl->num_sms * ag_occ, std::max<int64_t>(1, pl->ag_items.size()));
+  return TIDE_OK;
+}
+
+// Claim the next ring slot, waiting for the call that used it last.
+tide_status acquire_slot(tide_plan* pl, tide_plan::Slot** out) {
+  tide_plan::Slot& s = pl->ring[pl->next_slot];
+  if (s.in_flight) {
+    TIDE_CUDA(cudaEventSynchronize((cudaEvent_t)s.done), "waiting for a pointer-table slot");
+    s.in_flight = false;
+  }
+  pl->next_slot = (pl->next_slot + 1) % tide_plan::kRing;
+  *out = &s;
+  return TIDE_OK;
+}
+
+tide_status upload_and_mark(tide_plan::Slot* s, size_t bytes, cudaStream_t stream) {
+  TIDE_CUDA(cudaMemcpyAsync(s->dev, s->host, bytes, cudaMemcpyHostToDevice, stream), "pointer-table upload");
+  return TIDE_OK;
+}
+
+tide_status finish(tide_plan::Slot* s, int launch_err, cudaStream_t stream, const char* what) {
+  if (launch_err != cudaSuccess) return cuda_fail((cudaError_t)launch_err, what);
+  TIDE_CUDA(cudaEventRecord((cudaEvent_t)s->done, stream), "cudaEventRecord");
+  s->in_flight = true;
+  return TIDE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void tide_plan_destroy(tide_plan* pl) {
+  if (!pl) return;
+  if (pl->device >= 0) {
+    int cur = -1;
+    const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+    if (!have_cur || cur != pl->device) cudaSetDevice(pl->device);
+    release_device_state(pl);
+    if (have_cur && cur != pl->device) cudaSetDevice(cur);
+  }
+  delete pl;
+}
+
+tide_status tide_rs_reduce(tide_plan* pl, const void* const* grads, float* const* shards, void* stream) {
+  clear_error();
+  if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  if (pl->rs_items.empty()) return TIDE_OK;  // S == 0: nothing to write
+  if (!grads || !shards) return fail(TIDE_ERR_INVALID_ARG, "grads or shards array is NULL");
+  for (int32_t r = 0; r < pl->N; ++r) {
+    if (!shards[r]) return fail(TIDE_ERR_INVALID_ARG, "shards[" + std::to_string(r) + "] is NULL");
+    if ((uintptr_t)shards[r] & 3) return fail(TIDE_ERR_ALIGNMENT, "shard pointer not 4-byte aligned");
+  }
+  for (int32_t p = 0; p < pl->P; ++p) {
+    if (pl->e[p] == 0) continue;
+    for (int32_t r = 0; r < pl->N; ++r) {
+      const void* g = grads[(size_t)r * pl->P + p];
+      if (!g) return fail(TIDE_ERR_INVALID_ARG, "grads[" + std::to_string(r * pl->P + p) + "] is NULL");
+      if ((uintptr_t)g & 1) return fail(TIDE_ERR_ALIGNMENT, "gradient pointer not 2-byte aligned");
+    }
+  }
+  tide_status st = ensure_device(pl);
+  if (st != TIDE_OK) return st;
+  tide_plan::Slot* slot = nullptr;
+  if ((st = acquire_slot(pl, &slot)) != TIDE_OK) return st;
+
+  // Pointer table: [P][N] gradients, [N] shards, [P] phase flags.
+  const size_t n_grad = (size_t)pl->P * pl->N;
+  const uint16_t** gtab = (const uint16_t**)slot->host;
+  float** stab = (float**)(slot->host + n_grad * 8);
+  const size_t flags_at = align_up(n_grad * 8 + (size_t)pl->N * 8, 16);
+  uint8_t* flags = slot->host + flags_at;
+  for (int32_t p = 0; p < pl->P; ++p) {
+    const uintptr_t phase0 = (uintptr_t)grads[p] & 15;
+    uint8_t uniform = 1;
+    for (int32_t r = 0; r < pl->N; ++r) {
+      const void* g = grads[(size_t)r * pl->P + p];
+      gtab[(size_t)p * pl->N + r] = (const uint16_t*)g;
+      if (((uintptr_t)g & 15) != phase0) uniform = 0;
+    }
+    flags[p] = uniform;
+  }
+  for (int32_t r = 0; r < pl->N; ++r) stab[r] = shards[r];
+  const size_t bytes = flags_at + (size_t)pl->P;
+  cudaStream_t s = (cudaStream_t)stream;
+  if ((st = upload_and_mark(slot, bytes, s)) != TIDE_OK) return st;
+
+  RsArgs a;
+  a.items = pl->d_rs_items;
+  a.n_items = (int64_t)pl->rs_items.size();
+  a.grad_tab = (const uint16_t* const*)slot->dev;
+  a.shard_tab = (float* const*)(slot->dev + n_grad * 8);
+  a.uniform_phase = (const uint8_t*)(slot->dev + flags_at);
+  a.N = pl->N;
+  a.M = pl->M;
+  a.L = pl->L;
+  a.P = pl->P;
+  std::memcpy(a.order, pl->order, sizeof(a.order));
+  return finish(slot, launch_rs(a, pl->rs_grid, stream), s, "rs_fused launch");
+}
+
+tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const* params, int32_t elem_bytes,
+                          void* stream) {
+  clear_error();
+  if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  if (elem_bytes != 2 && elem_bytes != 4) return fail(TIDE_ERR_INVALID_ARG, "elem_bytes must be 2 or 4");
+  if (pl->ag_items.empty()) return TIDE_OK;
+  if (!shards || !params) return fail(TIDE_ERR_INVALID_ARG, "shards or params array is NULL");
+  for (int32_t r = 0; r < pl->N; ++r) {
+    if (!shards[r]) return fail(TIDE_ERR_INVALID_ARG, "shards[" + std::to_string(r) + "] is NULL");
+    if ((uintptr_t)shards[r] % elem_bytes) return fail(TIDE_ERR_ALIGNMENT, "shard pointer not element-aligned");
+  }
+  for (int32_t p = 0; p < pl->P; ++p) {
+    if (pl->e[p] == 0) continue;
+    if (!params[p]) return fail(TIDE_ERR_INVALID_ARG, "params[" + std::to_string(p) + "] is NULL");
+    if ((uintptr_t)params[p] % elem_bytes) return fail(TIDE_ERR_ALIGNMENT, "param pointer not element-aligned");
+  }
+  tide_status st = ensure_device(pl);
+  if (st != TIDE_OK) return st;
+  tide_plan::Slot* slot = nullptr;
+  if ((st = acquire_slot(pl, &slot)) != TIDE_OK) return st;
+  const void** stab = (const void**)slot->host;
+  void** ptab = (void**)(slot->host + (size_t)pl->N * 8);
+  for (int32_t r = 0; r < pl->N; ++r) stab[r] = shards[r];
+  for (int32_t p = 0; p < pl->P; ++p) ptab[p] = params[p];
+  cudaStream_t s = (cudaStream_t)stream;
+  if ((st = upload_and_mark(slot, ag_table_bytes(pl), s)) != TIDE_OK) return st;
+
+  AgArgs a;
+  a.items = pl->d_ag_items;
+  a.n_items = (int64_t)pl->ag_items.size();
+  a.shard_tab = (const unsigned char* const*)slot->dev;
+  a.param_tab = (unsigned char* const*)(slot->dev + (size_t)pl->N * 8);
+  a.elem_bytes = elem_bytes;
+  return finish(slot, launch_ag(a, pl->ag_grid, stream), s, "ag_place launch");
+}
+
+}  // extern "C"

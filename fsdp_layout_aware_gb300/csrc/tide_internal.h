@@ -1,0 +1,118 @@
+// Internal definitions shared by the host plan builder and the CUDA kernels of
+// libtide.  Nothing here is part of the public ABI (include/tide.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/tide.h"
+
+namespace tide {
+
+// Largest supported group: ranks and GPUs per NVSwitch domain.
+constexpr int kMaxL = 8;                 // at most eight GPUs per domain
+constexpr int kMaxN = kMaxL * kMaxL;     // M <= L, so N <= 64
+constexpr int kMaxNdim = 8;
+
+// Work-item kinds (RS_VALID / RS_PAD for the reduce-scatter list, AG for the
+// all-gather list).
+enum ItemKind : int16_t { RS_VALID = 0, RS_PAD = 1, AG_COPY = 2 };
+
+// One contiguous range of one (parameter, destination rank) piece.  32 bytes,
+// read once per CTA iteration.
+struct RsItem {
+  int64_t src_off;   // element offset inside every contributor's gradient of p
+  int64_t dst_off;   // element offset inside destination rank r's packed shard
+  int32_t n;         // elements in the range
+  int32_t p;         // parameter
+  int32_t r;         // destination rank
+  int16_t slice;     // level-2 slice of the whole range (ranges never straddle one)
+  int16_t kind;      // RS_VALID or RS_PAD
+};
+static_assert(sizeof(RsItem) == 32, "RsItem layout");
+
+struct AgItem {
+  int64_t src_off;   // element offset inside source rank r's packed shard
+  int64_t dst_off;   // element offset inside parameter p's gathered block
+  int32_t n;
+  int32_t p;
+  int32_t r;
+  int32_t pad_;
+};
+static_assert(sizeof(AgItem) == 32, "AgItem layout");
+
+// Work-list chunking.  A valid RS chunk covers at most kRsChunk elements and
+// starts on a multiple of kRsChunk in contributor-index space, so interior
+// chunks are whole, 16-byte aligned runs of every contributor; padding chunks
+// only write, so they are larger.  AG chunks are kAgChunkBytes of payload.
+constexpr int kRsThreads = 256;
+constexpr int64_t kRsChunk = 8192;
+constexpr int64_t kRsPadChunk = 32768;
+constexpr int kAgThreads = 256;
+constexpr int64_t kAgChunkBytes = 65536;
+
+// Level-2 order table: order[(n_dest * L + s) * M + k] is the k-th source node
+// whose partial is added for slice s of destination node n_dest.
+constexpr int kOrderTableSize = kMaxL * kMaxL * kMaxL;
+
+// Kernel argument blocks (passed by value as __grid_constant__).
+struct RsArgs {
+  const RsItem* items;
+  int64_t n_items;
+  const uint16_t* const* grad_tab;  // [P][N]: contributor src's gradient of p
+  float* const* shard_tab;          // [N]
+  const uint8_t* uniform_phase;     // [P]: 1 if all N gradients of p share addr mod 16
+  int32_t N, M, L, P;
+  uint8_t order[kOrderTableSize];
+};
+
+struct AgArgs {
+  const AgItem* items;
+  int64_t n_items;
+  const unsigned char* const* shard_tab;  // [N]
+  unsigned char* const* param_tab;        // [P]
+  int32_t elem_bytes;
+};
+
+// Launchers (rs_kernel.cu / ag_kernel.cu).  Return the cudaError_t as int.
+int launch_rs(const RsArgs& args, int grid, void* stream);
+int launch_ag(const AgArgs& args, int grid, void* stream);
+// Resident CTAs per SM of each kernel (occupancy), for grid sizing.
+int rs_blocks_per_sm(int L);
+int ag_blocks_per_sm();
+
+}  // namespace tide
+
+// The opaque plan.
+struct tide_plan {
+  int32_t N = 0, M = 0, L = 0, P = 0;
+  std::vector<int64_t> rows, Kp, Rp, e, o;
+  int64_t S = 0;
+  std::vector<tide::RsItem> rs_items;
+  std::vector<tide::AgItem> ag_items;
+  uint8_t order[tide::kOrderTableSize] = {};
+
+  // Device state, created by the first compute call.
+  int device = -1;
+  int num_sms = 0;
+  int rs_grid = 0, ag_grid = 0;
+  tide::RsItem* d_rs_items = nullptr;
+  tide::AgItem* d_ag_items = nullptr;
+  static constexpr int kRing = 8;
+  struct Slot {
+    unsigned char* host = nullptr;
+    unsigned char* dev = nullptr;
+    void* done = nullptr;   // cudaEvent_t
+    bool in_flight = false;
+  } ring[kRing];
+  int next_slot = 0;
+  size_t slot_bytes = 0;
+};
+
+namespace tide {
+// Thread-local error reporting (plan.cpp).
+tide_status fail(tide_status st, const std::string& msg);
+void clear_error();
+}  // namespace tide

@@ -1,0 +1,200 @@
+"""ctypes binding of libtide (include/tide.h): argument marshalling only.
+
+Every step of the hot path runs in the CUDA library; this module turns Python
+shapes, torch tensors and streams into the C ABI's plain integers and
+pointers.  Importing it loads ``libtide.so`` from this package directory and
+raises ``TideError`` if the library is missing -- there is no fallback.
+
+Names match the C entry points:
+    tide_plan_create(shapes, N, M, L) -> plan handle
+    tide_rs_reduce(plan, grads, shards, stream=None)
+    tide_ag_place(plan, shards, params, elem_bytes, stream=None)
+    tide_plan_destroy(plan)
+plus the geometry/work-list queries and the ``TidePlan`` owner object.
+"""
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libtide.so")
+
+TIDE_OK = 0
+STATUS_NAMES = {
+    0: "TIDE_OK", 1: "TIDE_ERR_INVALID_ARG", 2: "TIDE_ERR_ALIGNMENT", 3: "TIDE_ERR_OVERFLOW",
+    4: "TIDE_ERR_OUT_OF_MEMORY", 5: "TIDE_ERR_CUDA", 6: "TIDE_ERR_UNIMPLEMENTED",
+    7: "TIDE_ERR_DEVICE_MISMATCH",
+}
+ITEM_FIELDS = ("kind", "p", "r", "src_off", "dst_off", "n")
+
+
+class TideError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class GroupDesc(ctypes.Structure):
+    _fields_ = [("P", ctypes.c_int32), ("ndim", ctypes.POINTER(ctypes.c_int32)),
+                ("dims", ctypes.POINTER(ctypes.c_int64)), ("N", ctypes.c_int32),
+                ("M", ctypes.c_int32), ("L", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise TideError(-1, f"{LIB_PATH} is missing: build it with "
+                            "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    sig = {
+        "tide_plan_create": (i32, [ctypes.POINTER(GroupDesc), ctypes.POINTER(vp)]),
+        "tide_plan_destroy": (None, [vp]),
+        "tide_plan_shard_elems": (i64, [vp]),
+        "tide_plan_param_geometry": (i32, [vp, i32] + [ctypes.POINTER(i64)] * 4),
+        "tide_plan_num_items": (i64, [vp, i32]),
+        "tide_plan_level2_order": (i32, [vp, i32, i32, ctypes.POINTER(i32)]),
+        "tide_plan_get_items": (i32, [vp, i32, ctypes.POINTER(i64), i64]),
+        "tide_rs_reduce": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
+        "tide_ag_place": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp]),
+        "tide_status_string": (ctypes.c_char_p, [i32]),
+        "tide_last_error": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def _check(status):
+    if status != TIDE_OK:
+        raise TideError(status, _lib.tide_last_error().decode() or
+                        _lib.tide_status_string(status).decode())
+
+
+def _ptr(x):
+    """Device address of a tensor, or an int address, or None -> NULL."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr_array(items):
+    arr = (ctypes.c_void_p * len(items))()
+    for i, x in enumerate(items):
+        arr[i] = _ptr(x)
+    return arr
+
+
+def tide_plan_create(shapes, N, M, L):
+    """Plan for a group of parameters with the given shapes (dim 0 first)."""
+    shapes = [tuple(int(d) for d in s) for s in shapes]
+    ndim = (ctypes.c_int32 * max(1, len(shapes)))(*[len(s) for s in shapes])
+    flat = [d for s in shapes for d in s]
+    dims = (ctypes.c_int64 * max(1, len(flat)))(*flat)
+    desc = GroupDesc(len(shapes), ndim, dims, N, M, L)
+    handle = ctypes.c_void_p()
+    _check(_lib.tide_plan_create(ctypes.byref(desc), ctypes.byref(handle)))
+    return handle.value
+
+
+def tide_plan_destroy(plan):
+    _lib.tide_plan_destroy(plan)
+
+
+def tide_plan_shard_elems(plan):
+    return int(_lib.tide_plan_shard_elems(plan))
+
+
+def tide_plan_param_geometry(plan, p):
+    """(R_p, Rp, Kp, op) of parameter p."""
+    out = [ctypes.c_int64() for _ in range(4)]
+    _check(_lib.tide_plan_param_geometry(plan, p, *[ctypes.byref(o) for o in out]))
+    return tuple(int(o.value) for o in out)
+
+
+def tide_plan_level2_order(plan, n_dest, s, M):
+    """Source nodes of slice s of destination node n_dest, in summation order."""
+    out = (ctypes.c_int32 * M)()
+    _check(_lib.tide_plan_level2_order(plan, n_dest, s, out))
+    return list(out)
+
+
+def tide_plan_items(plan, which):
+    """Work list as a list of dicts (which=0: reduce-scatter, 1: all-gather)."""
+    n = int(_lib.tide_plan_num_items(plan, which))
+    if n < 0:
+        raise TideError(1, "bad plan or list selector")
+    buf = (ctypes.c_int64 * max(1, 6 * n))()
+    _check(_lib.tide_plan_get_items(plan, which, buf, n))
+    return [dict(zip(ITEM_FIELDS, buf[6 * i:6 * i + 6])) for i in range(n)]
+
+
+def tide_rs_reduce(plan, grads, shards, stream=None):
+    """grads: N*P tensors/addresses (entry r*P + p), shards: N fp32 tensors/addresses."""
+    _check(_lib.tide_rs_reduce(plan, _ptr_array(grads), _ptr_array(shards), _stream(stream)))
+
+
+def tide_ag_place(plan, shards, params, elem_bytes, stream=None):
+    """shards: N tensors/addresses of S elements, params: P tensors/addresses."""
+    _check(_lib.tide_ag_place(plan, _ptr_array(shards), _ptr_array(params), elem_bytes, _stream(stream)))
+
+
+class TidePlan:
+    """Owns a plan handle; geometry is read back from the library."""
+
+    def __init__(self, shapes, N, M, L):
+        self.shapes = [tuple(s) for s in shapes]
+        self.N, self.M, self.L = N, M, L
+        self.handle = tide_plan_create(self.shapes, N, M, L)
+        self.S = tide_plan_shard_elems(self.handle)
+        self.P = len(self.shapes)
+        geo = [tide_plan_param_geometry(self.handle, p) for p in range(self.P)]
+        self.rows = [g[0] for g in geo]
+        self.Rp = [g[1] for g in geo]
+        self.Kp = [g[2] for g in geo]
+        self.o = [g[3] for g in geo]
+        self.e = [g[1] * g[2] for g in geo]
+
+    def rs_reduce(self, grads, shards, stream=None):
+        tide_rs_reduce(self.handle, grads, shards, stream)
+
+    def ag_place(self, shards, params, elem_bytes, stream=None):
+        tide_ag_place(self.handle, shards, params, elem_bytes, stream)
+
+    def items(self, which):
+        return tide_plan_items(self.handle, which)
+
+    def level2_order(self, n_dest, s):
+        return tide_plan_level2_order(self.handle, n_dest, s, self.M)
+
+    def close(self):
+        if self.handle:
+            tide_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

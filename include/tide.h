@@ -1,0 +1,180 @@
+/*
+ * tide.h -- C ABI of libtide: the per-element hot path of TIDE's layout-aware
+ * FSDP2 collectives, emulated on one GPU with every rank's buffers resident in
+ * that GPU's memory.
+ *
+ * Sources (three web pages about the TIDE preprint, arXiv 2610.38228):
+ *   [Endgame]  "The Endgame of FSDP Communication: Layout-Aware Collectives on
+ *              Copy Engines, RDMA, and NVSwitch"
+ *   [Richland] "TIDE gives FSDP2 layout-aware zero-copy collectives: up to
+ *              27.1% faster steps on 64 GPUs, zero-SM all-gather, bf16->fp32
+ *              reduce-scatter"
+ *   [Abstract] the preprint's abstract page, its figure captions and tables
+ *
+ * Notation ([Abstract] Table 2): M nodes, L GPUs per NVSwitch domain,
+ * N = M*L ranks, rank r = n*L + l.  For parameter p of shape (R_p, d1, ...):
+ *   Kp = d1*d2*...   (1 for a 1-D tensor; a 0-D tensor counts as [1])
+ *   Rp = ceil(R_p / N), the padded per-rank row count; rank r owns global rows
+ *        [r*Rp, (r+1)*Rp), and rows at or beyond R_p are zero padding
+ *   e_p = Rp*Kp elements per rank ("sp" of Table 2, in elements)
+ *   op  = e_0 + ... + e_{p-1}, the prefix offset inside a packed shard
+ *   S   = sum of e_p, the packed shard length in elements.
+ * The dim-0 chunk-and-pad rule and the gap-free prefix sum are this library's
+ * reading of "sliced, zero-padded" ([Endgame] "What problem is it actually
+ * solving?") and of Table 2's "padded per-rank rows" and "prefix offset".
+ *
+ * Conventions for every call below:
+ *   - All sizes and offsets are in elements unless a name says bytes.
+ *   - Pointer arrays (grads, shards, params) are host arrays of DEVICE
+ *     pointers, read on the host during the call only.  The caller owns every
+ *     tensor; the library never frees or keeps a caller pointer.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Compute calls enqueue work on it and return; a fault inside a
+ *     kernel surfaces on a later synchronisation (as TIDE_ERR_CUDA from the
+ *     next call, or from the caller's own CUDA error check).
+ *   - Errors are status codes; nothing aborts, throws across the ABI or
+ *     exits.  tide_last_error() gives a thread-local message for the last
+ *     failing call.
+ *   - A plan may be used from one host thread at a time.  Its device state
+ *     (work lists, pointer-table ring) is created on the device current at
+ *     the first compute call and that device only; the first compute call
+ *     therefore allocates and synchronises, and should come before any CUDA
+ *     graph capture.  Later calls are stream-ordered and never allocate.
+ *   - Outputs must not overlap inputs or each other.
+ */
+#ifndef TIDE_H
+#define TIDE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tide_status {
+  TIDE_OK = 0,
+  TIDE_ERR_INVALID_ARG = 1,     /* bad descriptor, null pointer, bad index   */
+  TIDE_ERR_ALIGNMENT = 2,       /* pointer not aligned to its element size   */
+  TIDE_ERR_OVERFLOW = 3,        /* a size or offset does not fit in int64    */
+  TIDE_ERR_OUT_OF_MEMORY = 4,   /* host or device allocation failed          */
+  TIDE_ERR_CUDA = 5,            /* a CUDA runtime call failed                */
+  TIDE_ERR_UNIMPLEMENTED = 6,   /* valid request outside what is built       */
+  TIDE_ERR_DEVICE_MISMATCH = 7  /* plan used on another device than its own  */
+} tide_status;
+
+/* A parameter group over N = M*L ranks ([Abstract] Table 2).
+ *   P     number of parameters (>= 0)
+ *   ndim  [P] number of dimensions of each parameter (0..8)
+ *   dims  the P shapes concatenated, dim 0 first; every dim >= 0
+ *   M, L  nodes and GPUs per node: 1 <= L <= 8 (at most eight GPUs per
+ *         NVSwitch domain, [Endgame] "Where I think it falls short"),
+ *         1 <= M <= L (more nodes than GPUs per node needs the batched
+ *         inbox scheme of [Endgame] "Reduce-scatter: two levels of
+ *         addition...", which returns TIDE_ERR_UNIMPLEMENTED)
+ *   N     must equal M*L.
+ * The descriptor is copied; the caller may free it after tide_plan_create. */
+typedef struct tide_group_desc {
+  int32_t P;
+  const int32_t* ndim;
+  const int64_t* dims;
+  int32_t N;
+  int32_t M;
+  int32_t L;
+} tide_group_desc;
+
+typedef struct tide_plan tide_plan;  /* opaque; owned by the library */
+
+/* Build the geometry (Kp, Rp, e_p, op, S) and the per-CTA work lists of a
+ * group.  Host-only: touches no GPU.  On success *out_plan owns host memory
+ * until tide_plan_destroy.  Errors: INVALID_ARG (null pointer, N != M*L,
+ * L or M out of range, negative dim, ndim > 8), UNIMPLEMENTED (M > L),
+ * OVERFLOW (N*S or a shape product beyond int64), OUT_OF_MEMORY. */
+tide_status tide_plan_create(const tide_group_desc* desc, tide_plan** out_plan);
+
+/* Release a plan and its host and device state.  NULL-safe.  Waits for the
+ * plan's in-flight uses (its pointer-table slots) to finish first. */
+void tide_plan_destroy(tide_plan* plan);
+
+/* S, the packed shard length in elements; -1 for a NULL plan. */
+int64_t tide_plan_shard_elems(const tide_plan* plan);
+
+/* Geometry of parameter p: R_p (unpadded dim-0 rows), Rp, Kp and op.
+ * Any output pointer may be NULL.  INVALID_ARG for a bad plan or p. */
+tide_status tide_plan_param_geometry(const tide_plan* plan, int32_t p, int64_t* rows,
+                                     int64_t* Rp, int64_t* Kp, int64_t* op);
+
+/* Work-list introspection for tests.  which = 0: reduce-scatter items,
+ * which = 1: all-gather items.  Each item is 6 int64 values
+ * {kind, p, r, src_off, dst_off, n}:
+ *   RS: kind 0 = reduce valid rows, 1 = zero padding; src_off is the element
+ *       offset inside every contributor's gradient of p, dst_off the offset
+ *       inside rank r's packed shard, n the element count; one level-2 slice.
+ *   AG: kind 2; src_off inside rank r's packed shard, dst_off inside
+ *       parameter p's gathered block.
+ * tide_plan_num_items returns the count (-1 for a bad plan/which);
+ * tide_plan_get_items copies min(cap, count) items to out. */
+int64_t tide_plan_num_items(const tide_plan* plan, int32_t which);
+tide_status tide_plan_get_items(const tide_plan* plan, int32_t which, int64_t* out,
+                                int64_t cap);
+
+/* Level-2 summation order used by tide_rs_reduce for slice s (0 <= s < L)
+ * of destination node n_dest (0 <= n_dest < M): writes the M source node
+ * numbers, in the order their fp32 partials are added, to out[0..M).  The
+ * order is the Latin-square landing order of [Endgame] "Reduce-scatter: two
+ * levels of addition, the last one done by NVSwitch" and [Abstract]
+ * Figure 6(b): destination GPU g = 0..L-1 holds the partial of the source
+ * with relative index c = (s - g) mod L, if c < M.  Errors: INVALID_ARG. */
+tide_status tide_plan_level2_order(const tide_plan* plan, int32_t n_dest, int32_t s, int32_t* out);
+
+/* TIDE-RS: per-parameter bf16 gradients read in place, reduced in fp32
+ * straight into every rank's packed fp32 shard at its final offset
+ * ([Richland] "What shipped"; [Abstract] abstract and Figure 6;
+ * [Endgame] "Reduce-scatter: two levels of addition, the last one done by
+ * NVSwitch").
+ *   grads   host array [N*P] of device pointers; entry r*P + p is rank r's
+ *           bf16 gradient of parameter p, R_p*Kp contiguous row-major
+ *           elements, 2-byte aligned.  May be NULL where R_p*Kp == 0.
+ *   shards  host array [N] of device pointers; shards[r] receives S fp32
+ *           values, 4-byte aligned.  Every element is overwritten.
+ * For destination rank r = n_d*L + l_d and element e < e_p of parameter p,
+ * the result at shards[r][op + e] is, for a real row g = r*Rp + e/Kp < R_p:
+ *   level 1: part_n = fp32 sum over l = 0..L-1 of grads[n*L+l][p][r*e_p + e]
+ *            for every source node n (round-to-nearest-even, from +0.0);
+ *   level 2: the M partials added, from +0.0, in the order of the destination
+ *            GPU g = 0..L-1 they land on under the Latin-square placement:
+ *            slice s = (op+e) / ceil(S/L); GPU g holds the partial of the
+ *            source whose relative index c = (n_d - n) mod M satisfies
+ *            (s - c) mod L == g.
+ * and +0.0 for a padding row.  The result is bit-identical to that order.
+ * Errors: INVALID_ARG (null plan/arrays/pointer), ALIGNMENT, CUDA,
+ * OUT_OF_MEMORY (first call's device set-up), DEVICE_MISMATCH. */
+tide_status tide_rs_reduce(tide_plan* plan, const void* const* grads, float* const* shards,
+                           void* stream);
+
+/* TIDE-AG direct landing: every rank's packed shard piece is written once,
+ * at its final parameter-major address, with no rank-major temporary
+ * ([Endgame] "All-gather: parameters land at their final address";
+ * [Richland] "What shipped"; [Abstract] Figure 1).
+ *   shards      host array [N] of device pointers, S elements each
+ *   params      host array [P] of device pointers; params[p] receives the
+ *               padded gathered block of N*Rp rows x Kp (the parameter proper
+ *               is its first R_p rows).  May be NULL where e_p == 0.
+ *   elem_bytes  2 (bf16 parameters) or 4 (fp32, e.g. to gather RS output)
+ * For every p, r and e < e_p: params[p][r*e_p + e] = shards[r][op + e],
+ * bit for bit.  Pointers must be elem_bytes-aligned.
+ * Errors: INVALID_ARG, ALIGNMENT, CUDA, OUT_OF_MEMORY, DEVICE_MISMATCH. */
+tide_status tide_ag_place(tide_plan* plan, const void* const* shards, void* const* params,
+                          int32_t elem_bytes, void* stream);
+
+/* Static text for a status code. */
+const char* tide_status_string(tide_status status);
+
+/* Thread-local message describing the last failing call on this thread
+ * ("" if none). */
+const char* tide_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TIDE_H */

@@ -28,6 +28,8 @@ host and the GPU round identically):
 fp32 -> bf16 is round-to-nearest-even on the bit pattern (finite inputs only).
 """
 
+import sys
+
 import numpy as np
 
 GAMMA = 0x9E3779B97F4A7C15
@@ -61,8 +63,7 @@ def splitmix64_int(seed, i):
 
 
 def _mix64(z):
-    """Vectorised SplitMix64 finaliser on a uint64 array (wrapping arithmetic)."""
-    z = z.astype(np.uint64, copy=True)
+    """Vectorised SplitMix64 finaliser, in place on a uint64 array (wrapping)."""
     z ^= z >> np.uint64(30)
     z *= np.uint64(MIX1)
     z ^= z >> np.uint64(27)
@@ -73,9 +74,10 @@ def _mix64(z):
 
 def stream_bits(key, idx):
     """64 random bits for each element index in ``idx`` of stream ``key``."""
-    idx = np.asarray(idx, dtype=np.uint64)
-    with np.errstate(over="ignore"):
-        z = np.uint64(key) + (idx + np.uint64(1)) * np.uint64(GAMMA)
+    z = np.array(idx, dtype=np.uint64, copy=True)
+    z += np.uint64(1)
+    z *= np.uint64(GAMMA)
+    z += np.uint64(key)
     return _mix64(z)
 
 
@@ -113,10 +115,13 @@ def bf16_values(key, idx, dist, sigma=1e-3):
         u = (bits >> np.uint64(40)).astype(np.int64) - (1 << 23)
         f = u.astype(np.float32) * np.float32(2.0 ** -23)
     elif dist in (NORMAL, OUTLIER):
-        m16 = np.uint64(0xFFFF)
-        t = ((bits & m16) + ((bits >> np.uint64(16)) & m16)
-             + ((bits >> np.uint64(32)) & m16) + (bits >> np.uint64(48)))
-        t = t.astype(np.int64) - 2 * 65535
+        if sys.byteorder == "little":   # the four 16-bit fields, lowest first
+            t = bits.view(np.uint16).reshape(-1, 4).sum(axis=1, dtype=np.int64)
+        else:
+            m16 = np.uint64(0xFFFF)
+            t = ((bits & m16) + ((bits >> np.uint64(16)) & m16)
+                 + ((bits >> np.uint64(32)) & m16) + (bits >> np.uint64(48))).astype(np.int64)
+        t -= 2 * 65535
         f = t.astype(np.float32) * normal_scale_f32(sigma)
         if dist == OUTLIER:
             o = stream_bits(key ^ OUTLIER_SALT, idx) >> np.uint64(40)

@@ -1,0 +1,185 @@
+"""Host-side checks of libtide that need no GPU.
+
+* the shared library loads and exports every function include/tide.h declares;
+* plan geometry and the level-2 order table equal the oracle's, exactly;
+* the work lists tile every output exactly once, with the right sources;
+* invalid arguments return status codes (no GPU call is reached).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import fsdp_layout_aware_gb300 as tide
+import oracle.tide_oracle as O
+from synth import configs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(tide_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol():
+    names = _declared_functions()
+    assert "tide_rs_reduce" in names and "tide_ag_place" in names and len(names) >= 10
+    lib = ctypes.CDLL(tide.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+GROUPS = [
+    ([(8, 64), (4, 64), (12, 64)], 1, 4),
+    ([(5, 3), (1,), (7, 2, 2), (), (3, 1)], 2, 2),
+    ([(13, 5), (2, 7), (17,), (6, 6)], 2, 3),
+    ([(1, 9), (16, 8), (31, 3), (0, 5)], 4, 4),
+    ([(49, 3), (97, 4095), (1, 1), (48, 1), (47, 1)], 6, 8),
+    ([(100000, 3), (3, 70001)], 3, 5),
+]
+
+
+def _check_plan_against_oracle(shapes, M, L):
+    N = M * L
+    geo = O.geometry(shapes, N)
+    with tide.TidePlan(shapes, N, M, L) as plan:
+        assert plan.S == geo.S
+        assert plan.rows == geo.rows and plan.Rp == geo.Rp and plan.Kp == geo.Kp and plan.o == geo.o
+        for n_dest in range(M):
+            for s in range(L):
+                assert plan.level2_order(n_dest, s) == O.level2_order(s, n_dest, M, L)
+        _check_rs_items(plan, geo, M, L)
+        _check_ag_items(plan, geo)
+
+
+def _check_rs_items(plan, geo, M, L):
+    N = geo.N
+    cover = [bytearray(geo.S) for _ in range(N)]
+    for it in plan.items(0):
+        p, r, n, dst = it["p"], it["r"], it["n"], it["dst_off"]
+        assert n > 0 and geo.o[p] <= dst and dst + n <= geo.o[p] + geo.e[p]
+        e0 = dst - geo.o[p]
+        v = O.valid_elems(geo, p, r)
+        if it["kind"] == 0:
+            assert e0 + n <= v
+            assert it["src_off"] == r * geo.e[p] + e0     # contributors' rows r*Rp...
+            assert O.slice_of(dst, geo.S, L) == O.slice_of(dst + n - 1, geo.S, L)
+        else:
+            assert it["kind"] == 1 and e0 >= v
+        for x in range(dst, dst + n):
+            cover[r][x] += 1
+    for r in range(N):
+        assert all(c == 1 for c in cover[r]), f"rank {r}: RS items must tile the shard exactly once"
+
+
+def _check_ag_items(plan, geo):
+    N = geo.N
+    hits = bytearray(N * geo.S)
+    for it in plan.items(1):
+        p, r, n = it["p"], it["r"], it["n"]
+        e0 = it["dst_off"] - r * geo.e[p]
+        assert 0 <= e0 and e0 + n <= geo.e[p]
+        assert it["src_off"] == geo.o[p] + e0
+        base = O.param_major_offset(geo, p, r) + e0
+        for y in range(base, base + n):
+            hits[y] += 1
+    assert all(h == 1 for h in hits), "AG items must tile the gathered group exactly once"
+
+
+@pytest.mark.parametrize("shapes,M,L", GROUPS)
+def test_plan_matches_oracle(shapes, M, L):
+    _check_plan_against_oracle(shapes, M, L)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_workload_geometry_matches_oracle(cfg):
+    w = configs.get(cfg)
+    geo = O.geometry(w.shapes, w.N)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        assert (plan.S, plan.Rp, plan.Kp, plan.o) == (geo.S, geo.Rp, geo.Kp, geo.o)
+        for n_dest in range(w.M):
+            for s in range(w.L):
+                assert plan.level2_order(n_dest, s) == O.level2_order(s, n_dest, w.M, w.L)
+        items = plan.items(0)
+        # per destination rank, item lengths add up to the shard
+        per_rank = [0] * w.N
+        for it in items:
+            per_rank[it["r"]] += it["n"]
+        assert per_rank == [geo.S] * w.N
+        if cfg == 1:
+            _check_rs_items(plan, geo, w.M, w.L)
+            _check_ag_items(plan, geo)
+
+
+def test_all_level2_orders_small_groups():
+    for L in range(1, 9):
+        for M in range(1, L + 1):
+            with tide.TidePlan([(2 * M * L, 3)], M * L, M, L) as plan:
+                for n_dest in range(M):
+                    for s in range(L):
+                        assert plan.level2_order(n_dest, s) == O.level2_order(s, n_dest, M, L)
+
+
+@pytest.mark.parametrize("shapes,N,M,L,status", [
+    ([(4, 4)], 4, 2, 3, 1),      # N != M*L
+    ([(4, 4)], 18, 2, 9, 1),     # L > 8
+    ([(4, 4)], 0, 0, 4, 1),      # M < 1
+    ([(4, 4)], 8, 4, 2, 6),      # M > L: batched inboxes not built
+    ([(-1, 4)], 4, 1, 4, 1),     # negative dim
+    ([(1,) * 9], 4, 1, 4, 1),    # ndim > 8
+    ([(4, 1 << 40, 1 << 40)], 4, 1, 4, 3),   # row length overflow
+])
+def test_plan_create_rejects(shapes, N, M, L, status):
+    with pytest.raises(tide.TideError) as err:
+        tide.tide_plan_create(shapes, N, M, L)
+    assert err.value.status == status
+
+
+def test_empty_group_is_a_no_op():
+    with tide.TidePlan([], 4, 1, 4) as plan:
+        assert plan.S == 0 and plan.items(0) == [] and plan.items(1) == []
+        plan.rs_reduce([], [None] * 4, stream=0)        # nothing to do: OK without a GPU
+        plan.ag_place([None] * 4, [], 2, stream=0)
+    with tide.TidePlan([(0, 7), (0,)], 8, 1, 8) as plan:
+        assert plan.S == 0
+        plan.rs_reduce([None] * 16, [None] * 8, stream=0)
+
+
+def test_call_argument_errors_need_no_gpu():
+    with tide.TidePlan([(8, 64), (4, 64), (12, 64)], 4, 1, 4) as plan:
+        good = [0x10000 * (i + 1) for i in range(12)]
+        shards = [0x1000000 * (r + 1) for r in range(4)]
+        cases = [
+            (lambda: plan.rs_reduce(good, shards[:3] + [None], stream=0), 1),
+            (lambda: plan.rs_reduce(good[:5] + [None] + good[6:], shards, stream=0), 1),
+            (lambda: plan.rs_reduce(good[:5] + [good[5] + 1] + good[6:], shards, stream=0), 2),
+            (lambda: plan.rs_reduce(good, [shards[0] + 2] + shards[1:], stream=0), 2),
+            (lambda: plan.ag_place(shards, good[:3], 3, stream=0), 1),
+            (lambda: plan.ag_place(shards, [good[0] + 2] + good[1:3], 4, stream=0), 2),
+            (lambda: plan.ag_place([shards[0] + 1] + shards[1:], good[:3], 2, stream=0), 2),
+            (lambda: plan.ag_place(shards, [None] + good[1:3], 2, stream=0), 1),
+        ]
+        for fn, status in cases:
+            with pytest.raises(tide.TideError) as err:
+                fn()
+            assert err.value.status == status
+    with pytest.raises(tide.TideError) as err:
+        tide.tide_rs_reduce(None, [], [], 0)
+    assert err.value.status == 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device error path")
+def test_cuda_failure_is_a_status_without_a_gpu():
+    with tide.TidePlan([(8, 64)], 4, 1, 4) as plan:
+        with pytest.raises(tide.TideError) as err:
+            plan.rs_reduce([0x10000 * (i + 1) for i in range(4)], [0x1000000 * (r + 1) for r in range(4)], stream=0)
+        assert err.value.status == 5

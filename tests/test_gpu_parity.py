@@ -1,0 +1,305 @@
+"""GPU parity: libtide's CUDA kernels against the CPU oracle, element by element.
+
+Bit-exact for the all-gather (a copy) and for the reduce-scatter (the kernel
+adds in the oracle's order: l = 0..L-1, then Latin-square landing order).
+Small cases compare every output; the full-size workloads compare sampled
+outputs against the oracle computed one element at a time from the host
+generator, plus properties that hold at any size.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import fsdp_layout_aware_gb300 as tide
+import oracle.tide_oracle as O
+from synth import configs, gen
+
+from gpu_common import (DEV, device_ag_shards, device_grads, f32_bits, f32_guarded, host_grads, oracle_rs,
+                        run_rs, to_dev_u16, u16_of)
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 37  # sentinel elements before and after every output buffer
+
+
+def _small_workloads():
+    """Cases the oracle finishes in seconds: several items and CTAs, ragged tails,
+    padding, every level-2 layout (M = 1, 2, 8, 6) and odd row lengths."""
+    ws = [configs.get(1)]
+    ws.append(configs.scaled(configs.get(2), row_div=512, name="llama70b_rows/512"))
+    q = configs.get(3)
+    q.shapes = q.shapes[:5] + q.shapes[5:5 + 3 * 4] + q.shapes[-2:]
+    q.dists = q.dists[:len(q.shapes)]
+    ws.append(configs.scaled(q, row_div=32, name="qwen3moe_4experts_rows/32"))
+    ws.append(configs.scaled(configs.get(4), row_div=1024, name="wan22dit_rows/1024"))
+    u = configs.get(5)
+    shapes = [(min(r, 49), c) for r, c in u.shapes[:12]]
+    for r, c in u.shapes[12::12]:
+        c2 = min(c, 515)
+        if c % 2 and not c2 % 2:
+            c2 -= 1
+        shapes.append((min(r, 150), c2))
+    ws.append(configs.Workload("uneven_subset", u.N, u.M, u.L, shapes,
+                               [gen.UNIFORM if p % 2 == 0 else gen.INTEGER for p in range(len(shapes))],
+                               seed=u.seed))
+    ws.append(configs.Workload("ragged_mix", 12, 3, 4,
+                               [(5, 3), (1,), (7, 2, 2), (), (3, 1), (13, 5), (2, 7), (17,), (100, 33), (0, 4)],
+                               [gen.OUTLIER] * 10, seed=99))
+    ws.append(configs.Workload("single_rank", 1, 1, 1, [(37, 129), (5,)], [gen.UNIFORM] * 2, seed=7))
+    return ws
+
+
+SMALL = _small_workloads()
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_rs_small_bit_exact(w):
+    grads = host_grads(w)
+    geo, expect = oracle_rs(w, grads)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        assert plan.S == geo.S
+        dev = [[to_dev_u16(grads[r][p])[0] for p in range(w.P)] for r in range(w.N)]
+        outs = [f32_guarded(geo.S, GUARD, GUARD) for _ in range(w.N)]
+        run_rs(plan, dev, [o[0] for o in outs])
+        torch.cuda.synchronize()
+        for r in range(w.N):
+            got = f32_bits(outs[r][0])
+            want = expect[r].view(np.uint32)
+            bad = np.nonzero(got != want)[0]
+            assert bad.size == 0, f"rank {r}: {bad.size} mismatches, first at {bad[:5]}"
+            guards = f32_bits(outs[r][1])
+            assert (guards[:GUARD] == 0x7FC00000).all() and (guards[GUARD + geo.S:] == 0x7FC00000).all()
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+@pytest.mark.parametrize("elem_bytes", [2, 4])
+def test_ag_small_bit_exact(w, elem_bytes):
+    geo = O.geometry(w.shapes, w.N)
+    rng = np.random.default_rng(11)
+    dt = np.uint16 if elem_bytes == 2 else np.uint32
+    shards_h = [rng.integers(0, np.iinfo(dt).max, geo.S, dtype=dt) for _ in range(w.N)]
+    expect = O.ag_place(geo, shards_h)
+    tdt = torch.int16 if elem_bytes == 2 else torch.int32
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        shards = [torch.from_numpy(s.view(np.int16 if elem_bytes == 2 else np.int32)).to(DEV) for s in shards_h]
+        backs = [torch.full((GUARD + w.N * geo.e[p] + GUARD,), -7, dtype=tdt, device=DEV) for p in range(w.P)]
+        params = [b[GUARD:GUARD + w.N * geo.e[p]] for p, b in enumerate(backs)]
+        plan.ag_place(shards, params, elem_bytes)
+        torch.cuda.synchronize()
+        for p in range(w.P):
+            got = params[p].cpu().numpy().view(dt)
+            assert np.array_equal(got, expect[p]), f"param {p}"
+            g = backs[p].cpu().numpy()
+            assert (g[:GUARD] == -7).all() and (g[GUARD + w.N * geo.e[p]:] == -7).all()
+
+
+def test_rs_then_ag_round_trip_fp32():
+    w = SMALL[5]   # ragged mix
+    grads = host_grads(w)
+    geo, shards_o = oracle_rs(w, grads)
+    expect = O.ag_place(geo, shards_o)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        dev = [[to_dev_u16(grads[r][p])[0] for p in range(w.P)] for r in range(w.N)]
+        shards = [torch.empty(geo.S, dtype=torch.float32, device=DEV) for _ in range(w.N)]
+        run_rs(plan, dev, shards)
+        params = [torch.empty(w.N * geo.e[p], dtype=torch.float32, device=DEV) for p in range(w.P)]
+        plan.ag_place(shards, params, 4)
+        torch.cuda.synchronize()
+        for p in range(w.P):
+            assert np.array_equal(params[p].cpu().numpy().view(np.uint32), expect[p].view(np.uint32))
+
+
+@pytest.mark.parametrize("grad_shift,shard_shift", [((0, 0, 0, 0), 0), ((3, 3, 3, 3), 1), ((1, 5, 2, 7), 3),
+                                                    ((6, 6, 6, 6), 2), ((0, 1, 0, 1), 0)])
+def test_rs_misaligned_pointers(grad_shift, shard_shift):
+    """Gradients at element offsets 0..7 from 16-byte boundaries (equal or
+    unequal across ranks) and shards at 4-byte but not 16-byte alignment."""
+    w = configs.Workload("misaligned", 4, 2, 2, [(41, 37), (9,), (20, 64), (3, 1001)], [gen.UNIFORM] * 4, seed=5)
+    grads = host_grads(w)
+    geo, expect = oracle_rs(w, grads)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        keep = []
+        dev = []
+        for r in range(w.N):
+            row = []
+            for p in range(w.P):
+                view, back = to_dev_u16(grads[r][p], pad_before=grad_shift[r], pad_after=8)
+                keep.append(back)
+                row.append(view)
+            dev.append(row)
+        outs = [f32_guarded(geo.S, shard_shift, 4) for _ in range(w.N)]
+        run_rs(plan, dev, [o[0] for o in outs])
+        torch.cuda.synchronize()
+        for r in range(w.N):
+            assert np.array_equal(f32_bits(outs[r][0]), expect[r].view(np.uint32))
+
+
+@pytest.mark.parametrize("src_shift,dst_shift,elem_bytes", [(0, 1, 2), (3, 0, 2), (5, 2, 2), (1, 3, 4), (2, 2, 4),
+                                                            (7, 7, 2)])
+def test_ag_misaligned_pointers(src_shift, dst_shift, elem_bytes):
+    w = configs.Workload("misaligned_ag", 6, 2, 3, [(41, 37), (9,), (20, 64), (3, 1001), (127, 3)],
+                         [gen.UNIFORM] * 5, seed=5)
+    geo = O.geometry(w.shapes, w.N)
+    dt = np.uint16 if elem_bytes == 2 else np.uint32
+    tdt = torch.int16 if elem_bytes == 2 else torch.int32
+    npdt = np.int16 if elem_bytes == 2 else np.int32
+    rng = np.random.default_rng(3)
+    shards_h = [rng.integers(0, np.iinfo(dt).max, geo.S, dtype=dt) for _ in range(w.N)]
+    expect = O.ag_place(geo, shards_h)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        sb = [torch.zeros(src_shift + geo.S + 8, dtype=tdt, device=DEV) for _ in range(w.N)]
+        for r in range(w.N):
+            sb[r][src_shift:src_shift + geo.S].copy_(torch.from_numpy(shards_h[r].view(npdt)))
+        pb = [torch.full((dst_shift + w.N * geo.e[p] + 8,), -3, dtype=tdt, device=DEV) for p in range(w.P)]
+        plan.ag_place([b[src_shift:src_shift + geo.S] for b in sb],
+                      [b[dst_shift:dst_shift + w.N * geo.e[p]] for p, b in enumerate(pb)], elem_bytes)
+        torch.cuda.synchronize()
+        for p in range(w.P):
+            got = pb[p].cpu().numpy()
+            assert np.array_equal(got[dst_shift:dst_shift + w.N * geo.e[p]].view(dt), expect[p])
+            assert (got[:dst_shift] == -3).all() and (got[dst_shift + w.N * geo.e[p]:] == -3).all()
+
+
+def test_rs_edge_values():
+    """-0.0 everywhere (result +0.0), bf16 subnormals, and sums that overflow to inf."""
+    w = configs.Workload("edges", 8, 2, 4, [(16, 24)], [gen.UNIFORM], seed=1)
+    N = w.N
+    n = 16 * 24
+    grads = [[np.full(n, 0x8000, dtype=np.uint16)] for _ in range(N)]
+    for r in range(N):
+        grads[r][0][0:24] = 0x0001 + r            # subnormals
+        grads[r][0][24:48] = 0x7F7F               # bf16 max: the sum overflows to +inf
+        grads[r][0][48:72] = 0xFF7F if r % 2 else 0x7F7F   # +max/-max alternating
+    geo, expect = oracle_rs(w, grads)
+    with tide.TidePlan(w.shapes, N, w.M, w.L) as plan:
+        dev = [[to_dev_u16(grads[r][0])[0]] for r in range(N)]
+        shards = [torch.empty(geo.S, dtype=torch.float32, device=DEV) for _ in range(N)]
+        run_rs(plan, dev, shards)
+        torch.cuda.synchronize()
+        for r in range(N):
+            assert np.array_equal(f32_bits(shards[r]), expect[r].view(np.uint32))
+
+
+def test_rs_repeat_calls_on_a_side_stream():
+    """More calls than ring slots, queued without host syncs, on a side stream:
+    every call must use its own pointer table."""
+    w = SMALL[5]
+    geo = O.geometry(w.shapes, w.N)
+    s = torch.cuda.Stream()
+    sets = []
+    for k in range(11):
+        ww = configs.Workload(w.name, w.N, w.M, w.L, w.shapes, w.dists, seed=1000 + k)
+        grads = host_grads(ww)
+        sets.append((grads, oracle_rs(ww, grads)[1]))
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        devs = [[[to_dev_u16(g[r][p])[0] for p in range(w.P)] for r in range(w.N)] for g, _ in sets]
+        outs = [[torch.empty(geo.S, dtype=torch.float32, device=DEV) for _ in range(w.N)] for _ in sets]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            for k in range(len(sets)):
+                run_rs(plan, devs[k], outs[k], stream=s)
+        s.synchronize()
+        for k, (_, expect) in enumerate(sets):
+            for r in range(w.N):
+                assert np.array_equal(f32_bits(outs[k][r]), expect[r].view(np.uint32)), (k, r)
+
+
+def test_rs_deterministic():
+    w = SMALL[2]
+    grads = host_grads(w)
+    geo = O.geometry(w.shapes, w.N)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        dev = [[to_dev_u16(grads[r][p])[0] for p in range(w.P)] for r in range(w.N)]
+        a = [torch.empty(geo.S, dtype=torch.float32, device=DEV) for _ in range(w.N)]
+        b = [torch.empty(geo.S, dtype=torch.float32, device=DEV) for _ in range(w.N)]
+        run_rs(plan, dev, a)
+        run_rs(plan, dev, b)
+        torch.cuda.synchronize()
+        assert all(torch.equal(x.view(torch.int32), y.view(torch.int32)) for x, y in zip(a, b))
+
+
+def test_device_generator_matches_host():
+    from synth import device
+    for dist in (gen.UNIFORM, gen.NORMAL, gen.OUTLIER, gen.INTEGER):
+        key = gen.tensor_key(1238, 5, 3)
+        t = torch.empty(100003, dtype=torch.int16, device=DEV)
+        device.fill_bf16(t, key, dist, 1e-3, idx0=12345)
+        want = gen.bf16_values(key, np.arange(12345, 12345 + 100003, dtype=np.uint64), dist, 1e-3)
+        assert np.array_equal(u16_of(t), want), dist
+
+
+# ------------------------------------------------------------ full size
+
+def _sample_positions(rng, geo, N, count):
+    r = rng.integers(0, N, count)
+    x = rng.integers(0, max(1, geo.S), count)
+    # always include both ends of every rank's shard and every parameter start
+    extra = [(rr, 0) for rr in range(N)] + [(rr, geo.S - 1) for rr in range(N)]
+    extra += [(int(rng.integers(0, N)), o) for o in geo.o if o < geo.S]
+    return list(zip(r.tolist(), x.tolist())) + extra
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+def test_full_size_rs_ag_sampled(cfg):
+    """The bench's workloads at full size, through the same plan and launches:
+    sampled outputs against the oracle, and whole-output properties."""
+    w = configs.get(cfg)
+    geo = O.geometry(w.shapes, w.N)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        grads = device_grads(w)
+        shards = [torch.empty(geo.S, dtype=torch.float32, device=DEV) for _ in range(w.N)]
+        run_rs(plan, grads, shards)
+        ag_in = device_ag_shards(w, geo.S)
+        params = [torch.empty(w.N * geo.e[p], dtype=torch.int16, device=DEV) for p in range(w.P)]
+        plan.ag_place(ag_in, params, 2)
+        torch.cuda.synchronize()
+
+        rng = np.random.default_rng(cfg)
+        samples = _sample_positions(rng, geo, w.N, 1500)
+
+        def grad_at(src, p, idx):
+            return w.grad_values(src, p, idx.astype(np.uint64))
+
+        for r, x in samples:
+            want = O.rs_element(geo, w.M, w.L, r, x, grad_at)
+            got = shards[r][x].item()
+            assert np.float32(got).view(np.uint32) == np.float32(want).view(np.uint32), (r, x, got, want)
+
+        # AG sampled against the oracle from the host generator
+        for _ in range(1500):
+            p = int(rng.integers(0, w.P))
+            if geo.e[p] == 0:
+                continue
+            y = int(rng.integers(0, w.N * geo.e[p]))
+            want = O.ag_element(geo, p, y, lambda rr, idx: w.ag_values(rr, idx.astype(np.uint64)))
+            assert np.uint16(params[p][y].item() & 0xFFFF) == want
+
+        # whole-output properties: AG pieces equal their shard slices; padding is +0.0;
+        # integer-valued parameters reduce to their exact sum; the rest meet the
+        # two-level fp32 error bound against an fp64 sum.
+        u = 2.0 ** -24
+        k = (w.L - 1) + (w.M - 1)
+        gamma = k * u / (1 - k * u)
+        for p in range(w.P):
+            e_p, o_p = geo.e[p], geo.o[p]
+            if e_p == 0:
+                continue
+            for r in range(w.N):
+                assert torch.equal(params[p][r * e_p:(r + 1) * e_p], ag_in[r][o_p:o_p + e_p])
+            n = w.numel(p)
+            exact = torch.zeros(n, dtype=torch.float64, device=DEV)
+            mag = torch.zeros(n, dtype=torch.float64, device=DEV)
+            for src in range(w.N):
+                x = grads[src][p].view(torch.bfloat16).double()
+                exact += x
+                mag += x.abs()
+            got = torch.cat([shards[r][o_p:o_p + e_p] for r in range(w.N)])
+            assert (got[n:].view(torch.int32) == 0).all(), f"padding of param {p} not +0.0"
+            got = got[:n].double()
+            if w.dists[p] == gen.INTEGER:
+                assert torch.equal(got, exact), f"param {p}: integer sums must be exact"
+            else:
+                assert ((got - exact).abs() <= gamma * mag).all(), f"param {p}: error bound"
+        del grads, shards, ag_in, params
+    torch.cuda.empty_cache()
