@@ -1,0 +1,453 @@
+#!/usr/bin/env python
+"""Benchmark of the TIDE single-GPU hot path.
+
+One step = tide_rs_reduce (bf16 gradients of all N emulated ranks -> N packed
+fp32 shards) + tide_ag_place (N packed bf16 shards -> P parameter-major
+blocks) over one synthetic parameter group, everything resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama70b]
+    python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Prints one JSON line.  `value` is the effective HBM bandwidth of the step in
+GB/s of algorithmic bytes: reduce-scatter 2*N*G (every contributor's real bf16
+element read once) + 4*N*S (every fp32 shard element written once), all-gather
+2*2*N*S (every bf16 piece read once and written once).  Under torchrun each
+rank runs its own replica on its own GPU (no data-path collective), `value`
+sums all ranks' bytes over the slowest rank's time.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from datetime import datetime
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "RS/AG effective HBM GB/s and % of GB300 HBM peak (1 GPU); elements/s"
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_WORKLOAD = "llama70b"
+CLOCK_QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+               "clocks_event_reasons.sw_power_cap")
+REASON_NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    help="llama70b (default), qwen3moe, wan22dit, uneven or tiny")
+    ap.add_argument("--row-div", type=int, default=1,
+                    help="divide every parameter's rows (a smaller case of the same layer, for profiling)")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget of cpu_baseline")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- plumbing
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(local_seconds, local_units, world, device="cpu"):
+    """(max seconds over ranks, summed units over ranks)."""
+    if world == 1:
+        return local_seconds, local_units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=device)
+    u = torch.tensor([local_units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def algorithmic_bytes(w, geo):
+    """RS: 2*N*G + 4*N*S; AG (bf16): 2*2*N*S.  Also the element counts."""
+    G = w.total_grad_elems()
+    N, S = w.N, geo.S
+    return {"rs_bytes": 2 * N * G + 4 * N * S, "ag_bytes": 4 * N * S,
+            "rs_elems": N * G, "ag_elems": N * S, "G": G, "S": S}
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest(name):
+    path = os.path.join(ROOT, "fsdp_layout_aware_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def profiled_traffic(summary_name, kernel_file):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source
+    it was taken on is the current one; otherwise None."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith(" "):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("kernel_source_sha256") != kernel_source_digest(kernel_file):
+            return None
+        return float(fields["dram_bytes_per_full_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + CLOCK_QUERY, "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.gpu_index)], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) != 9:
+                    continue
+                try:
+                    ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 <= r[0] <= t1] or rows
+        if not inside:
+            return None
+        reasons = sorted({REASON_NAMES[i] for r in inside for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def get_workload(args):
+    from synth import configs
+    w = configs.get(args.workload)
+    if args.row_div > 1:
+        w = configs.scaled(w, row_div=args.row_div, name=f"{w.name}_rows{args.row_div}")
+    return w
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import fsdp_layout_aware_gb300 as tide
+    from synth import configs, device, gen
+
+    torch.cuda.set_device(local_rank)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local_rank)
+    w = get_workload(args)
+    plan = tide.TidePlan(w.shapes, w.N, w.M, w.L)
+    geo = plan
+    nbytes = algorithmic_bytes(w, geo)
+    S = plan.S
+    stream = torch.cuda.Stream(device=dev)
+
+    # Inputs resident in HBM before timing: every rank's bf16 gradients and
+    # bf16 packed parameter shards, from the seeded generator.
+    with torch.cuda.stream(stream):
+        grads = []
+        for r in range(w.N):
+            for p in range(w.P):
+                t = torch.empty(w.numel(p), dtype=torch.int16, device=dev)
+                device.fill_bf16(t, w.grad_key(r, p), w.dists[p], w.sigma, stream=stream)
+                grads.append(t)
+        rs_out = [torch.empty(S, dtype=torch.float32, device=dev) for _ in range(w.N)]
+        ag_in = []
+        for r in range(w.N):
+            t = torch.empty(S, dtype=torch.int16, device=dev)
+            device.fill_bf16(t, w.ag_key(r), gen.UNIFORM, stream=stream)
+            ag_in.append(t)
+        ag_out = [torch.empty(w.N * plan.e[p], dtype=torch.int16, device=dev) for p in range(w.P)]
+    stream.synchronize()
+
+    def step():
+        plan.rs_reduce(grads, rs_out, stream)
+        plan.ag_place(ag_in, ag_out, 2, stream)
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank).start() if rank == 0 else None
+    if sampler:
+        time.sleep(0.4)   # let nvidia-smi come up before the timed region
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        plan.rs_reduce(grads, rs_out, stream)
+        ev[k][1].record(stream)
+        plan.ag_place(ag_in, ag_out, 2, stream)
+        ev[k][2].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    clocks = sampler.stop(t_wall0, t_wall1) if sampler else None
+
+    local_s = start.elapsed_time(stop) / 1e3
+    rs_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    ag_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    step_bytes = nbytes["rs_bytes"] + nbytes["ag_bytes"]
+    max_s, total_bytes = aggregate(local_s, float(step_bytes * K), world, device=dev)
+    _, total_elems = aggregate(local_s, float((nbytes["rs_elems"] + nbytes["ag_elems"]) * K), world, device=dev)
+
+    e2e = None if args.no_e2e else run_e2e(args, plan, w, nbytes, grads, rs_out, ag_in, ag_out, stream, world, dev)
+
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_hbm_peak()
+    value = total_bytes / max_s / 1e9
+    rs_avg = statistics.mean(rs_ms) / 1e3
+    ag_avg = statistics.mean(ag_ms) / 1e3
+    rs_gbs = nbytes["rs_bytes"] / rs_avg / 1e9
+    ag_gbs = nbytes["ag_bytes"] / ag_avg / 1e9
+    traffic = profiled_traffic(f"rs_fused_{w.name}.txt", "rs_kernel.cu")
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(max_s / K * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded SplitMix64 bf16; shapes of the named layer)",
+        "config": {"workload": f"{w.name}: {w.notes}", "N": w.N, "M": w.M, "L": w.L, "P": w.P,
+                   "G_elems": nbytes["G"], "S_elems": S, "rs_bytes_per_step": nbytes["rs_bytes"],
+                   "ag_bytes_per_step": nbytes["ag_bytes"],
+                   "l2": "no flush: %.1f GB of inputs per step >> 129 MB L2" % (step_bytes / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_of_hbm_peak": round(100 * value / peak, 2),
+        "elements_per_s": round(total_elems / max_s, 1),
+        "rs": {"ms": round(rs_avg * 1e3, 4), "GB_s": round(rs_gbs, 2), "frac": round(rs_gbs / peak, 4),
+               "elements_per_s": round(nbytes["rs_elems"] / rs_avg, 1)},
+        "ag": {"ms": round(ag_avg * 1e3, 4), "GB_s": round(ag_gbs, 2), "frac": round(ag_gbs / peak, 4),
+               "elements_per_s": round(nbytes["ag_elems"] / ag_avg, 1)},
+        "roofline": {"kernel": "rs_fused", "bound": "hbm", "achieved": round(rs_gbs, 2), "peak": peak,
+                     "peak_source": peak_kind, "unit": "GB/s", "frac": round(rs_gbs / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": nbytes["rs_bytes"]},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(configs.get(args.workload), args.cpu_seconds)
+    return line
+
+
+def run_e2e(args, plan, w, nbytes, grads, rs_out, ag_in, ag_out, stream, world, dev):
+    """Same step through the public API with inputs in pinned host memory:
+    every step copies all gradients and shards in and all outputs back."""
+    import torch
+    h_grads = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in grads]
+    h_ag_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ag_in]
+    h_rs_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in rs_out]
+    h_ag_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ag_out]
+    with torch.cuda.stream(stream):
+        for h, d in zip(h_grads + h_ag_in, grads + ag_in):
+            h.copy_(d, non_blocking=True)
+    stream.synchronize()
+    h2d = sum(t.numel() * t.element_size() for t in h_grads + h_ag_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_rs_out + h_ag_out)
+
+    def step():
+        with torch.cuda.stream(stream):
+            for d, h in zip(grads + ag_in, h_grads + h_ag_in):
+                d.copy_(h, non_blocking=True)
+            plan.rs_reduce(grads, rs_out, stream)
+            plan.ag_place(ag_in, ag_out, 2, stream)
+            for h, d in zip(h_rs_out + h_ag_out, rs_out + ag_out):
+                h.copy_(d, non_blocking=True)
+
+    step()
+    stream.synchronize()
+    K = max(1, args.e2e_steps)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(K):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    sec = a.elapsed_time(b) / 1e3
+    max_s, tot = aggregate(sec, float((nbytes["rs_bytes"] + nbytes["ag_bytes"]) * K), world, device=dev)
+    return {"value": round(tot / max_s / 1e9, 3), "unit": "GB/s", "steps": K,
+            "ms_per_step": round(max_s / K * 1e3, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample(workload_name, row_div):
+    """A row subset of the workload (same row lengths, N, M, L) for CPU timing."""
+    import numpy as np
+    import oracle.tide_oracle as O
+    from synth import configs, gen
+    w = configs.scaled(configs.get(workload_name), row_div=row_div)
+    grads = [[gen.bf16_tensor(w.grad_key(r, p), w.numel(p), w.dists[p], w.sigma) for p in range(w.P)]
+             for r in range(w.N)]
+    geo = O.geometry(w.shapes, w.N)
+    ag_in = [gen.bf16_values(w.ag_key(r), np.arange(geo.S, dtype=np.uint64), gen.UNIFORM) for r in range(w.N)]
+    return w, geo, grads, ag_in
+
+
+def oracle_step(w, geo, grads, ag_in):
+    import oracle.tide_oracle as O
+    O.rs_reduce(geo, grads, w.M, w.L)
+    O.ag_place(geo, ag_in)
+
+
+SAMPLE_ROW_DIV = {"llama70b": 64, "qwen3moe": 16, "wan22dit": 64, "uneven": 8, "tiny": 1}
+
+
+def cpu_baseline(w, seconds):
+    """The oracle as it stands, single-threaded, over repeated passes of a row
+    subset of the same workload until `seconds` of CPU time are spent."""
+    div = SAMPLE_ROW_DIV.get(w.name, 16)
+    ws, geo, grads, ag_in = oracle_sample(w.name, div)
+    nb = algorithmic_bytes(ws, geo)
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(ws, geo, grads, ag_in)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    gbs = (nb["rs_bytes"] + nb["ag_bytes"]) * passes / el / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{w.name} rows/{div} (N={ws.N}, G={nb['G']}, S={nb['S']}): {passes} passes of RS+AG "
+                      f"in {el:.1f} s on one host core (numpy)",
+            "elements_per_s": round((nb["rs_elems"] + nb["ag_elems"]) * passes / el, 1)}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: rank 0 times K steps, each one
+    RS+AG pass over a row subset of the workload, on one host core."""
+    if rank != 0:
+        return None
+    from synth import configs
+    w = configs.get(args.workload)
+    div = SAMPLE_ROW_DIV.get(w.name, 16)
+    ws, geo, grads, ag_in = oracle_sample(w.name, div)
+    nb = algorithmic_bytes(ws, geo)
+    for _ in range(args.warmup):
+        oracle_step(ws, geo, grads, ag_in)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(ws, geo, grads, ag_in)
+    el = time.perf_counter() - t0
+    value = (nb["rs_bytes"] + nb["ag_bytes"]) * args.steps / el / 1e9
+    sample = f"{w.name} rows/{div} (N={ws.N}, G={nb['G']}, S={nb['S']}) per step, one host core (numpy)"
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded SplitMix64 bf16)",
+        "config": {"workload": f"{w.name}: {w.notes}", "N": w.N, "M": w.M, "L": w.L, "P": w.P,
+                   "sample_row_div": div},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "elements_per_s": round((nb["rs_elems"] + nb["ag_elems"]) * args.steps / el, 1),
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

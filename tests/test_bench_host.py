@@ -1,0 +1,81 @@
+"""bench.py host logic without a GPU: the reference (oracle) arm, the byte
+accounting, and the multi-rank aggregation over gloo with world_size 2."""
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import oracle.tide_oracle as O  # noqa: E402
+from synth import configs  # noqa: E402
+
+
+def test_algorithmic_bytes_match_closed_form():
+    w = configs.get(2)
+    geo = O.geometry(w.shapes, w.N)
+    nb = bench.algorithmic_bytes(w, geo)
+    assert nb["rs_bytes"] == 2 * 8 * 855_654_400 + 4 * 8 * 106_956_800
+    assert nb["ag_bytes"] == 4 * 8 * 106_956_800
+    w = configs.get(4)
+    geo = O.geometry(w.shapes, w.N)
+    assert bench.algorithmic_bytes(w, geo)["rs_bytes"] == 2 * 64 * 351_288_320 + 4 * 64 * 5_488_880
+
+
+def test_reference_arm_prints_one_json_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
+                          "--warmup", "1", "--workload", "tiny"], capture_output=True, text=True, timeout=300,
+                         cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["unit"] == "GB/s" and rec["value"] > 0
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    bench.init_dist(world, "gloo")
+    secs = [1.5, 2.5][rank]
+    units = [10.0, 30.0][rank]
+    q.put((rank, bench.aggregate(secs, units, world)))
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_aggregate_max_time_sum_units_over_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res[0] == res[1] == (2.5, 40.0)
+
+
+def test_reference_arm_only_rank0_prints(monkeypatch):
+    args = bench.parse_args(["--impl", "reference", "--steps", "1", "--warmup", "0", "--workload", "tiny"])
+    assert bench.run_reference(args, rank=1, world=2) is None
+    rec = bench.run_reference(args, rank=0, world=2)
+    assert rec["n_gpus"] == 2 and rec["impl"] == "reference"
