@@ -6,5 +6,5 @@
 
 from .tide import (  # noqa: F401
     TideError, TidePlan, tide_ag_place, tide_plan_create, tide_plan_destroy, tide_plan_items, tide_plan_level2_order,
-    tide_plan_param_geometry, tide_plan_shard_elems, tide_rs_reduce, LIB_PATH,
+    tide_plan_param_geometry, tide_plan_shard_elems, tide_rs_reduce, tide_rs_reduce_noalloc, LIB_PATH,
 )

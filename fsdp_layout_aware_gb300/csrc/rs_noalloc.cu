@@ -1,0 +1,161 @@
+// tide_rs_reduce_noalloc: the reduce-scatter for callers that cannot allocate
+// device memory.
+//
+// tide_rs_reduce keeps its work list and per-call pointer tables in device
+// memory that the plan allocates on first use (cudaMalloc, cudaHostAlloc).
+// Some callers cannot do that: a process whose device memory is all owned by
+// a caching allocator (so a cudaMalloc outside it fails or forces the cache to
+// be emptied), a runtime that must not add the implicit device
+// synchronisation cudaMalloc/cudaFree can bring, or code that runs under a
+// fixed, pre-reserved memory budget.  This entry point allocates nothing: the
+// same data live in one file-scope __device__ array of fixed size (below),
+// which the CUDA module loader places in every GPU that loads this library and
+// which stays there until the process exits.  The reduction itself is the
+// unchanged rs_fused kernel, so the results are bit-identical to
+// tide_rs_reduce.
+//
+// Sharing rules: every call on a device uses the same array, and the array
+// keeps whatever the last call left in it.  Each call rewrites every byte the
+// kernel reads before the kernel runs, so nothing has to start at zero.  Two
+// calls whose work overlaps on the GPU (different streams, no ordering
+// between them) race on the array; issue them on one stream or order them.
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "tide_internal.h"
+
+namespace tide {
+namespace {
+
+// Largest static scratch: work items (32 bytes each), the caller's pointer
+// array, the transposed gradient table, the shard table and the phase flags.
+// The five measured workloads need at most 3.2 MiB.
+constexpr size_t kNoallocScratchBytes = size_t(8) << 20;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+std::mutex g_setup_mutex;
+unsigned char* g_scratch_addr[kMaxDevices] = {};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// The caller passes gradient pointers rank-major ([r][p]); the kernel reads
+// them parameter-major ([p][r]).  Also flags each parameter whose N gradients
+// share one address phase mod 16 (the kernel's 16-byte load path).
+__global__ void noalloc_tables_kernel(const uint16_t* const* grads_rp, int N, int P, const uint16_t** gtab,
+                                      uint8_t* flags) {
+  const int64_t total = (int64_t)N * P;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int64_t p = i / N, r = i % N;
+    gtab[i] = grads_rp[r * P + p];
+  }
+  for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < P; p += stride) {
+    const uintptr_t phase0 = (uintptr_t)grads_rp[p] & 15;
+    uint8_t uniform = 1;
+    for (int r = 1; r < N; ++r)
+      if (((uintptr_t)grads_rp[(int64_t)r * P + p] & 15) != phase0) uniform = 0;
+    flags[p] = uniform;
+  }
+}
+
+tide_status cuda_status(cudaError_t err, const char* what) {
+  return fail(err == cudaErrorMemoryAllocation ? TIDE_ERR_OUT_OF_MEMORY : TIDE_ERR_CUDA,
+              std::string(what) + ": " + cudaGetErrorString(err));
+}
+
+}  // namespace
+}  // namespace tide
+
+using namespace tide;
+
+extern "C" tide_status tide_rs_reduce_noalloc(const tide_plan* pl, const void* const* grads, float* const* shards,
+                                              void* stream) {
+  clear_error();
+  if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  if (pl->rs_items.empty()) return TIDE_OK;
+  if (!grads || !shards) return fail(TIDE_ERR_INVALID_ARG, "grads or shards array is NULL");
+  for (int32_t r = 0; r < pl->N; ++r) {
+    if (!shards[r]) return fail(TIDE_ERR_INVALID_ARG, "shards[" + std::to_string(r) + "] is NULL");
+    if ((uintptr_t)shards[r] & 3) return fail(TIDE_ERR_ALIGNMENT, "shard pointer not 4-byte aligned");
+  }
+  for (int32_t p = 0; p < pl->P; ++p) {
+    if (pl->e[p] == 0) continue;
+    for (int32_t r = 0; r < pl->N; ++r) {
+      const void* g = grads[(size_t)r * pl->P + p];
+      if (!g) return fail(TIDE_ERR_INVALID_ARG, "grads[" + std::to_string(r * pl->P + p) + "] is NULL");
+      if ((uintptr_t)g & 1) return fail(TIDE_ERR_ALIGNMENT, "gradient pointer not 2-byte aligned");
+    }
+  }
+
+  // Scratch layout: items | caller's [r][p] pointers | [p][r] table | shards | flags.
+  const size_t n_ptr = (size_t)pl->N * pl->P;
+  const size_t items_bytes = pl->rs_items.size() * sizeof(RsItem);
+  const size_t off_grads_rp = align256(items_bytes);
+  const size_t off_gtab = align256(off_grads_rp + 8 * n_ptr);
+  const size_t off_shards = align256(off_gtab + 8 * n_ptr);
+  const size_t off_flags = align256(off_shards + 8 * (size_t)pl->N);
+  const size_t need = off_flags + (size_t)pl->P;
+  if (need > kNoallocScratchBytes)
+    return fail(TIDE_ERR_INVALID_ARG, "this group needs " + std::to_string(need) +
+                                          " bytes of static scratch; tide_rs_reduce_noalloc is limited to " +
+                                          std::to_string(kNoallocScratchBytes) + " bytes (use tide_rs_reduce)");
+
+  int dev = -1;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_status(err, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(TIDE_ERR_INVALID_ARG, "device ordinal beyond 63");
+  unsigned char* base;
+  {
+    // First call on this device: look up where the module loader put the
+    // array on this device (the address differs per device).
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (!g_scratch_addr[dev]) {
+      void* ptr = nullptr;
+      err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+      if (err != cudaSuccess) return cuda_status(err, "cudaGetSymbolAddress(static scratch)");
+      g_scratch_addr[dev] = (unsigned char*)ptr;
+    }
+    base = g_scratch_addr[dev];
+  }
+
+  cudaStream_t s = (cudaStream_t)stream;
+  if ((err = cudaMemcpyAsync(base, pl->rs_items.data(), items_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_status(err, "work-list upload");
+  if ((err = cudaMemcpyAsync(base + off_grads_rp, grads, 8 * n_ptr, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_status(err, "gradient pointer upload");
+  if ((err = cudaMemcpyAsync(base + off_shards, shards, 8 * (size_t)pl->N, cudaMemcpyHostToDevice, s)) !=
+      cudaSuccess)
+    return cuda_status(err, "shard pointer upload");
+  const int tgrid = (int)std::min<int64_t>(1024, ((int64_t)n_ptr + 255) / 256);
+  noalloc_tables_kernel<<<tgrid, 256, 0, s>>>((const uint16_t* const*)(base + off_grads_rp), pl->N, pl->P,
+                                               (const uint16_t**)(base + off_gtab), base + off_flags);
+  if ((err = cudaGetLastError()) != cudaSuccess) return cuda_status(err, "pointer-table kernel launch");
+
+  int sms = 0;
+  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return cuda_status(err, "cudaDeviceGetAttribute");
+  const int occ = rs_blocks_per_sm(pl->L);
+  if (occ <= 0) return fail(TIDE_ERR_CUDA, "occupancy query failed");
+
+  RsArgs a;
+  a.items = (const RsItem*)base;
+  a.n_items = (int64_t)pl->rs_items.size();
+  a.grad_tab = (const uint16_t* const*)(base + off_gtab);
+  a.shard_tab = (float* const*)(base + off_shards);
+  a.uniform_phase = base + off_flags;
+  a.N = pl->N;
+  a.M = pl->M;
+  a.L = pl->L;
+  a.P = pl->P;
+  std::memcpy(a.order, pl->order, sizeof(a.order));
+  const int grid = (int)std::min<int64_t>((int64_t)sms * occ, a.n_items);
+  const int lerr = launch_rs(a, grid, stream);
+  if (lerr != cudaSuccess) return cuda_status((cudaError_t)lerr, "rs_fused launch");
+  return TIDE_OK;
+}

@@ -56,6 +56,7 @@ def _load():
         "tide_plan_get_items": (i32, [vp, i32, ctypes.POINTER(i64), i64]),
         "tide_rs_reduce": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
         "tide_ag_place": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp]),
+        "tide_rs_reduce_noalloc": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
         "tide_status_string": (ctypes.c_char_p, [i32]),
         "tide_last_error": (ctypes.c_char_p, []),
     }
@@ -147,6 +148,11 @@ def tide_plan_items(plan, which):
 def tide_rs_reduce(plan, grads, shards, stream=None):
     """grads: N*P tensors/addresses (entry r*P + p), shards: N fp32 tensors/addresses."""
     _check(_lib.tide_rs_reduce(plan, _ptr_array(grads), _ptr_array(shards), _stream(stream)))
+
+
+def tide_rs_reduce_noalloc(plan, grads, shards, stream=None):
+    """tide_rs_reduce without any device allocation (fixed static scratch)."""
+    _check(_lib.tide_rs_reduce_noalloc(plan, _ptr_array(grads), _ptr_array(shards), _stream(stream)))
 
 
 def tide_ag_place(plan, shards, params, elem_bytes, stream=None):

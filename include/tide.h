@@ -166,6 +166,30 @@ tide_status tide_rs_reduce(tide_plan* plan, const void* const* grads, float* con
 tide_status tide_ag_place(tide_plan* plan, const void* const* shards, void* const* params,
                           int32_t elem_bytes, void* stream);
 
+/* tide_rs_reduce for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this call; it exists for users of this library.
+ * tide_rs_reduce allocates device memory for its work list and pointer tables
+ * on first use; some callers cannot: a process whose free device memory all
+ * belongs to a caching allocator, code that must not take the implicit device
+ * synchronisation that cudaMalloc/cudaFree can bring, or a fixed memory
+ * budget reserved up front.  This call allocates nothing.  It keeps the same
+ * data in one fixed 8 MiB __device__ array that every GPU loading libtide
+ * holds until the process exits, and runs the same kernel, so its results
+ * are bit-identical to tide_rs_reduce's.
+ *   plan, grads, shards, stream: as for tide_rs_reduce.  The plan's own
+ *   device state is not used or created.
+ * The first call on a device looks up the array's address on that device;
+ * make that first call before any CUDA graph capture.  Each call copies the
+ * plan's work list and the pointer arrays into the array from pageable host
+ * memory, so the call may wait for earlier work on `stream`.  The array is
+ * shared by all calls on a device and keeps the last call's contents; every
+ * call rewrites all it reads, so nothing needs clearing, but calls whose work
+ * overlaps on the GPU (different streams, no ordering) race.
+ * Errors: as tide_rs_reduce; INVALID_ARG also when the group's work list and
+ * tables exceed the 8 MiB array (use tide_rs_reduce for such groups). */
+tide_status tide_rs_reduce_noalloc(const tide_plan* plan, const void* const* grads, float* const* shards,
+                                   void* stream);
+
 /* Static text for a status code. */
 const char* tide_status_string(tide_status status);
 
