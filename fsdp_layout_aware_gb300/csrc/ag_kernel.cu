@@ -35,25 +35,26 @@ __device__ __forceinline__ void copy_elem(unsigned char* d, const unsigned char*
     *reinterpret_cast<uint16_t*>(d) = *reinterpret_cast<const uint16_t*>(s);
 }
 
-// Source and destination at the same address phase mod 16.
-__device__ __forceinline__ void copy_same_phase(unsigned char* dst, const unsigned char* src, int64_t nbytes,
-                                                int eb) {
+// One warp copies one item.  Source and destination at the same address
+// phase mod 16: a short element-wise head, then 16-byte vectors, four in
+// flight per lane, then an element-wise tail.
+__device__ __forceinline__ void warp_copy_same_phase(unsigned char* dst, const unsigned char* src, int64_t nbytes,
+                                                     int eb, int lane) {
   const int64_t head = min(nbytes, (int64_t)((16 - ((uintptr_t)dst & 15)) & 15));
-  for (int64_t i = (int64_t)threadIdx.x * eb; i < head; i += (int64_t)blockDim.x * eb) copy_elem(dst + i, src + i, eb);
+  for (int64_t i = (int64_t)lane * eb; i < head; i += 32 * eb) copy_elem(dst + i, src + i, eb);
   const int64_t nv = (nbytes - head) >> 4;
   const uint4* s4 = reinterpret_cast<const uint4*>(src + head);
   uint4* d4 = reinterpret_cast<uint4*>(dst + head);
-  const int64_t T = blockDim.x;
-  int64_t i = threadIdx.x;
-  for (; i + 3 * T < nv; i += 4 * T) {
-    const uint4 a = __ldcs(s4 + i), b = __ldcs(s4 + i + T), c = __ldcs(s4 + i + 2 * T), d = __ldcs(s4 + i + 3 * T);
+  int64_t i = lane;
+  for (; i + 96 < nv; i += 128) {
+    const uint4 a = __ldcs(s4 + i), b = __ldcs(s4 + i + 32), c = __ldcs(s4 + i + 64), d = __ldcs(s4 + i + 96);
     __stcs(d4 + i, a);
-    __stcs(d4 + i + T, b);
-    __stcs(d4 + i + 2 * T, c);
-    __stcs(d4 + i + 3 * T, d);
+    __stcs(d4 + i + 32, b);
+    __stcs(d4 + i + 64, c);
+    __stcs(d4 + i + 96, d);
   }
-  for (; i < nv; i += T) __stcs(d4 + i, __ldcs(s4 + i));
-  for (int64_t j = head + (nv << 4) + (int64_t)threadIdx.x * eb; j < nbytes; j += T * eb) copy_elem(dst + j, src + j, eb);
+  for (; i < nv; i += 32) __stcs(d4 + i, __ldcs(s4 + i));
+  for (int64_t j = head + (nv << 4) + (int64_t)lane * eb; j < nbytes; j += 32 * eb) copy_elem(dst + j, src + j, eb);
 }
 
 // Bytes [sh, sh + 16) of the 32-byte concatenation lo || hi (sh even).
@@ -83,54 +84,96 @@ __device__ __forceinline__ uint4 extract16(const uint4 lo, const uint4 hi, int s
   return o;
 }
 
+__device__ __forceinline__ uint4 shfl16(const uint4 v, int src_lane) {
+  uint4 o;
+  o.x = __shfl_sync(0xffffffffu, v.x, src_lane);
+  o.y = __shfl_sync(0xffffffffu, v.y, src_lane);
+  o.z = __shfl_sync(0xffffffffu, v.z, src_lane);
+  o.w = __shfl_sync(0xffffffffu, v.w, src_lane);
+  return o;
+}
+
+__device__ __forceinline__ uint4 load_granule(uintptr_t g, uintptr_t s_lo, uintptr_t s_hi) {
+  return (g + 16 > s_lo && g < s_hi) ? __ldcs(reinterpret_cast<const uint4*>(g)) : make_uint4(0, 0, 0, 0);
+}
+
 // Source and destination at different phases.  Destination word w covers
-// bytes [d0 + 16w, d0 + 16w + 16); its source bytes start at that address +
-// (src - dst) and straddle two aligned source granules.  A granule is loaded
-// only if it holds at least one byte of the source range.
-__device__ __forceinline__ void copy_shifted(unsigned char* dst, const unsigned char* src, int64_t nbytes, int eb) {
+// bytes [d0 + 16w, d0 + 16w + 16); its bytes come from source address
+// (that + src - dst), which straddles the aligned source granules g(w) and
+// g(w) + 16 = g(w + 1).  In a round the warp handles words base + 32j + lane
+// (j = 0..3, four in flight per lane); lane t loads g(w) for its words and
+// takes g(w + 1) from lane t + 1 by a rotating shuffle -- lane 31's next
+// granule is lane 0's granule of the following group, and lane 0 loads the
+// one after the round.  Every granule is read once, and only if it holds a
+// byte of the source range.  Called by all 32 lanes of the warp.
+__device__ __forceinline__ void warp_copy_shifted(unsigned char* dst, const unsigned char* src, int64_t nbytes, int eb,
+                                                  int lane) {
   const uintptr_t d_lo = (uintptr_t)dst, d_hi = d_lo + (uintptr_t)nbytes;
   const uintptr_t s_lo = (uintptr_t)src, s_hi = s_lo + (uintptr_t)nbytes;
   const uintptr_t d0 = d_lo & ~(uintptr_t)15;
-  const int64_t nw = (int64_t)((d_hi + 15 - d0) >> 4);
-  const uintptr_t delta = s_lo - d_lo;  // modular; source address = destination address + delta
+  const int nw = (int)((d_hi + 15 - d0) >> 4);  // items are at most 64 KiB
+  const uintptr_t delta = s_lo - d_lo;  // modular: source address = destination address + delta
   const int sh = (int)(delta & 15);
-  for (int64_t w = threadIdx.x; w < nw; w += blockDim.x) {
-    const uintptr_t dw = d0 + 16 * (uintptr_t)w;
-    const uintptr_t g0 = (dw + delta) & ~(uintptr_t)15, g1 = g0 + 16;
-    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-    if (g0 + 16 > s_lo && g0 < s_hi) lo = __ldg(reinterpret_cast<const uint4*>(g0));
-    if (g1 + 16 > s_lo && g1 < s_hi) hi = __ldg(reinterpret_cast<const uint4*>(g1));
-    Vec16 out;
-    out.v = extract16(lo, hi, sh);
-    if (dw >= d_lo && dw + 16 <= d_hi) {
-      __stcs(reinterpret_cast<uint4*>(dw), out.v);
-    } else if (eb == 2) {
+  const unsigned char* g_first = (const unsigned char*)((d0 + delta) & ~(uintptr_t)15);  // granule of word 0
+  unsigned char* const dbase = (unsigned char*)d0;
+  const int next_lane = (lane + 1) & 31;
+  for (int base = 0; base < nw; base += 128) {
+    uint4 lo[5];
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        const uintptr_t addr = dw + 2 * b;
-        if (addr >= d_lo && addr < d_hi) *reinterpret_cast<uint16_t*>(addr) = out.h[b];
-      }
-    } else {
+    for (int j = 0; j < 4; ++j) lo[j] = load_granule((uintptr_t)(g_first + 16 * (base + 32 * j + lane)), s_lo, s_hi);
+    lo[4] = lane == 0 ? load_granule((uintptr_t)(g_first + 16 * (base + 128)), s_lo, s_hi) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const uintptr_t addr = dw + 4 * b;
-        if (addr >= d_lo && addr < d_hi) *reinterpret_cast<uint32_t*>(addr) = out.w[b];
+    for (int j = 0; j < 4; ++j) {
+      const uint4 hi = shfl16(lane == 0 ? lo[j + 1] : lo[j], next_lane);
+      const int w = base + 32 * j + lane;
+      if (w >= nw) continue;
+      unsigned char* dw = dbase + 16 * w;
+      Vec16 out;
+      out.v = extract16(lo[j], hi, sh);
+      if ((uintptr_t)dw >= d_lo && (uintptr_t)dw + 16 <= d_hi) {
+        __stcs(reinterpret_cast<uint4*>(dw), out.v);
+      } else if (eb == 2) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          const uintptr_t addr = (uintptr_t)dw + 2 * b;
+          if (addr >= d_lo && addr < d_hi) *reinterpret_cast<uint16_t*>(addr) = out.h[b];
+        }
+      } else {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const uintptr_t addr = (uintptr_t)dw + 4 * b;
+          if (addr >= d_lo && addr < d_hi) *reinterpret_cast<uint32_t*>(addr) = out.w[b];
+        }
       }
     }
   }
 }
 
-__global__ void __launch_bounds__(kAgThreads) ag_place_kernel(const __grid_constant__ AgArgs a) {
+// Warp w of W processes units w, w + W, ...; the plan cut the units to equal
+// cost (bytes copied plus a per-item start-up charge), so a small or ragged
+// item never leaves one warp with more than its share, and neighbouring warps
+// copy neighbouring parts of the item list.
+__global__ void __launch_bounds__(kAgThreads, 4) ag_place_kernel(const __grid_constant__ AgArgs a) {
   const int eb = a.elem_bytes;
-  for (int64_t it = blockIdx.x; it < a.n_items; it += gridDim.x) {
-    const AgItem item = a.items[it];
-    const unsigned char* src = a.shard_tab[item.r] + item.src_off * eb;
-    unsigned char* dst = a.param_tab[item.p] + item.dst_off * eb;
-    const int64_t nbytes = (int64_t)item.n * eb;
-    if ((((uintptr_t)src ^ (uintptr_t)dst) & 15) == 0)
-      copy_same_phase(dst, src, nbytes, eb);
-    else
-      copy_shifted(dst, src, nbytes, eb);
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t u = warp; u < a.n_units; u += nwarps) {
+    const UnitStart s = a.units[u], e = a.units[u + 1];
+    const int64_t last = e.off > 0 ? e.item : (int64_t)e.item - 1;
+    for (int64_t i = s.item; i <= last; ++i) {
+      const AgItem item = a.items[i];
+      const int32_t ea = i == s.item ? s.off : 0;
+      const int32_t ee = i == e.item ? e.off : item.n;
+      if (ea >= ee) continue;
+      const unsigned char* src = a.shard_tab[item.r] + (item.src_off + ea) * eb;
+      unsigned char* dst = a.param_tab[item.p] + (item.dst_off + ea) * eb;
+      const int64_t nbytes = (int64_t)(ee - ea) * eb;
+      if ((((uintptr_t)src ^ (uintptr_t)dst) & 15) == 0)
+        warp_copy_same_phase(dst, src, nbytes, eb, lane);
+      else
+        warp_copy_shifted(dst, src, nbytes, eb, lane);
+    }
   }
 }
 

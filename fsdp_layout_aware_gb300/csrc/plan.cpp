@@ -83,7 +83,46 @@ void build_ag_items(tide_plan* pl) {
     }
   }
 }
+void build_prefixes(tide_plan* pl) {
+  pl->ag_prefix.resize(pl->ag_items.size() + 1);
+  pl->ag_prefix[0] = 0;
+  for (size_t i = 0; i < pl->ag_items.size(); ++i)
+    pl->ag_prefix[i + 1] = pl->ag_prefix[i] + ag_item_cost(pl->ag_items[i]);
+}
 }  // namespace
+
+namespace {
+template <class Item, class Split>
+std::vector<UnitStart> unit_starts(const std::vector<Item>& items, const std::vector<int64_t>& prefix,
+                                   int64_t workers, int64_t target, int64_t max_k, Split split) {
+  const int64_t total = prefix.back();
+  const int64_t n_items = (int64_t)items.size();
+  int64_t k = workers > 0 ? (total + workers * target - 1) / (workers * target) : 1;
+  k = std::max<int64_t>(1, std::min(k, max_k));
+  const int64_t U = std::max<int64_t>(1, k * workers);
+  std::vector<UnitStart> out(U + 1);
+  int64_t i = 0;
+  for (int64_t u = 0; u <= U; ++u) {
+    const int64_t t = (int64_t)((__int128)total * u / U);
+    while (i < n_items && prefix[i + 1] <= t) ++i;  // prefix[i] <= t < prefix[i + 1]
+    int64_t item = i, off = 0;
+    if (i < n_items) {
+      off = split(items[i], t - prefix[i]);
+      if (off >= items[i].n) {
+        item = i + 1;
+        off = 0;
+      }
+    }
+    out[u] = UnitStart{(int32_t)item, (int32_t)off};
+  }
+  return out;
+}
+}  // namespace
+
+std::vector<UnitStart> ag_unit_starts(const tide_plan* pl, int64_t workers, int64_t target, int64_t max_k) {
+  return unit_starts(pl->ag_items, pl->ag_prefix, workers, target, max_k,
+                     [](const AgItem& it, int64_t rel) { return ag_split(it, rel); });
+}
 
 tide_status fail(tide_status st, const std::string& msg) {
   g_last_error = msg;
@@ -182,6 +221,7 @@ tide_status tide_plan_create(const tide_group_desc* d, tide_plan** out_plan) {
     build_order_table(pl);
     build_rs_items(pl);
     build_ag_items(pl);
+    build_prefixes(pl);
   } catch (const std::bad_alloc&) {
     delete pl;
     return fail(TIDE_ERR_OUT_OF_MEMORY, "host allocation failed while building the plan");

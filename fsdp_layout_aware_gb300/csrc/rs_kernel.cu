@@ -54,27 +54,72 @@ __device__ __forceinline__ void zero_fill(float* dst, int n) {
   if ((int)threadIdx.x < n - t0) dst[t0 + threadIdx.x] = 0.f;
 }
 
-// Store the 8 results of a vector whose lane 0 is item element e0; lanes
-// outside [0, n) are skipped.  dmis is the address phase (bytes mod 16) of
-// lane 0's output, the same for every vector of an item.
-__device__ __forceinline__ void store8(float* dst, int e0, int n, int dmis, const float (&acc)[8]) {
+// Store the 8 results of a vector whose lane 0 is item element e0 when the
+// destination of e0 is 16-byte aligned; lanes outside [0, n) are skipped.
+__device__ __forceinline__ void store8_aligned(float* dst, int e0, int n, const float (&acc)[8]) {
   if (e0 >= 0 && e0 + 8 <= n) {
     float* o = dst + e0;
-    if (dmis == 0) {
-      __stcs(reinterpret_cast<float4*>(o), make_float4(acc[0], acc[1], acc[2], acc[3]));
-      __stcs(reinterpret_cast<float4*>(o + 4), make_float4(acc[4], acc[5], acc[6], acc[7]));
-    } else if (dmis == 8) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) __stcs(reinterpret_cast<float2*>(o + 2 * j), make_float2(acc[2 * j], acc[2 * j + 1]));
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) __stcs(o + i, acc[i]);
-    }
+    __stcs(reinterpret_cast<float4*>(o), make_float4(acc[0], acc[1], acc[2], acc[3]));
+    __stcs(reinterpret_cast<float4*>(o + 4), make_float4(acc[4], acc[5], acc[6], acc[7]));
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = e0 + i;
       if (e >= 0 && e < n) __stcs(dst + e, acc[i]);
+    }
+  }
+}
+
+__device__ __forceinline__ void store4(float* dst, int a, int n, float w0, float w1, float w2, float w3) {
+  if (a >= 0 && a + 4 <= n) {
+    __stcs(reinterpret_cast<float4*>(dst + a), make_float4(w0, w1, w2, w3));
+  } else {
+    if (a >= 0 && a < n) __stcs(dst + a, w0);
+    if (a + 1 >= 0 && a + 1 < n) __stcs(dst + a + 1, w1);
+    if (a + 2 >= 0 && a + 2 < n) __stcs(dst + a + 2, w2);
+    if (a + 3 >= 0 && a + 3 < n) __stcs(dst + a + 3, w3);
+  }
+}
+
+// Destination of e0 is delta = 1..3 elements short of a 16-byte boundary.
+// Lane t writes the 16-byte aligned elements [e0+delta, e0+delta+8): its own
+// results from delta on, then the first delta results of lane t+1, which hold
+// the next 8 elements (one warp holds 256 consecutive elements).  Lane 31 has
+// no such neighbour and writes only its own part; lane 0 also writes its
+// first delta elements, which the previous warp's lane 31 cannot.  Together
+// the lanes write every element once.  Called by all 32 lanes.
+__device__ __forceinline__ void store8_shifted(float* dst, int e0, int n, int delta, int lane,
+                                               const float (&acc)[8]) {
+  const float n0 = __shfl_down_sync(0xffffffffu, acc[0], 1);
+  const float n1 = __shfl_down_sync(0xffffffffu, acc[1], 1);
+  const float n2 = __shfl_down_sync(0xffffffffu, acc[2], 1);
+  float w[8];
+  if (delta == 1) {
+    w[0] = acc[1]; w[1] = acc[2]; w[2] = acc[3]; w[3] = acc[4];
+    w[4] = acc[5]; w[5] = acc[6]; w[6] = acc[7]; w[7] = n0;
+  } else if (delta == 2) {
+    w[0] = acc[2]; w[1] = acc[3]; w[2] = acc[4]; w[3] = acc[5];
+    w[4] = acc[6]; w[5] = acc[7]; w[6] = n0; w[7] = n1;
+  } else {
+    w[0] = acc[3]; w[1] = acc[4]; w[2] = acc[5]; w[3] = acc[6];
+    w[4] = acc[7]; w[5] = n0; w[6] = n1; w[7] = n2;
+  }
+  const int a = e0 + delta;
+  store4(dst, a, n, w[0], w[1], w[2], w[3]);   // always this lane's own results
+  if (lane != 31) {
+    store4(dst, a + 4, n, w[4], w[5], w[6], w[7]);
+  } else {
+#pragma unroll
+    for (int i = 4; i < 8; ++i) {
+      const int j = a + i;
+      if (j < e0 + 8 && j >= 0 && j < n) __stcs(dst + j, w[i]);
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const int j = e0 + i;
+      if (i < delta && j >= 0 && j < n) __stcs(dst + j, acc[i]);
     }
   }
 }
@@ -89,26 +134,35 @@ __device__ __forceinline__ void reduce_aligned(const uint16_t* const* src, const
                                                int n) {
   const int ph = (int)(((uintptr_t)src[0] >> 1) & 7);
   const int nvec = (ph + n + 7) >> 3;
-  const int dmis = (int)(((uintptr_t)dst - 4u * (unsigned)ph) & 15);
-  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+  // elements from a vector's first element to the next 16-byte boundary of dst
+  const int delta = (int)(((unsigned)ph - (unsigned)((uintptr_t)dst >> 2)) & 3u);
+  const int lane = threadIdx.x & 31;
+  // The loop condition is uniform per warp (the warp's first vector), so all
+  // 32 lanes reach the shuffles in store8_shifted.
+  for (int v = threadIdx.x; v - lane < nvec; v += blockDim.x) {
     const int e0 = v * 8 - ph;
     float acc2[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc2[i] = 0.f;
-    for (int k = 0; k < M; ++k) {
-      const int node = ord[k];
-      uint4 x[L];
+    if (v < nvec) {
+      for (int k = 0; k < M; ++k) {
+        const int node = ord[k];
+        uint4 x[L];
 #pragma unroll
-      for (int l = 0; l < L; ++l) x[l] = __ldcs(reinterpret_cast<const uint4*>(src[node * L + l] + e0));
-      float acc1[8];
+        for (int l = 0; l < L; ++l) x[l] = __ldcs(reinterpret_cast<const uint4*>(src[node * L + l] + e0));
+        float acc1[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc1[i] = 0.f;
+        for (int i = 0; i < 8; ++i) acc1[i] = 0.f;
 #pragma unroll
-      for (int l = 0; l < L; ++l) add_bf16x8(acc1, x[l]);
+        for (int l = 0; l < L; ++l) add_bf16x8(acc1, x[l]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc2[i] = __fadd_rn(acc2[i], acc1[i]);
+        for (int i = 0; i < 8; ++i) acc2[i] = __fadd_rn(acc2[i], acc1[i]);
+      }
     }
-    store8(dst, e0, n, dmis, acc2);
+    if (delta == 0)
+      store8_aligned(dst, e0, n, acc2);
+    else
+      store8_shifted(dst, e0, n, delta, lane, acc2);
   }
 }
 
@@ -144,11 +198,18 @@ __device__ __forceinline__ void reduce_unaligned(const uint16_t* const* src, con
   }
 }
 
+// CTA b processes items b, b + G, b + 2G, ... (G = grid size): at any moment
+// the CTAs work on neighbouring items, so the contributors are read in nearly
+// address order across the GPU.  The next item's descriptor is fetched while
+// the current one is reduced.
 template <int L>
-__global__ void __launch_bounds__(kRsThreads) rs_fused_kernel(const __grid_constant__ RsArgs a) {
+__global__ void __launch_bounds__(kRsThreads, 4) rs_fused_kernel(const __grid_constant__ RsArgs a) {
   __shared__ const uint16_t* src[kMaxN];
+  if ((int64_t)blockIdx.x >= a.n_items) return;
+  RsItem next = a.items[blockIdx.x];
   for (int64_t it = blockIdx.x; it < a.n_items; it += gridDim.x) {
-    const RsItem item = a.items[it];
+    const RsItem item = next;
+    if (it + gridDim.x < a.n_items) next = a.items[it + gridDim.x];
     float* dst = a.shard_tab[item.r] + item.dst_off;
     if (item.kind == RS_PAD) {
       zero_fill(dst, item.n);

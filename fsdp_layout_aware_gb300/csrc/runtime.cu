@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <new>
 
 #include "tide_internal.h"
 
@@ -45,8 +46,10 @@ void release_device_state(tide_plan* pl) {
   }
   if (pl->d_rs_items) cudaFree(pl->d_rs_items);
   if (pl->d_ag_items) cudaFree(pl->d_ag_items);
+  if (pl->d_ag_units) cudaFree(pl->d_ag_units);
   pl->d_rs_items = nullptr;
   pl->d_ag_items = nullptr;
+  pl->d_ag_units = nullptr;
   pl->device = -1;
 }
 
@@ -99,7 +102,21 @@ tide_status ensure_device(tide_plan* pl) {
     return fail(TIDE_ERR_CUDA, "occupancy query failed (is this an sm_103 device?)");
   }
   pl->rs_grid = (int)std::min<int64_t>((int64_t)pl->num_sms * rs_occ, std::max<int64_t>(1, pl->rs_items.size()));
-  pl->ag_grid = (int)std::min<int64_t>((int64_t)pl->num_sms * ag_occ, std::max<int64_t>(1, pl->ag_items.size()));
+  pl->ag_grid = (int)std::min<int64_t>((int64_t)pl->num_sms * ag_occ,
+                                       std::max<int64_t>(1, ((int64_t)pl->ag_items.size() + 7) / 8));
+  // Equal-cost all-gather units: about 16 KiB each, at most 32 per warp.
+  try {
+    const std::vector<UnitStart> au = ag_unit_starts(pl, (int64_t)pl->ag_grid * (kAgThreads / 32), 16 << 10, 32);
+    pl->ag_units = (int64_t)au.size() - 1;
+    if ((err = cudaMalloc(&pl->d_ag_units, au.size() * sizeof(UnitStart))) != cudaSuccess)
+      return bail(err, "cudaMalloc(ag units)");
+    if ((err = cudaMemcpy(pl->d_ag_units, au.data(), au.size() * sizeof(UnitStart), cudaMemcpyHostToDevice)) !=
+        cudaSuccess)
+      return bail(err, "cudaMemcpy(ag units)");
+  } catch (const std::bad_alloc&) {
+    release_device_state(pl);
+    return fail(TIDE_ERR_OUT_OF_MEMORY, "host allocation failed while building work units");
+  }
   return TIDE_OK;
 }
 
@@ -229,6 +246,8 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
 
   AgArgs a;
   a.items = pl->d_ag_items;
+  a.units = pl->d_ag_units;
+  a.n_units = pl->ag_units;
   a.n_items = (int64_t)pl->ag_items.size();
   a.shard_tab = (const unsigned char* const*)slot->dev;
   a.param_tab = (unsigned char* const*)(slot->dev + (size_t)pl->N * 8);

@@ -53,11 +53,46 @@ constexpr int64_t kRsPadChunk = 32768;
 constexpr int kAgThreads = 256;
 constexpr int64_t kAgChunkBytes = 65536;
 
+// All-gather load balance.  Every item has a cost (a start-up charge for its
+// descriptor and pointer loads, plus bytes moved per element) and the plan
+// keeps the prefix sum of the costs.  When the plan is set up on a device it
+// cuts the total cost into U = k*W equal units (W = warps of the grid),
+// splitting items where a boundary falls inside one.  Warp w takes units
+// w, w+W, w+2W, ...: every warp gets k units of equal cost, and at any moment
+// neighbouring warps copy neighbouring parts of the item list, which keeps
+// DRAM accesses in nearly address order.  (The reduce-scatter's items are
+// already of near-equal cost -- 8192 elements -- and it takes them
+// round-robin.)
+#if defined(__CUDACC__)
+#define TIDE_HD __host__ __device__
+#else
+#define TIDE_HD
+#endif
+constexpr int64_t kAgItemCost = 2048;
+
+TIDE_HD inline int64_t ag_item_cost(const AgItem& it) { return kAgItemCost + 4 * (int64_t)it.n; }
+
+// First element of an item that a worker whose range starts `rel` cost units
+// into the item copies, rounded up to 8 destination elements.
+TIDE_HD inline int32_t ag_split(const AgItem& it, int64_t rel) {
+  if (rel <= kAgItemCost) return 0;
+  int64_t e = (rel - kAgItemCost + 3) / 4;
+  e = (it.dst_off + e + 7) / 8 * 8 - it.dst_off;
+  return (int32_t)(e < it.n ? e : it.n);
+}
+
 // Level-2 order table: order[(n_dest * L + s) * M + k] is the k-th source node
 // whose partial is added for slice s of destination node n_dest.
 constexpr int kOrderTableSize = kMaxL * kMaxL * kMaxL;
 
 // Kernel argument blocks (passed by value as __grid_constant__).
+// Start of a unit: item index and first element of that item.  Unit u spans
+// [units[u], units[u+1]); units[n_units] = {n_items, 0}.
+struct UnitStart {
+  int32_t item;
+  int32_t off;
+};
+
 struct RsArgs {
   const RsItem* items;
   int64_t n_items;
@@ -71,6 +106,8 @@ struct RsArgs {
 struct AgArgs {
   const AgItem* items;
   int64_t n_items;
+  const UnitStart* units;           // [n_units + 1]
+  int64_t n_units;
   const unsigned char* const* shard_tab;  // [N]
   unsigned char* const* param_tab;        // [P]
   int32_t elem_bytes;
@@ -92,6 +129,7 @@ struct tide_plan {
   int64_t S = 0;
   std::vector<tide::RsItem> rs_items;
   std::vector<tide::AgItem> ag_items;
+  std::vector<int64_t> ag_prefix;  // all-gather cost prefix sums (load balance)
   uint8_t order[tide::kOrderTableSize] = {};
 
   // Device state, created by the first compute call.
@@ -100,6 +138,8 @@ struct tide_plan {
   int rs_grid = 0, ag_grid = 0;
   tide::RsItem* d_rs_items = nullptr;
   tide::AgItem* d_ag_items = nullptr;
+  tide::UnitStart* d_ag_units = nullptr;
+  int64_t ag_units = 0;
   static constexpr int kRing = 8;
   struct Slot {
     unsigned char* host = nullptr;
@@ -112,6 +152,9 @@ struct tide_plan {
 };
 
 namespace tide {
+// Equal-cost all-gather unit boundaries for W workers (plan.cpp); at most
+// max_k units per worker, each worth about `target` cost units.
+std::vector<UnitStart> ag_unit_starts(const tide_plan* pl, int64_t workers, int64_t target, int64_t max_k);
 // Thread-local error reporting (plan.cpp).
 tide_status fail(tide_status st, const std::string& msg);
 void clear_error();
