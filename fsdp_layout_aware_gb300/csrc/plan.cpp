@@ -147,6 +147,7 @@ const char* tide_status_string(tide_status status) {
     case TIDE_ERR_CUDA: return "CUDA error";
     case TIDE_ERR_UNIMPLEMENTED: return "not implemented";
     case TIDE_ERR_DEVICE_MISMATCH: return "plan used on another device";
+    case TIDE_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
   }
   return "unknown status";
 }

@@ -1,0 +1,579 @@
+// TIDE-RS hot loop, bulk-copy pipeline (sm_103a).
+//
+// Same result as rs_fused (bit for bit: identical fp32 addition order) but the
+// contributors' bf16 data reach the SM through the Tensor Memory Accelerator
+// instead of per-thread loads, so the bytes in flight per SM are set by the
+// shared-memory ring, not by registers:
+//
+//   * one CTA per SM, a producer warp and 8 consumer warps;
+//   * a ring of S stages; a stage holds, for one tile of T = 8*V outputs of one
+//     item, the aligned 16-byte window of every contributor (N windows of at
+//     most 16*V bytes, with V = 256 / M vectors per tile);
+//   * the producer walks the CTA's items (round-robin over the grid, as in
+//     rs_fused) and, per tile, arms the stage's "full" mbarrier with the
+//     expected byte count and issues one cp.async.bulk per contributor;
+//   * consumer thread t < V*M takes source node j = t / V and vector
+//     v = t % V of the tile: it sums the node's L contributions from shared memory
+//     (level 1, l ascending) and writes the 8 fp32 partials to a transposition
+//     buffer; after a consumer barrier, thread t produces outputs t, t+256, ...
+//     by adding the M partials of each in the Latin-square landing order
+//     (level 2) and stores them (consecutive threads, consecutive addresses);
+//   * a consumer warp releases the stage ("empty" mbarrier) as soon as its
+//     level-1 loads are done, so the producer refills it while level 2 runs.
+//
+// Padding ranges are zero-filled by the consumers; parameters whose N
+// gradients do not share an address phase mod 16 (bulk copies need 16-byte
+// aligned sources) are reduced by the consumers with element-wise loads.
+//
+// Every wait is bounded by %globaltimer.  On timeout a thread records
+// TIDE_DEVICE_TIMEOUT in the plan's status word and raises the CTA's abort
+// flag; all loops stop, the CTA waits (again bounded) until every bulk copy it
+// issued has landed, and returns.  tide_plan_check reports the status word.
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "tide_internal.h"
+
+namespace tide {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+
+enum TileKind : int32_t { TILE_BULK = 0, TILE_PAD = 1, TILE_DIRECT = 2, TILE_END = 3 };
+
+struct TileDesc {
+  float* dst;        // first output of the tile
+  int64_t src_off;   // DIRECT: element offset inside the contributors' gradients
+  int32_t n;         // outputs in the tile
+  int32_t ph;        // BULK: elements of the first granule before the first output
+  int32_t kind;
+  int32_t p;         // DIRECT: parameter
+  uint32_t ord_lo;   // level-2 source-node order, one byte per node: nodes 0..3
+  uint32_t ord_hi;   //   and 4..7 (M <= 8)
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                   smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(smem_dst)),
+               "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void consumer_barrier() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
+__device__ __forceinline__ uint4 lds16(const unsigned char* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 v) {
+  acc[0] = __fadd_rn(acc[0], __uint_as_float(v.x << 16));
+  acc[1] = __fadd_rn(acc[1], __uint_as_float(v.x & 0xFFFF0000u));
+  acc[2] = __fadd_rn(acc[2], __uint_as_float(v.y << 16));
+  acc[3] = __fadd_rn(acc[3], __uint_as_float(v.y & 0xFFFF0000u));
+  acc[4] = __fadd_rn(acc[4], __uint_as_float(v.z << 16));
+  acc[5] = __fadd_rn(acc[5], __uint_as_float(v.z & 0xFFFF0000u));
+  acc[6] = __fadd_rn(acc[6], __uint_as_float(v.w << 16));
+  acc[7] = __fadd_rn(acc[7], __uint_as_float(v.w & 0xFFFF0000u));
+}
+
+// Store the 8 results of a vector whose lane 0 is item element e0 when the
+// destination of e0 is 16-byte aligned; lanes outside [0, n) are skipped.
+__device__ __forceinline__ void store8_aligned(float* dst, int e0, int n, const float (&acc)[8]) {
+  if (e0 >= 0 && e0 + 8 <= n) {
+    float* o = dst + e0;
+    __stcs(reinterpret_cast<float4*>(o), make_float4(acc[0], acc[1], acc[2], acc[3]));
+    __stcs(reinterpret_cast<float4*>(o + 4), make_float4(acc[4], acc[5], acc[6], acc[7]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = e0 + i;
+      if (e >= 0 && e < n) __stcs(dst + e, acc[i]);
+    }
+  }
+}
+
+__device__ __forceinline__ void store4(float* dst, int a, int n, float w0, float w1, float w2, float w3) {
+  if (a >= 0 && a + 4 <= n) {
+    __stcs(reinterpret_cast<float4*>(dst + a), make_float4(w0, w1, w2, w3));
+  } else {
+    if (a >= 0 && a < n) __stcs(dst + a, w0);
+    if (a + 1 >= 0 && a + 1 < n) __stcs(dst + a + 1, w1);
+    if (a + 2 >= 0 && a + 2 < n) __stcs(dst + a + 2, w2);
+    if (a + 3 >= 0 && a + 3 < n) __stcs(dst + a + 3, w3);
+  }
+}
+
+// Destination of e0 is delta = 1..3 elements short of a 16-byte boundary.
+// Lane t writes the 16-byte aligned elements [e0+delta, e0+delta+8): its own
+// results from delta on, then the first delta results of lane t+1, which hold
+// the next 8 elements (one warp holds 256 consecutive elements).  Lane 31 has
+// no such neighbour and writes only its own part; lane 0 also writes its
+// first delta elements, which the previous warp's lane 31 cannot.  Together
+// the lanes write every element once.  Called by all 32 lanes.
+__device__ __forceinline__ void store8_shifted(float* dst, int e0, int n, int delta, int lane,
+                                               const float (&acc)[8]) {
+  const float n0 = __shfl_down_sync(0xffffffffu, acc[0], 1);
+  const float n1 = __shfl_down_sync(0xffffffffu, acc[1], 1);
+  const float n2 = __shfl_down_sync(0xffffffffu, acc[2], 1);
+  float w[8];
+  if (delta == 1) {
+    w[0] = acc[1]; w[1] = acc[2]; w[2] = acc[3]; w[3] = acc[4];
+    w[4] = acc[5]; w[5] = acc[6]; w[6] = acc[7]; w[7] = n0;
+  } else if (delta == 2) {
+    w[0] = acc[2]; w[1] = acc[3]; w[2] = acc[4]; w[3] = acc[5];
+    w[4] = acc[6]; w[5] = acc[7]; w[6] = n0; w[7] = n1;
+  } else {
+    w[0] = acc[3]; w[1] = acc[4]; w[2] = acc[5]; w[3] = acc[6];
+    w[4] = acc[7]; w[5] = n0; w[6] = n1; w[7] = n2;
+  }
+  const int a = e0 + delta;
+  store4(dst, a, n, w[0], w[1], w[2], w[3]);   // always this lane's own results
+  if (lane != 31) {
+    store4(dst, a + 4, n, w[4], w[5], w[6], w[7]);
+  } else {
+#pragma unroll
+    for (int i = 4; i < 8; ++i) {
+      const int j = a + i;
+      if (j < e0 + 8 && j >= 0 && j < n) __stcs(dst + j, w[i]);
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const int j = e0 + i;
+      if (i < delta && j >= 0 && j < n) __stcs(dst + j, acc[i]);
+    }
+  }
+}
+
+// Shared-memory carve-up, computed on the host (rs_bulk_layout).
+struct Smem {
+  unsigned char* stages;
+  float* part;           // 2 x V*PS transposition buffers
+  TileDesc* desc;        // [S]
+  uint64_t* full;        // [S]
+  uint64_t* empty;       // [S]
+  const uint16_t** src;  // [kMaxN] DIRECT tiles
+  int* ctl;              // [0] abort flag, [1 + s] rounds issued on stage s,
+                         // [1 + kMaxBulkStages + s] consumers' wait result for stage s
+};
+
+__device__ __forceinline__ Smem carve(unsigned char* base, const RsArgs& a) {
+  Smem m;
+  m.stages = base;
+  m.part = reinterpret_cast<float*>(base + a.bulk.off_part);
+  m.desc = reinterpret_cast<TileDesc*>(base + a.bulk.off_desc);
+  m.full = reinterpret_cast<uint64_t*>(base + a.bulk.off_bar);
+  m.empty = m.full + a.bulk.stages;
+  m.src = reinterpret_cast<const uint16_t**>(base + a.bulk.off_src);
+  m.ctl = reinterpret_cast<int*>(base + a.bulk.off_ctl);
+  return m;
+}
+
+// Bounded wait for the phase of `bar` with the given parity.  False on
+// timeout (recorded in the plan's status word, abort raised) or when the CTA
+// is already aborting.
+__device__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag, const RsArgs& a) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > a.bulk.wait_limit_ns) {
+      atomicOr(a.bulk.status, TIDE_DEVICE_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// A phase another thread has already seen complete: acquire it in this thread
+// too (returns at once; bounded all the same).
+__device__ __forceinline__ void acquire_completed(uint64_t* bar, uint32_t parity) {
+  for (int i = 0; i < (1 << 20) && !mbar_try_wait(bar, parity); ++i) {
+  }
+}
+
+// The producer warp decides as one: lane 0 waits, the warp follows its answer.
+__device__ __forceinline__ bool warp_wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                const RsArgs& a) {
+  const int lane = threadIdx.x & 31;
+  int ok = 0;
+  if (lane == 0) ok = wait_phase(bar, parity, abort_flag, a) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok && lane != 0) acquire_completed(bar, parity);
+  return ok != 0;
+}
+
+template <int L>
+__device__ void producer(const RsArgs& a, const Smem& m) {
+  const int lane = threadIdx.x & 31;
+  const int N = a.N;
+  const int V = a.bulk.V;
+  const int T = 8 * V;
+  volatile int* abort_flag = m.ctl;
+  uint32_t stage = 0, round = 0;
+  int64_t tile = 0;
+  bool ok = true;
+  // Claim the next stage: wait until the consumers have released its previous use.
+  auto acquire = [&]() -> bool { return warp_wait_phase(&m.empty[stage], (round & 1) ^ 1, abort_flag, a); };
+  auto advance = [&]() {
+    if (++stage == (uint32_t)a.bulk.stages) {
+      stage = 0;
+      ++round;
+    }
+    ++tile;
+  };
+  for (int64_t it = blockIdx.x; ok && it < a.n_items; it += gridDim.x) {
+    const RsItem item = a.items[it];
+    float* dst = a.shard_tab[item.r] + item.dst_off;
+    uint32_t ord_lo = 0, ord_hi = 0;
+    {
+      const uint8_t* ord = a.order + ((item.r / L) * L + item.slice) * a.M;
+      for (int k = 0; k < a.M; ++k) {
+        if (k < 4) ord_lo |= (uint32_t)ord[k] << (8 * k);
+        else ord_hi |= (uint32_t)ord[k] << (8 * (k - 4));
+      }
+    }
+    if (item.kind == RS_PAD || !a.uniform_phase[item.p]) {
+      if (!(ok = acquire())) break;
+      if (lane == 0) {
+        TileDesc d;
+        d.dst = dst;
+        d.src_off = item.src_off;
+        d.n = item.n;
+        d.ph = 0;
+        d.kind = item.kind == RS_PAD ? TILE_PAD : TILE_DIRECT;
+        d.p = item.p;
+        d.ord_lo = ord_lo;
+        d.ord_hi = ord_hi;
+        m.desc[stage] = d;
+        if (tile != a.bulk.test_drop_tile) mbar_arrive(&m.full[stage]);
+      }
+      __syncwarp();
+      advance();
+      continue;
+    }
+    const uint16_t* g0 = lane < N ? a.grad_tab[(int64_t)item.p * N + lane] + item.src_off : nullptr;
+    const uint16_t* g1 = lane + 32 < N ? a.grad_tab[(int64_t)item.p * N + lane + 32] + item.src_off : nullptr;
+    const uintptr_t first = __shfl_sync(0xffffffffu, (unsigned long long)(uintptr_t)g0, 0);
+    const int ph0 = (int)((first >> 1) & 7);
+    for (int e = 0; e < item.n;) {
+      const int ph = e == 0 ? ph0 : 0;
+      const int nt = min(item.n - e, T - ph);
+      const uint32_t bytes = (uint32_t)((2 * (ph + nt) + 15) & ~15);
+      if (!(ok = acquire())) break;
+      unsigned char* sbuf = m.stages + (size_t)stage * a.bulk.stage_bytes;
+      const bool drop = tile == a.bulk.test_drop_tile;
+      if (lane == 0) {
+        TileDesc d;
+        d.dst = dst + e;
+        d.src_off = 0;
+        d.n = nt;
+        d.ph = ph;
+        d.kind = TILE_BULK;
+        d.p = item.p;
+        d.ord_lo = ord_lo;
+        d.ord_hi = ord_hi;
+        m.desc[stage] = d;
+        if (!drop) {
+          mbar_arrive_expect_tx(&m.full[stage], bytes * (uint32_t)N);
+          m.ctl[1 + stage] = (int)round + 1;
+        }
+      }
+      __syncwarp();
+      if (!drop) {
+        if (g0) bulk_load(sbuf + (size_t)lane * 16 * V, g0 + e - ph, bytes, &m.full[stage]);
+        if (g1) bulk_load(sbuf + (size_t)(lane + 32) * 16 * V, g1 + e - ph, bytes, &m.full[stage]);
+      }
+      advance();
+      e += nt;
+    }
+  }
+  if (ok && acquire()) {
+    if (lane == 0) {
+      m.desc[stage].kind = TILE_END;
+      mbar_arrive(&m.full[stage]);
+    }
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void zero_fill_consumers(float* dst, int n, int tid) {
+  const int head = min(n, (int)(((16 - ((uintptr_t)dst & 15)) & 15) >> 2));
+  if (tid < head) dst[tid] = 0.f;
+  const int nv = (n - head) >> 2;
+  float4* d4 = reinterpret_cast<float4*>(dst + head);
+  for (int i = tid; i < nv; i += kConsumers) __stcs(d4 + i, make_float4(0.f, 0.f, 0.f, 0.f));
+  const int t0 = head + (nv << 2);
+  if (tid < n - t0) dst[t0 + tid] = 0.f;
+}
+
+template <int L>
+__device__ void consumers(const RsArgs& a, const Smem& m) {
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int M = a.M;
+  const int V = a.bulk.V;
+  const int PS = a.bulk.PS;
+  volatile int* abort_flag = m.ctl;
+  uint32_t stage = 0, round = 0;
+  int pb = 0;
+  for (;;) {
+    // The consumer warps decide as one (a named barrier must never lose a
+    // participant): thread 0 waits, publishes the answer in this stage's slot,
+    // and every thread then acquires the completed phase itself.
+    if (tid == 0) m.ctl[1 + kMaxBulkStages + stage] = wait_phase(&m.full[stage], round & 1, abort_flag, a) ? 1 : 0;
+    consumer_barrier();
+    if (!m.ctl[1 + kMaxBulkStages + stage]) break;
+    if (tid != 0) acquire_completed(&m.full[stage], round & 1);
+    const TileDesc d = m.desc[stage];
+    if (d.kind == TILE_END) break;
+    if (d.kind == TILE_BULK) {
+      const unsigned char* sbuf = m.stages + (size_t)stage * a.bulk.stage_bytes;
+      const int nvec = (d.ph + d.n + 7) >> 3;
+      if (M == 1) {
+        // One node: the level-1 sum is the result.  Thread v stores its 8
+        // outputs (16-byte stores, realigned across lanes when needed).
+        float acc2[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc2[i] = 0.f;
+        if (tid < nvec) {
+          float acc1[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc1[i] = 0.f;
+          uint4 x[L];
+#pragma unroll
+          for (int l = 0; l < L; ++l) x[l] = lds16(sbuf + (size_t)l * 16 * V + 16 * tid);
+#pragma unroll
+          for (int l = 0; l < L; ++l) add_bf16x8(acc1, x[l]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc2[i] = __fadd_rn(acc2[i], acc1[i]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m.empty[stage]);
+        if (tid - lane < nvec) {  // warp-uniform: the shuffles need every lane
+          const int delta = (int)(((unsigned)d.ph - (unsigned)((uintptr_t)d.dst >> 2)) & 3u);
+          const int e0 = tid * 8 - d.ph;
+          if (delta == 0)
+            store8_aligned(d.dst, e0, d.n, acc2);
+          else
+            store8_shifted(d.dst, e0, d.n, delta, lane, acc2);
+        }
+      } else {
+        float* part = m.part + pb * V * PS;
+        if (tid < V * M) {
+          // consecutive threads take consecutive vectors of one node, so a
+          // warp's 16-byte loads hit consecutive shared-memory addresses
+          const int j = tid / V, v = tid - (tid / V) * V;
+          if (v < nvec) {
+            float acc1[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc1[i] = 0.f;
+            uint4 x[L];
+#pragma unroll
+            for (int l = 0; l < L; ++l) x[l] = lds16(sbuf + (size_t)(j * L + l) * 16 * V + 16 * v);
+#pragma unroll
+            for (int l = 0; l < L; ++l) add_bf16x8(acc1, x[l]);
+            float4* o = reinterpret_cast<float4*>(part + v * PS + j * 8);
+            o[0] = make_float4(acc1[0], acc1[1], acc1[2], acc1[3]);
+            o[1] = make_float4(acc1[4], acc1[5], acc1[6], acc1[7]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m.empty[stage]);  // this warp is done reading the stage
+        consumer_barrier();
+#pragma unroll 4
+        for (int e = tid; e < d.n; e += kConsumers) {
+          const int x = e + d.ph;
+          const float* pv = part + (x >> 3) * PS + (x & 7);
+          float acc2 = 0.f;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t node = (k < 4 ? d.ord_lo >> (8 * k) : d.ord_hi >> (8 * (k - 4))) & 0xFFu;
+            if (k < M) acc2 = __fadd_rn(acc2, pv[node * 8]);
+          }
+          __stcs(d.dst + e, acc2);
+        }
+        pb ^= 1;
+      }
+    } else if (d.kind == TILE_PAD) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m.empty[stage]);
+      zero_fill_consumers(d.dst, d.n, tid);
+    } else {  // TILE_DIRECT: contributors at different address phases
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m.empty[stage]);
+      consumer_barrier();  // previous DIRECT tile's readers of src[] are done
+      if (tid < a.N) m.src[tid] = a.grad_tab[(int64_t)d.p * a.N + tid] + d.src_off;
+      consumer_barrier();
+      for (int e0 = tid * 8; e0 < d.n; e0 += kConsumers * 8) {
+        const int cnt = min(8, d.n - e0);
+        float acc2[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc2[i] = 0.f;
+        for (int k = 0; k < M; ++k) {
+          const int node = (int)(((k < 4 ? d.ord_lo >> (8 * k) : d.ord_hi >> (8 * (k - 4)))) & 0xFFu);
+          float acc1[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc1[i] = 0.f;
+#pragma unroll
+          for (int l = 0; l < L; ++l) {
+            const uint16_t* s = m.src[node * L + l] + e0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (i < cnt) acc1[i] = __fadd_rn(acc1[i], __uint_as_float((uint32_t)__ldcs(s + i) << 16));
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc2[i] = __fadd_rn(acc2[i], acc1[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i < cnt) __stcs(d.dst + e0 + i, acc2[i]);
+      }
+    }
+    if (++stage == (uint32_t)a.bulk.stages) {
+      stage = 0;
+      ++round;
+    }
+  }
+}
+
+template <int L>
+__global__ void __launch_bounds__(kConsumers + 32, 1) rs_bulk_kernel(const __grid_constant__ RsArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Smem m = carve(smem, a);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.bulk.stages; ++s) {
+      mbar_init(&m.full[s], 1);
+      mbar_init(&m.empty[s], kConsumerWarps);
+      m.ctl[1 + s] = 0;
+      m.ctl[1 + kMaxBulkStages + s] = 0;
+    }
+    m.ctl[0] = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x >= kConsumers)
+    producer<L>(a, m);
+  else
+    consumers<L>(a, m);
+  __syncthreads();
+  // After an abort, wait (bounded) until every bulk copy this CTA issued has
+  // landed, so that none writes into shared memory after the CTA exits.
+  if (threadIdx.x == 0 && m.ctl[0]) {
+    for (int s = 0; s < a.bulk.stages; ++s) {
+      const int issued = m.ctl[1 + s];
+      if (issued == 0) continue;
+      const uint32_t parity = (uint32_t)(issued - 1) & 1;
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(&m.full[s], parity) && global_ns() - t0 < a.bulk.wait_limit_ns) {
+      }
+    }
+  }
+  __syncthreads();
+}
+
+template <int L>
+int launch_t(const RsArgs& a, int grid, cudaStream_t s) {
+  rs_bulk_kernel<L><<<grid, kConsumers + 32, a.bulk.smem_bytes, s>>>(a);
+  return (int)cudaGetLastError();
+}
+
+template <int L>
+int setup_t(int smem_bytes) {
+  return (int)cudaFuncSetAttribute(rs_bulk_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+}
+
+}  // namespace
+
+BulkLayout rs_bulk_layout(int N, int M, int L, int smem_budget) {
+  BulkLayout b{};
+  b.V = 256 / M;
+  b.PS = 8 * M + (M % 2 == 0 ? 8 : 0);
+  b.stage_bytes = 16 * N * b.V;
+  const int part_bytes = 2 * b.V * b.PS * 4;
+  const int fixed = part_bytes + 1024 + kMaxN * 8 + 4 * 64;
+  int stages = (smem_budget - fixed) / b.stage_bytes;
+  stages = stages < 2 ? 2 : (stages > kMaxBulkStages ? kMaxBulkStages : stages);
+  b.stages = stages;
+  b.off_part = stages * b.stage_bytes;
+  b.off_desc = b.off_part + part_bytes;
+  b.off_bar = b.off_desc + kMaxBulkStages * (int)sizeof(TileDesc);
+  b.off_src = b.off_bar + 2 * kMaxBulkStages * 8;
+  b.off_ctl = b.off_src + kMaxN * 8;
+  b.smem_bytes = b.off_ctl + (1 + 2 * kMaxBulkStages) * 4;
+  (void)L;
+  return b;
+}
+
+int rs_bulk_setup(int L, int smem_bytes) {
+  switch (L) {
+    case 1: return setup_t<1>(smem_bytes);
+    case 2: return setup_t<2>(smem_bytes);
+    case 3: return setup_t<3>(smem_bytes);
+    case 4: return setup_t<4>(smem_bytes);
+    case 5: return setup_t<5>(smem_bytes);
+    case 6: return setup_t<6>(smem_bytes);
+    case 7: return setup_t<7>(smem_bytes);
+    case 8: return setup_t<8>(smem_bytes);
+  }
+  return (int)cudaErrorInvalidValue;
+}
+
+int launch_rs_bulk(const RsArgs& a, int grid, void* stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  switch (a.L) {
+    case 1: return launch_t<1>(a, grid, s);
+    case 2: return launch_t<2>(a, grid, s);
+    case 3: return launch_t<3>(a, grid, s);
+    case 4: return launch_t<4>(a, grid, s);
+    case 5: return launch_t<5>(a, grid, s);
+    case 6: return launch_t<6>(a, grid, s);
+    case 7: return launch_t<7>(a, grid, s);
+    case 8: return launch_t<8>(a, grid, s);
+  }
+  return (int)cudaErrorInvalidValue;
+}
+
+}  // namespace tide

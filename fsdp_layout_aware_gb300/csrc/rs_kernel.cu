@@ -198,32 +198,39 @@ __device__ __forceinline__ void reduce_unaligned(const uint16_t* const* src, con
   }
 }
 
-// CTA b processes items b, b + G, b + 2G, ... (G = grid size): at any moment
-// the CTAs work on neighbouring items, so the contributors are read in nearly
-// address order across the GPU.  The next item's descriptor is fetched while
-// the current one is reduced.
+// CTAs take items in list order from a shared counter (one atomicAdd per
+// item, issued one item ahead so its latency is hidden): the work balances
+// whatever the items' sizes, and at any moment the CTAs are on neighbouring
+// items, so the contributors are read in nearly address order across the GPU.
+// Without a counter (noalloc entry point) CTA b takes items b, b+G, b+2G, ...
 template <int L>
 __global__ void __launch_bounds__(kRsThreads, 4) rs_fused_kernel(const __grid_constant__ RsArgs a) {
   __shared__ const uint16_t* src[kMaxN];
-  if ((int64_t)blockIdx.x >= a.n_items) return;
-  RsItem next = a.items[blockIdx.x];
-  for (int64_t it = blockIdx.x; it < a.n_items; it += gridDim.x) {
-    const RsItem item = next;
-    if (it + gridDim.x < a.n_items) next = a.items[it + gridDim.x];
+  __shared__ long long next_item[2];
+  unsigned long long* counter = a.counter;
+  if (threadIdx.x == 0)
+    next_item[0] = counter ? (long long)atomicAdd(counter, 1ull) : (long long)blockIdx.x;
+  __syncthreads();
+  int slot = 0;
+  for (int64_t it = next_item[0]; it < a.n_items; it = next_item[slot]) {
+    slot ^= 1;
+    if (threadIdx.x == 0)
+      next_item[slot] = counter ? (long long)atomicAdd(counter, 1ull) : (long long)(it + gridDim.x);
+    const RsItem item = a.items[it];
     float* dst = a.shard_tab[item.r] + item.dst_off;
     if (item.kind == RS_PAD) {
       zero_fill(dst, item.n);
-      continue;
+    } else {
+      if ((int)threadIdx.x < a.N)
+        src[threadIdx.x] = a.grad_tab[(int64_t)item.p * a.N + threadIdx.x] + item.src_off;
+      __syncthreads();
+      const uint8_t* ord = a.order + ((item.r / L) * L + item.slice) * a.M;
+      if (a.uniform_phase[item.p])
+        reduce_aligned<L>(src, ord, a.M, dst, item.n);
+      else
+        reduce_unaligned<L>(src, ord, a.M, dst, item.n);
     }
-    __syncthreads();  // the previous item's readers of src[] are done
-    if ((int)threadIdx.x < a.N)
-      src[threadIdx.x] = a.grad_tab[(int64_t)item.p * a.N + threadIdx.x] + item.src_off;
-    __syncthreads();
-    const uint8_t* ord = a.order + ((item.r / L) * L + item.slice) * a.M;
-    if (a.uniform_phase[item.p])
-      reduce_aligned<L>(src, ord, a.M, dst, item.n);
-    else
-      reduce_unaligned<L>(src, ord, a.M, dst, item.n);
+    __syncthreads();  // next_item[slot] is visible; this item's readers of src[] are done
   }
 }
 

@@ -28,9 +28,10 @@ tide_status cuda_fail(cudaError_t err, const char* what) {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Bytes of one per-call pointer table: RS needs [P][N] gradient pointers, [N]
-// shard pointers and [P] phase flags; AG needs [N] shard and [P] param pointers.
+// shard pointers, [P] phase flags and its 8-byte work counter; AG needs [N]
+// shard and [P] param pointers.
 size_t rs_table_bytes(const tide_plan* pl) {
-  return align_up((size_t)pl->P * pl->N * 8 + (size_t)pl->N * 8, 16) + align_up((size_t)pl->P, 16);
+  return align_up((size_t)pl->P * pl->N * 8 + (size_t)pl->N * 8, 16) + align_up((size_t)pl->P, 16) + 16;
 }
 size_t ag_table_bytes(const tide_plan* pl) { return (size_t)pl->N * 8 + (size_t)pl->P * 8; }
 
@@ -47,6 +48,8 @@ void release_device_state(tide_plan* pl) {
   if (pl->d_rs_items) cudaFree(pl->d_rs_items);
   if (pl->d_ag_items) cudaFree(pl->d_ag_items);
   if (pl->d_ag_units) cudaFree(pl->d_ag_units);
+  if (pl->d_status) cudaFree(pl->d_status);
+  pl->d_status = nullptr;
   pl->d_rs_items = nullptr;
   pl->d_ag_items = nullptr;
   pl->d_ag_units = nullptr;
@@ -94,6 +97,23 @@ tide_status ensure_device(tide_plan* pl) {
     if ((err = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess)
       return bail(err, "cudaEventCreate");
     s.done = ev;
+  }
+  if ((err = cudaMalloc(&pl->d_status, sizeof(int))) != cudaSuccess) return bail(err, "cudaMalloc(status)");
+  if ((err = cudaMemset(pl->d_status, 0, sizeof(int))) != cudaSuccess) return bail(err, "cudaMemset(status)");
+  {
+    // Bulk-copy pipeline: one CTA per SM with as many stages as the opt-in
+    // shared memory allows (a little is left for the static allocations).
+    int optin = 0;
+    if ((err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+      return bail(err, "cudaDeviceGetAttribute(smem)");
+    pl->bulk = rs_bulk_layout(pl->N, pl->M, pl->L, optin - 2048);
+    if (pl->bulk.smem_bytes > optin) {
+      release_device_state(pl);
+      return fail(TIDE_ERR_UNIMPLEMENTED, "device has too little shared memory for the bulk-copy pipeline");
+    }
+    if ((err = (cudaError_t)rs_bulk_setup(pl->L, pl->bulk.smem_bytes)) != cudaSuccess)
+      return bail(err, "cudaFuncSetAttribute(rs_bulk)");
+    pl->bulk_grid = (int)std::min<int64_t>(pl->num_sms, std::max<int64_t>(1, pl->rs_items.size()));
   }
   const int rs_occ = rs_blocks_per_sm(pl->L);
   const int ag_occ = ag_blocks_per_sm();
@@ -160,6 +180,44 @@ void tide_plan_destroy(tide_plan* pl) {
   delete pl;
 }
 
+tide_status tide_plan_set_option(tide_plan* pl, int32_t option, int64_t value) {
+  clear_error();
+  if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  switch (option) {
+    case TIDE_OPT_RS_KERNEL:
+      if (value != 0 && value != 1) return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_RS_KERNEL must be 0 or 1");
+      pl->rs_kernel = (int32_t)value;
+      return TIDE_OK;
+    case TIDE_OPT_WAIT_LIMIT_NS:
+      if (value <= 0) return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_WAIT_LIMIT_NS must be positive");
+      pl->wait_limit_ns = (uint64_t)value;
+      return TIDE_OK;
+    case TIDE_OPT_TEST_DROP_TILE:
+      if (value < -1) return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_TEST_DROP_TILE must be >= -1");
+      pl->test_drop_tile = value;
+      return TIDE_OK;
+  }
+  return fail(TIDE_ERR_INVALID_ARG, "unknown option " + std::to_string(option));
+}
+
+tide_status tide_plan_check(tide_plan* pl) {
+  clear_error();
+  if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  if (pl->device < 0 || !pl->d_status) return TIDE_OK;
+  int cur = -1;
+  TIDE_CUDA(cudaGetDevice(&cur), "cudaGetDevice");
+  if (cur != pl->device) TIDE_CUDA(cudaSetDevice(pl->device), "cudaSetDevice");
+  cudaError_t err = cudaDeviceSynchronize();
+  int word = 0;
+  if (err == cudaSuccess) err = cudaMemcpy(&word, pl->d_status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (err == cudaSuccess && word) err = cudaMemset(pl->d_status, 0, sizeof(int));
+  if (cur != pl->device) cudaSetDevice(cur);
+  if (err != cudaSuccess) return cuda_fail(err, "reading the plan's status word");
+  if (word & TIDE_DEVICE_TIMEOUT)
+    return fail(TIDE_ERR_TIMEOUT, "a kernel of this plan gave up a bounded wait; its outputs are undefined");
+  return TIDE_OK;
+}
+
 tide_status tide_rs_reduce(tide_plan* pl, const void* const* grads, float* const* shards, void* stream) {
   clear_error();
   if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
@@ -199,12 +257,15 @@ tide_status tide_rs_reduce(tide_plan* pl, const void* const* grads, float* const
     flags[p] = uniform;
   }
   for (int32_t r = 0; r < pl->N; ++r) stab[r] = shards[r];
-  const size_t bytes = flags_at + (size_t)pl->P;
+  const size_t counter_at = flags_at + align_up((size_t)pl->P, 16);
+  *(unsigned long long*)(slot->host + counter_at) = 0;  // the kernels' work counter starts at item 0
+  const size_t bytes = counter_at + 8;
   cudaStream_t s = (cudaStream_t)stream;
   if ((st = upload_and_mark(slot, bytes, s)) != TIDE_OK) return st;
 
   RsArgs a;
   a.items = pl->d_rs_items;
+  a.counter = (unsigned long long*)(slot->dev + counter_at);
   a.n_items = (int64_t)pl->rs_items.size();
   a.grad_tab = (const uint16_t* const*)slot->dev;
   a.shard_tab = (float* const*)(slot->dev + n_grad * 8);
@@ -214,6 +275,11 @@ tide_status tide_rs_reduce(tide_plan* pl, const void* const* grads, float* const
   a.L = pl->L;
   a.P = pl->P;
   std::memcpy(a.order, pl->order, sizeof(a.order));
+  a.bulk = pl->bulk;
+  a.bulk.status = pl->d_status;
+  a.bulk.wait_limit_ns = pl->wait_limit_ns;
+  a.bulk.test_drop_tile = pl->test_drop_tile;
+  if (pl->rs_kernel == 1) return finish(slot, launch_rs_bulk(a, pl->bulk_grid, stream), s, "rs_bulk launch");
   return finish(slot, launch_rs(a, pl->rs_grid, stream), s, "rs_fused launch");
 }
 

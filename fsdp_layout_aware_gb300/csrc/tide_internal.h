@@ -93,13 +93,30 @@ struct UnitStart {
   int32_t off;
 };
 
+// Bulk-copy pipeline of the reduce-scatter (rs_bulk.cu): tile geometry and
+// shared-memory carve-up, fixed per plan when it is set up on a device.
+constexpr int kMaxBulkStages = 16;
+constexpr int TIDE_DEVICE_TIMEOUT = 1;  // status-word bit: a kernel gave up waiting
+struct BulkLayout {
+  int32_t V;            // 8-element vectors per tile (256 / M)
+  int32_t PS;           // floats per vector row of the transposition buffer
+  int32_t stage_bytes;  // 16 * N * V
+  int32_t stages;
+  int32_t off_part, off_desc, off_bar, off_src, off_ctl, smem_bytes;
+  int* status;              // plan's device status word
+  uint64_t wait_limit_ns;   // bound on every wait
+  int64_t test_drop_tile;   // tile whose data the producer withholds (tests); -1: none
+};
+
 struct RsArgs {
   const RsItem* items;
   int64_t n_items;
+  unsigned long long* counter;      // next item to take (zero at launch); NULL: round-robin
   const uint16_t* const* grad_tab;  // [P][N]: contributor src's gradient of p
   float* const* shard_tab;          // [N]
   const uint8_t* uniform_phase;     // [P]: 1 if all N gradients of p share addr mod 16
   int32_t N, M, L, P;
+  BulkLayout bulk;                  // rs_bulk only
   uint8_t order[kOrderTableSize];
 };
 
@@ -116,6 +133,9 @@ struct AgArgs {
 // Launchers (rs_kernel.cu / ag_kernel.cu).  Return the cudaError_t as int.
 int launch_rs(const RsArgs& args, int grid, void* stream);
 int launch_ag(const AgArgs& args, int grid, void* stream);
+int launch_rs_bulk(const RsArgs& args, int grid, void* stream);
+BulkLayout rs_bulk_layout(int N, int M, int L, int smem_budget);
+int rs_bulk_setup(int L, int smem_bytes);  // raises the kernel's dynamic shared-memory limit
 // Resident CTAs per SM of each kernel (occupancy), for grid sizing.
 int rs_blocks_per_sm(int L);
 int ag_blocks_per_sm();
@@ -135,7 +155,13 @@ struct tide_plan {
   // Device state, created by the first compute call.
   int device = -1;
   int num_sms = 0;
-  int rs_grid = 0, ag_grid = 0;
+  int rs_grid = 0, ag_grid = 0, bulk_grid = 0;
+  int* d_status = nullptr;                 // device status word (TIDE_DEVICE_TIMEOUT)
+  tide::BulkLayout bulk{};
+  // Options (tide_plan_set_option).
+  int32_t rs_kernel = 0;                   // 0: direct loads (rs_fused), 1: bulk-copy pipeline
+  uint64_t wait_limit_ns = 2000000000ull;  // 2 s
+  int64_t test_drop_tile = -1;
   tide::RsItem* d_rs_items = nullptr;
   tide::AgItem* d_ag_items = nullptr;
   tide::UnitStart* d_ag_units = nullptr;

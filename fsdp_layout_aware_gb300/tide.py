@@ -23,8 +23,11 @@ TIDE_OK = 0
 STATUS_NAMES = {
     0: "TIDE_OK", 1: "TIDE_ERR_INVALID_ARG", 2: "TIDE_ERR_ALIGNMENT", 3: "TIDE_ERR_OVERFLOW",
     4: "TIDE_ERR_OUT_OF_MEMORY", 5: "TIDE_ERR_CUDA", 6: "TIDE_ERR_UNIMPLEMENTED",
-    7: "TIDE_ERR_DEVICE_MISMATCH",
+    7: "TIDE_ERR_DEVICE_MISMATCH", 8: "TIDE_ERR_TIMEOUT",
 }
+TIDE_OPT_RS_KERNEL = 1
+TIDE_OPT_WAIT_LIMIT_NS = 2
+TIDE_OPT_TEST_DROP_TILE = 3
 ITEM_FIELDS = ("kind", "p", "r", "src_off", "dst_off", "n")
 
 
@@ -57,6 +60,8 @@ def _load():
         "tide_rs_reduce": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
         "tide_ag_place": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp]),
         "tide_rs_reduce_noalloc": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
+        "tide_plan_set_option": (i32, [vp, i32, i64]),
+        "tide_plan_check": (i32, [vp]),
         "tide_status_string": (ctypes.c_char_p, [i32]),
         "tide_last_error": (ctypes.c_char_p, []),
     }
@@ -115,6 +120,15 @@ def tide_plan_create(shapes, N, M, L):
 
 def tide_plan_destroy(plan):
     _lib.tide_plan_destroy(plan)
+
+
+def tide_plan_set_option(plan, option, value):
+    _check(_lib.tide_plan_set_option(plan, option, value))
+
+
+def tide_plan_check(plan):
+    """Synchronise and raise TideError(TIDE_ERR_TIMEOUT) if a kernel gave up a wait."""
+    _check(_lib.tide_plan_check(plan))
 
 
 def tide_plan_shard_elems(plan):
@@ -184,6 +198,12 @@ class TidePlan:
 
     def items(self, which):
         return tide_plan_items(self.handle, which)
+
+    def set_option(self, option, value):
+        tide_plan_set_option(self.handle, option, value)
+
+    def check(self):
+        tide_plan_check(self.handle)
 
     def level2_order(self, n_dest, s):
         return tide_plan_level2_order(self.handle, n_dest, s, self.M)

@@ -59,7 +59,9 @@ typedef enum tide_status {
   TIDE_ERR_OUT_OF_MEMORY = 4,   /* host or device allocation failed          */
   TIDE_ERR_CUDA = 5,            /* a CUDA runtime call failed                */
   TIDE_ERR_UNIMPLEMENTED = 6,   /* valid request outside what is built       */
-  TIDE_ERR_DEVICE_MISMATCH = 7  /* plan used on another device than its own  */
+  TIDE_ERR_DEVICE_MISMATCH = 7, /* plan used on another device than its own  */
+  TIDE_ERR_TIMEOUT = 8          /* a kernel gave up a bounded wait (see
+                                   tide_plan_check)                          */
 } tide_status;
 
 /* A parameter group over N = M*L ranks ([Abstract] Table 2).
@@ -125,6 +127,37 @@ tide_status tide_plan_get_items(const tide_plan* plan, int32_t which, int64_t* o
  * Figure 6(b): destination GPU g = 0..L-1 holds the partial of the source
  * with relative index c = (s - g) mod L, if c < M.  Errors: INVALID_ARG. */
 tide_status tide_plan_level2_order(const tide_plan* plan, int32_t n_dest, int32_t s, int32_t* out);
+
+/* Plan options, set before or between calls (never while a call of the
+ * plan is in flight on another thread).
+ *   TIDE_OPT_RS_KERNEL     0 (default): every thread loads its
+ *                          contributions directly (16-byte loads); 1: a
+ *                          producer warp streams the contributors into shared
+ *                          memory with bulk copies (TMA).  Both add in the
+ *                          same order and give bit-identical results; the
+ *                          bulk path pays one copy request per contributor
+ *                          window, so it suits groups with few ranks.
+ *   TIDE_OPT_WAIT_LIMIT_NS bound, in nanoseconds, on every wait inside the
+ *                          bulk-copy kernel (default 2e9).  A kernel that runs
+ *                          out records TIDE_ERR_TIMEOUT for tide_plan_check,
+ *                          drains its copies and returns; the outputs of that
+ *                          call are then undefined.
+ *   TIDE_OPT_TEST_DROP_TILE  test hook: the bulk kernel's producer withholds
+ *                          the given tile (counted per CTA from 0), so the
+ *                          consumers' wait runs out; -1 (default) disables.
+ * Errors: INVALID_ARG for an unknown option or value. */
+typedef enum tide_option {
+  TIDE_OPT_RS_KERNEL = 1,
+  TIDE_OPT_WAIT_LIMIT_NS = 2,
+  TIDE_OPT_TEST_DROP_TILE = 3
+} tide_option;
+tide_status tide_plan_set_option(tide_plan* plan, int32_t option, int64_t value);
+
+/* Synchronise the device the plan runs on and report whether any of the
+ * plan's kernels gave up a bounded wait since the last check
+ * (TIDE_ERR_TIMEOUT; the flag is then cleared).  TIDE_OK for a plan that has
+ * not run yet.  Errors: INVALID_ARG, CUDA. */
+tide_status tide_plan_check(tide_plan* plan);
 
 /* TIDE-RS: per-parameter bf16 gradients read in place, reduced in fp32
  * straight into every rank's packed fp32 shard at its final offset

@@ -183,3 +183,17 @@ def test_cuda_failure_is_a_status_without_a_gpu():
         with pytest.raises(tide.TideError) as err:
             plan.rs_reduce([0x10000 * (i + 1) for i in range(4)], [0x1000000 * (r + 1) for r in range(4)], stream=0)
         assert err.value.status == 5
+
+
+def test_plan_options_validate_without_a_gpu():
+    with tide.TidePlan([(8, 64)], 4, 1, 4) as plan:
+        plan.set_option(tide.TIDE_OPT_RS_KERNEL, 1)
+        plan.set_option(tide.TIDE_OPT_RS_KERNEL, 0)
+        plan.set_option(tide.TIDE_OPT_WAIT_LIMIT_NS, 1000)
+        plan.set_option(tide.TIDE_OPT_TEST_DROP_TILE, -1)
+        plan.check()   # never ran on a device: nothing to report
+        for opt, val in [(tide.TIDE_OPT_RS_KERNEL, 2), (tide.TIDE_OPT_WAIT_LIMIT_NS, 0),
+                         (tide.TIDE_OPT_TEST_DROP_TILE, -2), (99, 0)]:
+            with pytest.raises(tide.TideError) as err:
+                plan.set_option(opt, val)
+            assert err.value.status == 1

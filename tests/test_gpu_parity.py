@@ -303,3 +303,45 @@ def test_full_size_rs_ag_sampled(cfg):
                 assert ((got - exact).abs() <= gamma * mag).all(), f"param {p}: error bound"
         del grads, shards, ag_in, params
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------- kernel choice and waits
+
+@pytest.mark.parametrize("w", [SMALL[0], SMALL[2], SMALL[4], SMALL[5], SMALL[6]], ids=lambda w: w.name)
+def test_rs_bulk_kernel_bit_exact(w):
+    """The bulk-copy kernel (TIDE_OPT_RS_KERNEL = 1) gives the oracle's bits too."""
+    grads = host_grads(w)
+    geo, expect = oracle_rs(w, grads)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        plan.set_option(tide.TIDE_OPT_RS_KERNEL, 1)
+        dev = [[to_dev_u16(grads[r][p])[0] for p in range(w.P)] for r in range(w.N)]
+        outs = [f32_guarded(geo.S, GUARD, GUARD) for _ in range(w.N)]
+        run_rs(plan, dev, [o[0] for o in outs])
+        plan.check()
+        for r in range(w.N):
+            assert np.array_equal(f32_bits(outs[r][0]), expect[r].view(np.uint32)), r
+
+
+def test_bulk_kernel_wait_runs_out_and_context_survives():
+    """Withhold one tile's data so the bulk kernel's bounded wait runs out: the
+    plan reports TIDE_ERR_TIMEOUT, and the next call on the same context is
+    exact again."""
+    w = SMALL[1]
+    grads = host_grads(w)
+    geo, expect = oracle_rs(w, grads)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        dev = [[to_dev_u16(grads[r][p])[0] for p in range(w.P)] for r in range(w.N)]
+        outs = [torch.empty(geo.S, dtype=torch.float32, device=DEV) for _ in range(w.N)]
+        plan.set_option(tide.TIDE_OPT_RS_KERNEL, 1)
+        plan.set_option(tide.TIDE_OPT_WAIT_LIMIT_NS, 20_000_000)
+        plan.set_option(tide.TIDE_OPT_TEST_DROP_TILE, 1)
+        run_rs(plan, dev, outs)
+        with pytest.raises(tide.TideError) as err:
+            plan.check()
+        assert err.value.status == 8
+        plan.set_option(tide.TIDE_OPT_TEST_DROP_TILE, -1)
+        plan.set_option(tide.TIDE_OPT_WAIT_LIMIT_NS, 2_000_000_000)
+        run_rs(plan, dev, outs)
+        plan.check()
+        for r in range(w.N):
+            assert np.array_equal(f32_bits(outs[r]), expect[r].view(np.uint32)), r
