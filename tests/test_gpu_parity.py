@@ -347,3 +347,23 @@ def test_bulk_kernel_wait_runs_out_and_context_survives():
         plan.check()
         for r in range(w.N):
             assert np.array_equal(f32_bits(outs[r]), expect[r].view(np.uint32)), r
+
+
+def test_host_buffers_through_the_c_abi():
+    """Pinned host memory passed straight to the C ABI (the kernels read and
+    write it over the host link): same bits as the oracle."""
+    w = SMALL[5]
+    grads = host_grads(w)
+    geo, expect = oracle_rs(w, grads)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        h = [[torch.from_numpy(grads[r][p].view(np.int16)).pin_memory() for p in range(w.P)] for r in range(w.N)]
+        shards = [torch.full((geo.S,), float("nan"), dtype=torch.float32).pin_memory() for _ in range(w.N)]
+        run_rs(plan, h, shards)
+        params = [torch.empty(w.N * geo.e[p], dtype=torch.float32).pin_memory() for p in range(w.P)]
+        plan.ag_place(shards, params, 4)
+        torch.cuda.synchronize()
+        for r in range(w.N):
+            assert np.array_equal(shards[r].numpy().view(np.uint32), expect[r].view(np.uint32)), r
+        gathered = O.ag_place(geo, expect)
+        for p in range(w.P):
+            assert np.array_equal(params[p].numpy().view(np.uint32), gathered[p].view(np.uint32)), p
