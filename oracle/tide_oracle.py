@@ -278,3 +278,55 @@ def ag_element(geo, p, y, shard_at):
     """Element y of parameter p's gathered block, from ``shard_at(r, idx)``."""
     r, e = divmod(y, geo.e[p])
     return shard_at(r, np.array([geo.o[p] + e], dtype=np.int64))[0]
+
+
+# --------------------------------------------------------------------------
+# All-gather across nodes by recursive doubling ([Endgame] "All-gather:
+# parameters land at their final address"; [Abstract] Figure 5).  On rail l
+# (GPU l of every node) each node starts with its own piece; in round d
+# (from 0) a node sends the first min(2^d, M - 2^d) pieces it has collected
+# to the node 2^d lower and receives as many from the node 2^d higher
+# (modulo M), appending them in arrival order.
+# --------------------------------------------------------------------------
+
+def rd_send_count(M, d):
+    """Pieces each node sends in round d."""
+    return min(2 ** d, M - 2 ** d)
+
+
+def rd_rounds(M):
+    """Rounds until every node holds every piece: rounds run while 2^d < M."""
+    d = 0
+    while 2 ** d < M:
+        d += 1
+    return d
+
+
+def rd_simulate(M):
+    """Collected pieces (source node numbers, in arrival order) of every node
+    after each round: a list of rounds, each a list of M lists."""
+    have = [[n] for n in range(M)]
+    history = []
+    for d in range(rd_rounds(M)):
+        c = rd_send_count(M, d)
+        sent = [list(have[n][:c]) for n in range(M)]          # what each node sends this round
+        for n in range(M):
+            have[n] = have[n] + sent[(n + 2 ** d) % M]        # received from the node 2^d higher
+        history.append([list(h) for h in have])
+    return history
+
+
+def rd_stage_place(geo, stage, node, rail, L, params):
+    """Place rail `rail`'s pieces from node `node`'s stage buffer into params.
+
+    stage[k] is the packed shard held in stage slot k (arrival order), which
+    is node (node + k) mod M's shard on this rail, i.e. rank
+    ((node + k) mod M) * L + rail.  Every parameter receives its M pieces of
+    this rail at their parameter-major offsets ([Abstract] Figure 5(b))."""
+    M = len(stage)
+    for p in range(geo.P):
+        e_p, o_p = geo.e[p], geo.o[p]
+        for k in range(M):
+            r = ((node + k) % M) * L + rail
+            params[p][r * e_p:(r + 1) * e_p] = stage[k][o_p:o_p + e_p]
+    return params

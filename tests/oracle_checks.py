@@ -313,4 +313,43 @@ def check_ag_of_rs_round_trip():
             assert (full[p][n:].view(np.uint32) == 0).all()
 
 
+# ------------------------------------------------------ recursive doubling
+
+def check_recursive_doubling_page_facts():
+    g = _golden("recursive_doubling.json")
+    for m, rounds in g["rounds"].items():
+        assert O.rd_rounds(int(m)) == rounds
+    assert O.rd_rounds(8) < g["ring_rounds"]["8"] == 8 - 1
+    assert [O.rd_send_count(5, d) for d in range(O.rd_rounds(5))] == g["send_counts_M5"]
+
+
+def check_recursive_doubling_bruteforce():
+    """For M = 1..64: every node ends with every piece exactly once, after
+    ceil(log2 M) rounds, and node n's k-th piece is node (n + k) mod M's."""
+    import math
+    for M in range(1, 65):
+        hist = O.rd_simulate(M)
+        assert len(hist) == (math.ceil(math.log2(M)) if M > 1 else 0)
+        final = hist[-1] if hist else [[n] for n in range(M)]
+        for n in range(M):
+            assert final[n] == [(n + k) % M for k in range(M)], (M, n)
+        for d, state in enumerate(hist):  # counts double until the last round
+            assert all(len(h) == min(2 ** (d + 1), M) for h in state)
+
+
+def check_stage_place_equals_direct_landing():
+    """Placing every rail's stage buffer of one node gives the direct all-gather."""
+    for shapes, M, L in _tiny_groups():
+        N = M * L
+        geo = O.geometry(shapes, N)
+        shards = [np.arange(r * geo.S, (r + 1) * geo.S, dtype=np.int64) for r in range(N)]
+        direct = O.ag_place(geo, shards)
+        for node in range(M):
+            params = [np.full(N * e, -1, dtype=np.int64) for e in geo.e]
+            for rail in range(L):
+                stage = [shards[((node + k) % M) * L + rail] for k in range(M)]
+                O.rd_stage_place(geo, stage, node, rail, L, params)
+            assert all(np.array_equal(a, b) for a, b in zip(params, direct))
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

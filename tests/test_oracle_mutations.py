@@ -40,6 +40,10 @@ MUTATIONS = {
     "accumulators start at first term": [
         ("acc1 = np.zeros(count, dtype=np.float32)", "acc1 = np.full(count, -0.0, dtype=np.float32)"),
         ("acc2 = np.zeros(b - a, dtype=np.float32)", "acc2 = np.full(b - a, -0.0, dtype=np.float32)")],
+    "recursive doubling sends 2^d": ("return min(2 ** d, M - 2 ** d)", "return 2 ** d"),
+    "recursive doubling from the lower node": ("have[n] = have[n] + sent[(n + 2 ** d) % M]",
+                                               "have[n] = have[n] + sent[(n - 2 ** d) % M]"),
+    "stage slot rotated the wrong way": ("r = ((node + k) % M) * L + rail", "r = ((node - k) % M) * L + rail"),
     "AG piece offset": ("block[r * e_p:(r + 1) * e_p] = shards[r][o_p:o_p + e_p]",
                         "block[r * e_p:(r + 1) * e_p] = shards[(r + 1) % geo.N][o_p:o_p + e_p]"),
 }
