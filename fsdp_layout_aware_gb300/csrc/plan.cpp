@@ -119,6 +119,13 @@ std::vector<UnitStart> unit_starts(const std::vector<Item>& items, const std::ve
 }
 }  // namespace
 
+std::vector<UnitStart> ag_unit_starts_of(const std::vector<AgItem>& items, int64_t workers, int64_t target,
+                                         int64_t max_k) {
+  std::vector<int64_t> prefix(items.size() + 1, 0);
+  for (size_t i = 0; i < items.size(); ++i) prefix[i + 1] = prefix[i] + ag_item_cost(items[i]);
+  return unit_starts(items, prefix, workers, target, max_k, [](const AgItem& it, int64_t rel) { return ag_split(it, rel); });
+}
+
 std::vector<UnitStart> ag_unit_starts(const tide_plan* pl, int64_t workers, int64_t target, int64_t max_k) {
   return unit_starts(pl->ag_items, pl->ag_prefix, workers, target, max_k,
                      [](const AgItem& it, int64_t rel) { return ag_split(it, rel); });
@@ -229,6 +236,19 @@ tide_status tide_plan_create(const tide_group_desc* d, tide_plan** out_plan) {
   }
   *out_plan = pl;
   return TIDE_OK;
+}
+
+int32_t tide_rd_rounds(int32_t M) {
+  if (M < 1) return -1;
+  int32_t d = 0;
+  while ((int64_t(1) << d) < M) ++d;  // rounds run while 2^d < M
+  return d;
+}
+
+int32_t tide_rd_send_count(int32_t M, int32_t d) {
+  if (M < 1 || d < 0 || d >= tide_rd_rounds(M)) return -1;
+  const int64_t half = int64_t(1) << d;
+  return (int32_t)std::min<int64_t>(half, M - half);
 }
 
 int64_t tide_plan_shard_elems(const tide_plan* pl) { return pl ? pl->S : -1; }

@@ -48,6 +48,13 @@ void release_device_state(tide_plan* pl) {
   if (pl->d_rs_items) cudaFree(pl->d_rs_items);
   if (pl->d_ag_items) cudaFree(pl->d_ag_items);
   if (pl->d_ag_units) cudaFree(pl->d_ag_units);
+  for (int l = 0; l < kMaxL; ++l) {
+    if (pl->d_rail_items[l]) cudaFree(pl->d_rail_items[l]);
+    if (pl->d_rail_units[l]) cudaFree(pl->d_rail_units[l]);
+    pl->d_rail_items[l] = nullptr;
+    pl->d_rail_units[l] = nullptr;
+    pl->rail_n_items[l] = pl->rail_n_units[l] = 0;
+  }
   if (pl->d_status) cudaFree(pl->d_status);
   pl->d_status = nullptr;
   pl->d_rs_items = nullptr;
@@ -128,6 +135,26 @@ tide_status ensure_device(tide_plan* pl) {
   try {
     const std::vector<UnitStart> au = ag_unit_starts(pl, (int64_t)pl->ag_grid * (kAgThreads / 32), 16 << 10, 32);
     pl->ag_units = (int64_t)au.size() - 1;
+    // Per-rail item lists for tide_ag_stage_place.
+    for (int l = 0; l < pl->L; ++l) {
+      std::vector<AgItem> ri;
+      for (const AgItem& it : pl->ag_items)
+        if (it.r % pl->L == l) ri.push_back(it);
+      pl->rail_n_items[l] = (int64_t)ri.size();
+      if (ri.empty()) continue;
+      const std::vector<UnitStart> ru = ag_unit_starts_of(ri, (int64_t)pl->ag_grid * (kAgThreads / 32), 16 << 10, 32);
+      pl->rail_n_units[l] = (int64_t)ru.size() - 1;
+      if ((err = cudaMalloc(&pl->d_rail_items[l], ri.size() * sizeof(AgItem))) != cudaSuccess)
+        return bail(err, "cudaMalloc(rail items)");
+      if ((err = cudaMemcpy(pl->d_rail_items[l], ri.data(), ri.size() * sizeof(AgItem), cudaMemcpyHostToDevice)) !=
+          cudaSuccess)
+        return bail(err, "cudaMemcpy(rail items)");
+      if ((err = cudaMalloc(&pl->d_rail_units[l], ru.size() * sizeof(UnitStart))) != cudaSuccess)
+        return bail(err, "cudaMalloc(rail units)");
+      if ((err = cudaMemcpy(pl->d_rail_units[l], ru.data(), ru.size() * sizeof(UnitStart), cudaMemcpyHostToDevice)) !=
+          cudaSuccess)
+        return bail(err, "cudaMemcpy(rail units)");
+    }
     if ((err = cudaMalloc(&pl->d_ag_units, au.size() * sizeof(UnitStart))) != cudaSuccess)
       return bail(err, "cudaMalloc(ag units)");
     if ((err = cudaMemcpy(pl->d_ag_units, au.data(), au.size() * sizeof(UnitStart), cudaMemcpyHostToDevice)) !=
@@ -319,6 +346,73 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
   a.param_tab = (unsigned char* const*)(slot->dev + (size_t)pl->N * 8);
   a.elem_bytes = elem_bytes;
   return finish(slot, launch_ag(a, pl->ag_grid, stream), s, "ag_place launch");
+}
+
+tide_status tide_ag_rd_exchange(tide_plan* pl, void* const* stages, int32_t elem_bytes, void* stream) {
+  clear_error();
+  if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  if (elem_bytes != 2 && elem_bytes != 4) return fail(TIDE_ERR_INVALID_ARG, "elem_bytes must be 2 or 4");
+  if (pl->S == 0 || pl->M == 1) return TIDE_OK;
+  if (!stages) return fail(TIDE_ERR_INVALID_ARG, "stages array is NULL");
+  for (int32_t n = 0; n < pl->M; ++n) {
+    if (!stages[n]) return fail(TIDE_ERR_INVALID_ARG, "stages[" + std::to_string(n) + "] is NULL");
+    for (int32_t m = 0; m < n; ++m)
+      if (stages[m] == stages[n]) return fail(TIDE_ERR_INVALID_ARG, "two nodes share a stage buffer");
+  }
+  const size_t piece = (size_t)pl->S * elem_bytes;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int32_t rounds = tide_rd_rounds(pl->M);
+  for (int32_t d = 0; d < rounds; ++d) {
+    const int32_t have = 1 << d;                     // pieces every node holds before round d
+    const int32_t c = tide_rd_send_count(pl->M, d);  // pieces sent this round
+    for (int32_t n = 0; n < pl->M; ++n) {
+      const unsigned char* from = (const unsigned char*)stages[(n + have) % pl->M];
+      unsigned char* to = (unsigned char*)stages[n] + (size_t)have * piece;
+      TIDE_CUDA(cudaMemcpyAsync(to, from, (size_t)c * piece, cudaMemcpyDeviceToDevice, s), "exchange copy");
+    }
+  }
+  return TIDE_OK;
+}
+
+tide_status tide_ag_stage_place(tide_plan* pl, const void* stage, int32_t node, int32_t rail, void* const* params,
+                                int32_t elem_bytes, void* stream) {
+  clear_error();
+  if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  if (elem_bytes != 2 && elem_bytes != 4) return fail(TIDE_ERR_INVALID_ARG, "elem_bytes must be 2 or 4");
+  if (node < 0 || node >= pl->M || rail < 0 || rail >= pl->L) return fail(TIDE_ERR_INVALID_ARG, "node or rail out of range");
+  if (pl->ag_items.empty()) return TIDE_OK;
+  if (!stage || !params) return fail(TIDE_ERR_INVALID_ARG, "stage or params is NULL");
+  if ((uintptr_t)stage % elem_bytes) return fail(TIDE_ERR_ALIGNMENT, "stage pointer not element-aligned");
+  for (int32_t p = 0; p < pl->P; ++p) {
+    if (pl->e[p] == 0) continue;
+    if (!params[p]) return fail(TIDE_ERR_INVALID_ARG, "params[" + std::to_string(p) + "] is NULL");
+    if ((uintptr_t)params[p] % elem_bytes) return fail(TIDE_ERR_ALIGNMENT, "param pointer not element-aligned");
+  }
+  tide_status st = ensure_device(pl);
+  if (st != TIDE_OK) return st;
+  if (pl->rail_n_items[rail] == 0) return TIDE_OK;
+  tide_plan::Slot* slot = nullptr;
+  if ((st = acquire_slot(pl, &slot)) != TIDE_OK) return st;
+  // Shard table indexed by rank: rank ((node + k) mod M) * L + rail reads slot k.
+  const unsigned char** stab = (const unsigned char**)slot->host;
+  void** ptab = (void**)(slot->host + (size_t)pl->N * 8);
+  for (int32_t r = 0; r < pl->N; ++r) stab[r] = nullptr;
+  for (int32_t k = 0; k < pl->M; ++k) {
+    const int32_t r = ((node + k) % pl->M) * pl->L + rail;
+    stab[r] = (const unsigned char*)stage + (size_t)k * pl->S * elem_bytes;
+  }
+  for (int32_t p = 0; p < pl->P; ++p) ptab[p] = params[p];
+  cudaStream_t s = (cudaStream_t)stream;
+  if ((st = upload_and_mark(slot, ag_table_bytes(pl), s)) != TIDE_OK) return st;
+  AgArgs a;
+  a.items = pl->d_rail_items[rail];
+  a.n_items = pl->rail_n_items[rail];
+  a.units = pl->d_rail_units[rail];
+  a.n_units = pl->rail_n_units[rail];
+  a.shard_tab = (const unsigned char* const*)slot->dev;
+  a.param_tab = (unsigned char* const*)(slot->dev + (size_t)pl->N * 8);
+  a.elem_bytes = elem_bytes;
+  return finish(slot, launch_ag(a, pl->ag_grid, stream), s, "ag_place (stage) launch");
 }
 
 }  // extern "C"

@@ -166,6 +166,12 @@ struct tide_plan {
   tide::AgItem* d_ag_items = nullptr;
   tide::UnitStart* d_ag_units = nullptr;
   int64_t ag_units = 0;
+  // Per-rail all-gather work (tide_ag_stage_place): rail l's items (ranks
+  // r = n*L + l) and their equal-cost units.
+  tide::AgItem* d_rail_items[tide::kMaxL] = {};
+  tide::UnitStart* d_rail_units[tide::kMaxL] = {};
+  int64_t rail_n_items[tide::kMaxL] = {};
+  int64_t rail_n_units[tide::kMaxL] = {};
   static constexpr int kRing = 8;
   struct Slot {
     unsigned char* host = nullptr;
@@ -181,6 +187,8 @@ namespace tide {
 // Equal-cost all-gather unit boundaries for W workers (plan.cpp); at most
 // max_k units per worker, each worth about `target` cost units.
 std::vector<UnitStart> ag_unit_starts(const tide_plan* pl, int64_t workers, int64_t target, int64_t max_k);
+std::vector<UnitStart> ag_unit_starts_of(const std::vector<AgItem>& items, int64_t workers, int64_t target,
+                                         int64_t max_k);
 // Thread-local error reporting (plan.cpp).
 tide_status fail(tide_status st, const std::string& msg);
 void clear_error();

@@ -62,6 +62,10 @@ def _load():
         "tide_rs_reduce_noalloc": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
         "tide_plan_set_option": (i32, [vp, i32, i64]),
         "tide_plan_check": (i32, [vp]),
+        "tide_rd_rounds": (i32, [i32]),
+        "tide_rd_send_count": (i32, [i32, i32]),
+        "tide_ag_rd_exchange": (i32, [vp, ctypes.POINTER(vp), i32, vp]),
+        "tide_ag_stage_place": (i32, [vp, vp, i32, i32, ctypes.POINTER(vp), i32, vp]),
         "tide_status_string": (ctypes.c_char_p, [i32]),
         "tide_last_error": (ctypes.c_char_p, []),
     }
@@ -143,6 +147,24 @@ def tide_plan_create(shapes, N, M, L):
 
 def tide_plan_destroy(plan):
     _lib.tide_plan_destroy(plan)
+
+
+def tide_rd_rounds(M):
+    return int(_lib.tide_rd_rounds(M))
+
+
+def tide_rd_send_count(M, d):
+    return int(_lib.tide_rd_send_count(M, d))
+
+
+def tide_ag_rd_exchange(plan, stages, elem_bytes, stream=None):
+    """stages: M device buffers of M*S elements (slot 0 = the node's own shard)."""
+    _check(_lib.tide_ag_rd_exchange(plan, _ptr_array(stages), elem_bytes, _stream(stream)))
+
+
+def tide_ag_stage_place(plan, stage, node, rail, params, elem_bytes, stream=None):
+    _check(_lib.tide_ag_stage_place(plan, _ptr(stage), node, rail, _ptr_array(params), elem_bytes,
+                                    _stream(stream)))
 
 
 def tide_plan_set_option(plan, option, value):

@@ -223,6 +223,43 @@ tide_status tide_ag_place(tide_plan* plan, const void* const* shards, void* cons
 tide_status tide_rs_reduce_noalloc(const tide_plan* plan, const void* const* grads, float* const* shards,
                                    void* stream);
 
+/* ---- All-gather across nodes by recursive doubling ----------------------
+ * [Endgame] "All-gather: parameters land at their final address" and
+ * [Abstract] Figure 5: on rail l (GPU l of every node) each node starts with
+ * its own packed shard; in round d = 0, 1, ... a node sends the first
+ * min(2^d, M - 2^d) pieces it has collected to node (n - 2^d) mod M and
+ * appends as many from node (n + 2^d) mod M.  After ceil(log2 M) rounds node
+ * n's stage slot k holds node (n + k) mod M's shard (rank
+ * ((n + k) mod M) * L + l). */
+
+/* Rounds the exchange needs: ceil(log2 M) (0 for M = 1); -1 if M < 1. */
+int32_t tide_rd_rounds(int32_t M);
+
+/* Pieces each node sends in round d: min(2^d, M - 2^d); -1 if d is not a
+ * round of the exchange. */
+int32_t tide_rd_send_count(int32_t M, int32_t d);
+
+/* Emulate one rail's exchange between the M nodes' stage buffers on this GPU.
+ *   stages      host array [M] of device pointers; stages[n] holds M packed
+ *               shards of S elements (slot k at k*S); slot 0 must already
+ *               hold node n's own shard.  Slots 1..M-1 are overwritten.
+ *   elem_bytes  2 or 4
+ * Every round is one device-to-device copy per node (copy engines, as the
+ * pages' transport), enqueued on `stream` in round order.
+ * Errors: INVALID_ARG (null or aliasing buffers), CUDA. */
+tide_status tide_ag_rd_exchange(tide_plan* plan, void* const* stages, int32_t elem_bytes, void* stream);
+
+/* Destination phase of the exchange ([Abstract] Figure 5(b)): write rail
+ * `rail`'s M pieces from node `node`'s stage buffer (slot k = rank
+ * ((node + k) mod M) * L + rail, S elements each) into the parameters'
+ * parameter-major blocks, every piece once at its final address:
+ * params[p][r*e_p + e] = stage[k*S + op + e].  Same kernel and the same
+ * argument rules as tide_ag_place; `stage` is a device pointer to M*S
+ * elements.  Errors: INVALID_ARG, ALIGNMENT, CUDA, OUT_OF_MEMORY,
+ * DEVICE_MISMATCH. */
+tide_status tide_ag_stage_place(tide_plan* plan, const void* stage, int32_t node, int32_t rail,
+                                void* const* params, int32_t elem_bytes, void* stream);
+
 /* Static text for a status code. */
 const char* tide_status_string(tide_status status);
 

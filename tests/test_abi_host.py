@@ -207,3 +207,12 @@ def test_pointer_array_is_passed_through():
         with pytest.raises(tide.TideError) as err:
             plan.rs_reduce(bad, tide.pointer_array([0x100000] * 4), stream=0)
         assert err.value.status == 2
+
+
+def test_recursive_doubling_schedule_matches_oracle():
+    for M in range(1, 65):
+        assert tide.tide_rd_rounds(M) == O.rd_rounds(M)
+        for d in range(O.rd_rounds(M)):
+            assert tide.tide_rd_send_count(M, d) == O.rd_send_count(M, d)
+        assert tide.tide_rd_send_count(M, O.rd_rounds(M)) == -1
+    assert tide.tide_rd_rounds(0) == -1

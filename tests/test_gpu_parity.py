@@ -367,3 +367,35 @@ def test_host_buffers_through_the_c_abi():
         gathered = O.ag_place(geo, expect)
         for p in range(w.P):
             assert np.array_equal(params[p].numpy().view(np.uint32), gathered[p].view(np.uint32)), p
+
+
+@pytest.mark.parametrize("w", [SMALL[0], SMALL[3], SMALL[4], SMALL[5]], ids=lambda w: w.name)
+@pytest.mark.parametrize("elem_bytes", [2, 4])
+def test_ag_by_recursive_doubling_matches_direct_landing(w, elem_bytes):
+    """All-gather the pages' way -- per rail, recursive-doubling exchange
+    between the nodes' stage buffers, then the strided stage placement --
+    must land every piece exactly where the direct all-gather does."""
+    geo = O.geometry(w.shapes, w.N)
+    M, L, S = w.M, w.L, geo.S
+    dt, tdt = (np.uint16, torch.int16) if elem_bytes == 2 else (np.uint32, torch.int32)
+    rng = np.random.default_rng(17)
+    shards_h = [rng.integers(0, np.iinfo(dt).max, S, dtype=dt) for _ in range(w.N)]
+    expect = O.ag_place(geo, shards_h)
+    shards = [torch.from_numpy(x.view(np.int16 if elem_bytes == 2 else np.int32)).to(DEV) for x in shards_h]
+    with tide.TidePlan(w.shapes, w.N, M, L) as plan:
+        for node in sorted({0, M - 1}):
+            params = [torch.full((w.N * geo.e[p],), -5, dtype=tdt, device=DEV) for p in range(w.P)]
+            for rail in range(L):
+                stages = [torch.full((M * S,), -9, dtype=tdt, device=DEV) for _ in range(M)]
+                for n in range(M):
+                    stages[n][:S].copy_(shards[n * L + rail])
+                tide.tide_ag_rd_exchange(plan.handle, stages, elem_bytes)
+                torch.cuda.synchronize()
+                # after the exchange, slot k of node n holds node (n + k) mod M's shard
+                for n in range(M):
+                    for k in range(M):
+                        assert torch.equal(stages[n][k * S:(k + 1) * S], shards[((n + k) % M) * L + rail])
+                tide.tide_ag_stage_place(plan.handle, stages[node], node, rail, params, elem_bytes)
+            torch.cuda.synchronize()
+            for p in range(w.P):
+                assert np.array_equal(params[p].cpu().numpy().view(dt), expect[p]), (node, p)
