@@ -330,3 +330,65 @@ def rd_stage_place(geo, stage, node, rail, L, params):
             r = ((node + k) % M) * L + rail
             params[p][r * e_p:(r + 1) * e_p] = stage[k][o_p:o_p + e_p]
     return params
+
+
+# --------------------------------------------------------------------------
+# Reduce-scatter in the pages' two stages, with the inbox made explicit
+# ([Endgame] "Reduce-scatter: two levels of addition, the last one done by
+# NVSwitch"; [Abstract] Figure 6).  Stage 1: on source node n_src, for
+# destination node n_dest, the GPU that owns slice s sums the node's L local
+# copies into one fp32 partial and sends it on its own line, so it lands on
+# destination GPU g = (s - c) mod L, c = relative_index(n_dest, n_src, M).
+# Stage 2: every destination rank adds the partials of its own block of each
+# slice from the landing GPUs 0..L-1 in turn.  Inbox layout:
+# inbox[n_dest][g][c] is an array of L*B floats (B = slice_len), rank
+# n_dest*L + l_d's block at l_d*B.
+# --------------------------------------------------------------------------
+
+def rs_inbox(geo, grads, M, L):
+    """Stage 1: every node partial, at the inbox position it lands on."""
+    N, S = geo.N, geo.S
+    B = slice_len(S, L)
+    inbox = np.zeros((M, L, M, L * B), dtype=np.float32)
+    for r in range(N):
+        n_dest, l_dest = divmod(r, L)
+        for p in range(geo.P):
+            e_p, o_p = geo.e[p], geo.o[p]
+            v = valid_elems(geo, p, r)
+            a = 0
+            while a < v:
+                s = slice_of(o_p + a, S, L)
+                b = min(v, (s + 1) * B - o_p)
+                first = r * e_p + a             # rank r's rows start at global row r*Rp
+                for n_src in range(M):
+                    part = _node_partial(lambda k, p=p, s0=first, cnt=b - a: grads[k][p][s0:s0 + cnt],
+                                         n_src, L, b - a)
+                    c = relative_index(n_dest, n_src, M)
+                    g = landing_gpu(s, c, L)
+                    x0 = o_p + a - s * B
+                    inbox[n_dest, g, c, l_dest * B + x0:l_dest * B + x0 + (b - a)] = part
+                a = b
+            # padding rows carry +0.0 partials (inbox starts at +0.0)
+    return inbox
+
+
+def rs_land(geo, inbox, M, L):
+    """Stage 2: each destination rank's shard from the landed partials."""
+    N, S = geo.N, geo.S
+    B = slice_len(S, L)
+    shards = []
+    for r in range(N):
+        n_dest, l_dest = divmod(r, L)
+        out = np.empty(S, dtype=np.float32)
+        for s in range(L):
+            lo, hi = s * B, min(S, (s + 1) * B)
+            if lo >= hi:
+                continue
+            acc = np.zeros(hi - lo, dtype=np.float32)
+            for g in range(L):
+                c = (s - g) % L                         # the source whose slice s lands on GPU g
+                if c < M:
+                    acc = acc + inbox[n_dest, g, c, l_dest * B:l_dest * B + (hi - lo)]
+            out[lo:hi] = acc
+        shards.append(out)
+    return shards

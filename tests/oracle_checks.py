@@ -313,6 +313,29 @@ def check_ag_of_rs_round_trip():
             assert (full[p][n:].view(np.uint32) == 0).all()
 
 
+def check_staged_reduce_scatter_equals_fused():
+    """The two-stage form (partials landed in the inbox, then added per
+    landing GPU) gives the same bits as the direct definition, and every
+    partial sits where the Latin square puts it."""
+    for t, (shapes, M, L) in enumerate(_tiny_groups()):
+        N = M * L
+        geo = O.geometry(shapes, N)
+        grads = [[gen.bf16_values(gen.tensor_key(900 + t, r, p), np.arange(int(np.prod(s)) if len(s) else 1,
+                                                                          dtype=np.uint64), gen.OUTLIER)
+                  for p, s in enumerate(shapes)] for r in range(N)]
+        inbox = O.rs_inbox(geo, grads, M, L)
+        staged = O.rs_land(geo, inbox, M, L)
+        fused = O.rs_reduce(geo, grads, M, L)
+        for r in range(N):
+            assert np.array_equal(staged[r].view(np.uint32), fused[r].view(np.uint32)), r
+        # each (dest node, slice, source) partial occupies exactly one landing GPU
+        B = O.slice_len(geo.S, L)
+        for n_dest in range(M):
+            for s in range(L):
+                gpus = [O.landing_gpu(s, O.relative_index(n_dest, n, M), L) for n in range(M)]
+                assert len(set(gpus)) == M
+
+
 # ------------------------------------------------------ recursive doubling
 
 def check_recursive_doubling_page_facts():

@@ -44,6 +44,8 @@ MUTATIONS = {
     "recursive doubling from the lower node": ("have[n] = have[n] + sent[(n + 2 ** d) % M]",
                                                "have[n] = have[n] + sent[(n - 2 ** d) % M]"),
     "stage slot rotated the wrong way": ("r = ((node + k) % M) * L + rail", "r = ((node - k) % M) * L + rail"),
+    "landing stage adds a wrong source": ("c = (s - g) % L                         # the source",
+                                          "c = (s + g) % L                         # the source"),
     "AG piece offset": ("block[r * e_p:(r + 1) * e_p] = shards[r][o_p:o_p + e_p]",
                         "block[r * e_p:(r + 1) * e_p] = shards[(r + 1) % geo.N][o_p:o_p + e_p]"),
 }
