@@ -60,9 +60,11 @@ void build_rs_items(tide_plan* pl) {
         e = end;
       }
       for (int64_t e = v; e < e_p;) {
+        const int64_t s = (o_p + e) / slice_len;
+        const int64_t slice_end = (s + 1) * slice_len - o_p;
         const int64_t chunk_end = ((o_p + e) / kRsPadChunk + 1) * kRsPadChunk - o_p;
-        const int64_t end = std::min(e_p, chunk_end);
-        pl->rs_items.push_back(RsItem{0, o_p + e, (int32_t)(end - e), p, r, 0, RS_PAD});
+        const int64_t end = std::min(e_p, std::min(slice_end, chunk_end));
+        pl->rs_items.push_back(RsItem{0, o_p + e, (int32_t)(end - e), p, r, (int16_t)s, RS_PAD});
         e = end;
       }
     }

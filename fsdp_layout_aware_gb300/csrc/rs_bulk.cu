@@ -34,6 +34,7 @@
 
 #include <cstdint>
 
+#include "rs_device.cuh"
 #include "tide_internal.h"
 
 namespace tide {
@@ -103,87 +104,6 @@ __device__ __forceinline__ uint4 lds16(const unsigned char* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(smem_addr(p)));
   return v;
-}
-
-__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 v) {
-  acc[0] = __fadd_rn(acc[0], __uint_as_float(v.x << 16));
-  acc[1] = __fadd_rn(acc[1], __uint_as_float(v.x & 0xFFFF0000u));
-  acc[2] = __fadd_rn(acc[2], __uint_as_float(v.y << 16));
-  acc[3] = __fadd_rn(acc[3], __uint_as_float(v.y & 0xFFFF0000u));
-  acc[4] = __fadd_rn(acc[4], __uint_as_float(v.z << 16));
-  acc[5] = __fadd_rn(acc[5], __uint_as_float(v.z & 0xFFFF0000u));
-  acc[6] = __fadd_rn(acc[6], __uint_as_float(v.w << 16));
-  acc[7] = __fadd_rn(acc[7], __uint_as_float(v.w & 0xFFFF0000u));
-}
-
-// Store the 8 results of a vector whose lane 0 is item element e0 when the
-// destination of e0 is 16-byte aligned; lanes outside [0, n) are skipped.
-__device__ __forceinline__ void store8_aligned(float* dst, int e0, int n, const float (&acc)[8]) {
-  if (e0 >= 0 && e0 + 8 <= n) {
-    float* o = dst + e0;
-    __stcs(reinterpret_cast<float4*>(o), make_float4(acc[0], acc[1], acc[2], acc[3]));
-    __stcs(reinterpret_cast<float4*>(o + 4), make_float4(acc[4], acc[5], acc[6], acc[7]));
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = e0 + i;
-      if (e >= 0 && e < n) __stcs(dst + e, acc[i]);
-    }
-  }
-}
-
-__device__ __forceinline__ void store4(float* dst, int a, int n, float w0, float w1, float w2, float w3) {
-  if (a >= 0 && a + 4 <= n) {
-    __stcs(reinterpret_cast<float4*>(dst + a), make_float4(w0, w1, w2, w3));
-  } else {
-    if (a >= 0 && a < n) __stcs(dst + a, w0);
-    if (a + 1 >= 0 && a + 1 < n) __stcs(dst + a + 1, w1);
-    if (a + 2 >= 0 && a + 2 < n) __stcs(dst + a + 2, w2);
-    if (a + 3 >= 0 && a + 3 < n) __stcs(dst + a + 3, w3);
-  }
-}
-
-// Destination of e0 is delta = 1..3 elements short of a 16-byte boundary.
-// Lane t writes the 16-byte aligned elements [e0+delta, e0+delta+8): its own
-// results from delta on, then the first delta results of lane t+1, which hold
-// the next 8 elements (one warp holds 256 consecutive elements).  Lane 31 has
-// no such neighbour and writes only its own part; lane 0 also writes its
-// first delta elements, which the previous warp's lane 31 cannot.  Together
-// the lanes write every element once.  Called by all 32 lanes.
-__device__ __forceinline__ void store8_shifted(float* dst, int e0, int n, int delta, int lane,
-                                               const float (&acc)[8]) {
-  const float n0 = __shfl_down_sync(0xffffffffu, acc[0], 1);
-  const float n1 = __shfl_down_sync(0xffffffffu, acc[1], 1);
-  const float n2 = __shfl_down_sync(0xffffffffu, acc[2], 1);
-  float w[8];
-  if (delta == 1) {
-    w[0] = acc[1]; w[1] = acc[2]; w[2] = acc[3]; w[3] = acc[4];
-    w[4] = acc[5]; w[5] = acc[6]; w[6] = acc[7]; w[7] = n0;
-  } else if (delta == 2) {
-    w[0] = acc[2]; w[1] = acc[3]; w[2] = acc[4]; w[3] = acc[5];
-    w[4] = acc[6]; w[5] = acc[7]; w[6] = n0; w[7] = n1;
-  } else {
-    w[0] = acc[3]; w[1] = acc[4]; w[2] = acc[5]; w[3] = acc[6];
-    w[4] = acc[7]; w[5] = n0; w[6] = n1; w[7] = n2;
-  }
-  const int a = e0 + delta;
-  store4(dst, a, n, w[0], w[1], w[2], w[3]);   // always this lane's own results
-  if (lane != 31) {
-    store4(dst, a + 4, n, w[4], w[5], w[6], w[7]);
-  } else {
-#pragma unroll
-    for (int i = 4; i < 8; ++i) {
-      const int j = a + i;
-      if (j < e0 + 8 && j >= 0 && j < n) __stcs(dst + j, w[i]);
-    }
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < 3; ++i) {
-      const int j = e0 + i;
-      if (i < delta && j >= 0 && j < n) __stcs(dst + j, acc[i]);
-    }
-  }
 }
 
 // Shared-memory carve-up, computed on the host (rs_bulk_layout).

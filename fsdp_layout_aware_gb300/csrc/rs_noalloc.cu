@@ -154,6 +154,9 @@ extern "C" tide_status tide_rs_reduce_noalloc(const tide_plan* pl, const void* c
   a.M = pl->M;
   a.L = pl->L;
   a.P = pl->P;
+  a.S = pl->S;
+  a.inbox = nullptr;
+  a.slice_len = pl->S > 0 ? (pl->S + pl->L - 1) / pl->L : 0;
   std::memcpy(a.order, pl->order, sizeof(a.order));
   const int grid = (int)std::min<int64_t>((int64_t)sms * occ, a.n_items);
   const int lerr = launch_rs(a, grid, stream);

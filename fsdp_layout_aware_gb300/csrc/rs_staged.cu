@@ -1,0 +1,163 @@
+// TIDE-RS in the pages' two stages, emulated on one GPU ("Reduce-scatter:
+// two levels of addition, the last one done by NVSwitch" in "The Endgame of
+// FSDP Communication"; Figure 6 of the preprint).
+//
+// Stage 1, the summing CTAs: for every destination rank r (node n_d, local
+// GPU l_d) and every source node n_s, the fp32 partial of n_s's L local bf16
+// copies (l ascending) is written to the inbox slot it lands in.  On the
+// pages the GPU of n_s that owns slice s sends its partial over its own line,
+// so it arrives on destination GPU g = (s - c) mod L with c = (n_d - n_s)
+// mod M; the emulated inbox is laid out [n_d][g][c][L * B] floats, rank
+// l_d's block of the slice at l_d * B (B = ceil(S / L)).
+//
+// Stage 2, the landing CTAs (the NVSwitch read-and-add plus the CTAs that
+// accumulate into the shard): every destination element adds the partials of
+// its slice from landing GPUs g = 0..L-1 in turn and stores the sum.
+//
+// The additions happen in the same order as in rs_fused, so the shards are
+// bit-identical; the price is 8*M extra bytes per shard element (every
+// partial written once and read once).  CTA counts can be set per emulated
+// rank to reproduce the pages' budget (16 summing, 4 landing CTAs per GPU).
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "rs_device.cuh"
+#include "tide_internal.h"
+
+namespace tide {
+namespace {
+
+__device__ __forceinline__ float* inbox_block(const RsArgs& a, int n_dest, int l_dest, int n_src, int slice,
+                                             int64_t dst_off) {
+  const int M = a.M, L = a.L;
+  const int c = ((n_dest - n_src) % M + M) % M;
+  const int g = ((slice - c) % L + L) % L;
+  const int64_t slot = (int64_t)L * a.slice_len;
+  return a.inbox + ((int64_t)(n_dest * L + g) * M + c) * slot + (int64_t)l_dest * a.slice_len +
+         (dst_off - (int64_t)slice * a.slice_len);
+}
+
+// Stage 1 for one item whose contributors share their address phase mod 16.
+template <int L>
+__device__ __forceinline__ void sum_aligned(const RsArgs& a, const uint16_t* const* src, const RsItem& item) {
+  const int ph = (int)(((uintptr_t)src[0] >> 1) & 7);
+  const int n = item.n;
+  const int nvec = (ph + n + 7) >> 3;
+  const int lane = threadIdx.x & 31;
+  const int n_dest = item.r / L, l_dest = item.r % L;
+  for (int v = threadIdx.x; v - lane < nvec; v += blockDim.x) {
+    const int e0 = v * 8 - ph;
+    for (int n_src = 0; n_src < a.M; ++n_src) {
+      float acc1[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc1[i] = 0.f;
+      if (v < nvec) {
+        uint4 x[L];
+#pragma unroll
+        for (int l = 0; l < L; ++l) x[l] = __ldcs(reinterpret_cast<const uint4*>(src[n_src * L + l] + e0));
+#pragma unroll
+        for (int l = 0; l < L; ++l) add_bf16x8(acc1, x[l]);
+      }
+      float* dst = inbox_block(a, n_dest, l_dest, n_src, item.slice, item.dst_off);
+      const int delta = (int)(((unsigned)ph - (unsigned)((uintptr_t)dst >> 2)) & 3u);
+      if (delta == 0)
+        store8_aligned(dst, e0, n, acc1);
+      else
+        store8_shifted(dst, e0, n, delta, lane, acc1);
+    }
+  }
+}
+
+// Stage 1 for contributors at different address phases: element-wise loads.
+template <int L>
+__device__ __forceinline__ void sum_unaligned(const RsArgs& a, const uint16_t* const* src, const RsItem& item) {
+  const int n = item.n;
+  const int n_dest = item.r / L, l_dest = item.r % L;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    for (int n_src = 0; n_src < a.M; ++n_src) {
+      float acc1 = 0.f;
+#pragma unroll
+      for (int l = 0; l < L; ++l) acc1 = __fadd_rn(acc1, bf16_to_f32(__ldcs(src[n_src * L + l] + e)));
+      __stcs(inbox_block(a, n_dest, l_dest, n_src, item.slice, item.dst_off) + e, acc1);
+    }
+  }
+}
+
+template <int L>
+__global__ void __launch_bounds__(kRsThreads, 4) rs_sum_kernel(const __grid_constant__ RsArgs a) {
+  __shared__ const uint16_t* src[kMaxN];
+  __shared__ long long next_item[2];
+  if (threadIdx.x == 0) next_item[0] = (long long)atomicAdd(a.counter, 1ull);
+  __syncthreads();
+  int slot = 0;
+  for (int64_t it = next_item[0]; it < a.n_items; it = next_item[slot]) {
+    slot ^= 1;
+    if (threadIdx.x == 0) next_item[slot] = (long long)atomicAdd(a.counter, 1ull);
+    const RsItem item = a.items[it];
+    if (item.kind == RS_PAD) {
+      // padding rows: every source's partial is +0.0
+      for (int n_src = 0; n_src < a.M; ++n_src)
+        zero_fill(inbox_block(a, item.r / L, item.r % L, n_src, item.slice, item.dst_off), item.n);
+    } else {
+      if ((int)threadIdx.x < a.N)
+        src[threadIdx.x] = a.grad_tab[(int64_t)item.p * a.N + threadIdx.x] + item.src_off;
+      __syncthreads();
+      if (a.uniform_phase[item.p])
+        sum_aligned<L>(a, src, item);
+      else
+        sum_unaligned<L>(a, src, item);
+    }
+    __syncthreads();
+  }
+}
+
+// Stage 2.  blockIdx.y is the destination rank; the CTAs of one rank stride
+// over its shard.
+__global__ void __launch_bounds__(256) rs_land_kernel(const float* __restrict__ inbox, float* const* shard_tab,
+                                                     int M, int L, int64_t S, int64_t B) {
+  const int r = blockIdx.y;
+  const int n_dest = r / L, l_dest = r % L;
+  float* out = shard_tab[r];
+  const int64_t slot = (int64_t)L * B;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < S; x += stride) {
+    const int s = (int)(x / B);
+    const int64_t off = (int64_t)l_dest * B + (x - (int64_t)s * B);
+    float acc = 0.f;
+    for (int g = 0; g < L; ++g) {
+      const int c = ((s - g) % L + L) % L;  // the source whose slice s landed on GPU g
+      if (c < M) acc = __fadd_rn(acc, __ldcs(inbox + ((int64_t)(n_dest * L + g) * M + c) * slot + off));
+    }
+    __stcs(out + x, acc);
+  }
+}
+
+template <int L>
+int launch_sum_t(const RsArgs& a, int grid, cudaStream_t s) {
+  rs_sum_kernel<L><<<grid, kRsThreads, 0, s>>>(a);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_rs_staged(const RsArgs& a, int sum_grid, int land_grid_x, void* stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  int err = (int)cudaErrorInvalidValue;
+  switch (a.L) {
+    case 1: err = launch_sum_t<1>(a, sum_grid, s); break;
+    case 2: err = launch_sum_t<2>(a, sum_grid, s); break;
+    case 3: err = launch_sum_t<3>(a, sum_grid, s); break;
+    case 4: err = launch_sum_t<4>(a, sum_grid, s); break;
+    case 5: err = launch_sum_t<5>(a, sum_grid, s); break;
+    case 6: err = launch_sum_t<6>(a, sum_grid, s); break;
+    case 7: err = launch_sum_t<7>(a, sum_grid, s); break;
+    case 8: err = launch_sum_t<8>(a, sum_grid, s); break;
+  }
+  if (err != cudaSuccess) return err;
+  rs_land_kernel<<<dim3(land_grid_x, a.N), 256, 0, s>>>(a.inbox, a.shard_tab, a.M, a.L, a.S, a.slice_len);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace tide

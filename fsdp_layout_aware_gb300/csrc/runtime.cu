@@ -245,10 +245,13 @@ tide_status tide_plan_check(tide_plan* pl) {
   return TIDE_OK;
 }
 
-tide_status tide_rs_reduce(tide_plan* pl, const void* const* grads, float* const* shards, void* stream) {
-  clear_error();
-  if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
-  if (pl->rs_items.empty()) return TIDE_OK;  // S == 0: nothing to write
+}  // extern "C"
+
+namespace {
+// Validate a reduce-scatter call, set up the device on first use, fill and
+// upload the call's pointer table, and return the kernel arguments.
+tide_status prepare_rs(tide_plan* pl, const void* const* grads, float* const* shards, void* stream, RsArgs* a,
+                       tide_plan::Slot** out_slot) {
   if (!grads || !shards) return fail(TIDE_ERR_INVALID_ARG, "grads or shards array is NULL");
   for (int32_t r = 0; r < pl->N; ++r) {
     if (!shards[r]) return fail(TIDE_ERR_INVALID_ARG, "shards[" + std::to_string(r) + "] is NULL");
@@ -267,7 +270,7 @@ tide_status tide_rs_reduce(tide_plan* pl, const void* const* grads, float* const
   tide_plan::Slot* slot = nullptr;
   if ((st = acquire_slot(pl, &slot)) != TIDE_OK) return st;
 
-  // Pointer table: [P][N] gradients, [N] shards, [P] phase flags.
+  // Pointer table: [P][N] gradients, [N] shards, [P] phase flags, work counter.
   const size_t n_grad = (size_t)pl->P * pl->N;
   const uint16_t** gtab = (const uint16_t**)slot->host;
   float** stab = (float**)(slot->host + n_grad * 8);
@@ -287,27 +290,70 @@ tide_status tide_rs_reduce(tide_plan* pl, const void* const* grads, float* const
   const size_t counter_at = flags_at + align_up((size_t)pl->P, 16);
   *(unsigned long long*)(slot->host + counter_at) = 0;  // the kernels' work counter starts at item 0
   const size_t bytes = counter_at + 8;
-  cudaStream_t s = (cudaStream_t)stream;
-  if ((st = upload_and_mark(slot, bytes, s)) != TIDE_OK) return st;
+  if ((st = upload_and_mark(slot, bytes, (cudaStream_t)stream)) != TIDE_OK) return st;
 
+  a->items = pl->d_rs_items;
+  a->n_items = (int64_t)pl->rs_items.size();
+  a->counter = (unsigned long long*)(slot->dev + counter_at);
+  a->grad_tab = (const uint16_t* const*)slot->dev;
+  a->shard_tab = (float* const*)(slot->dev + n_grad * 8);
+  a->uniform_phase = (const uint8_t*)(slot->dev + flags_at);
+  a->N = pl->N;
+  a->M = pl->M;
+  a->L = pl->L;
+  a->P = pl->P;
+  a->S = pl->S;
+  a->inbox = nullptr;
+  a->slice_len = pl->S > 0 ? (pl->S + pl->L - 1) / pl->L : 0;
+  std::memcpy(a->order, pl->order, sizeof(a->order));
+  a->bulk = pl->bulk;
+  a->bulk.status = pl->d_status;
+  a->bulk.wait_limit_ns = pl->wait_limit_ns;
+  a->bulk.test_drop_tile = pl->test_drop_tile;
+  *out_slot = slot;
+  return TIDE_OK;
+}
+}  // namespace
+
+extern "C" {
+
+tide_status tide_rs_reduce(tide_plan* pl, const void* const* grads, float* const* shards, void* stream) {
+  clear_error();
+  if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  if (pl->rs_items.empty()) return TIDE_OK;  // S == 0: nothing to write
   RsArgs a;
-  a.items = pl->d_rs_items;
-  a.counter = (unsigned long long*)(slot->dev + counter_at);
-  a.n_items = (int64_t)pl->rs_items.size();
-  a.grad_tab = (const uint16_t* const*)slot->dev;
-  a.shard_tab = (float* const*)(slot->dev + n_grad * 8);
-  a.uniform_phase = (const uint8_t*)(slot->dev + flags_at);
-  a.N = pl->N;
-  a.M = pl->M;
-  a.L = pl->L;
-  a.P = pl->P;
-  std::memcpy(a.order, pl->order, sizeof(a.order));
-  a.bulk = pl->bulk;
-  a.bulk.status = pl->d_status;
-  a.bulk.wait_limit_ns = pl->wait_limit_ns;
-  a.bulk.test_drop_tile = pl->test_drop_tile;
+  tide_plan::Slot* slot = nullptr;
+  tide_status st = prepare_rs(pl, grads, shards, stream, &a, &slot);
+  if (st != TIDE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
   if (pl->rs_kernel == 1) return finish(slot, launch_rs_bulk(a, pl->bulk_grid, stream), s, "rs_bulk launch");
   return finish(slot, launch_rs(a, pl->rs_grid, stream), s, "rs_fused launch");
+}
+
+int64_t tide_plan_inbox_elems(const tide_plan* pl) {
+  if (!pl) return -1;
+  if (pl->S == 0) return 0;
+  const int64_t B = (pl->S + pl->L - 1) / pl->L;
+  return (int64_t)pl->M * pl->L * pl->M * pl->L * B;
+}
+
+tide_status tide_rs_staged(tide_plan* pl, const void* const* grads, float* const* shards, float* inbox,
+                           int32_t sum_ctas_per_rank, int32_t landing_ctas_per_rank, void* stream) {
+  clear_error();
+  if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  if (sum_ctas_per_rank < 0 || landing_ctas_per_rank < 0) return fail(TIDE_ERR_INVALID_ARG, "negative CTA count");
+  if (pl->rs_items.empty()) return TIDE_OK;
+  if (!inbox) return fail(TIDE_ERR_INVALID_ARG, "inbox is NULL");
+  if ((uintptr_t)inbox & 3) return fail(TIDE_ERR_ALIGNMENT, "inbox not 4-byte aligned");
+  RsArgs a;
+  tide_plan::Slot* slot = nullptr;
+  tide_status st = prepare_rs(pl, grads, shards, stream, &a, &slot);
+  if (st != TIDE_OK) return st;
+  a.inbox = inbox;
+  const int64_t sum_grid =
+      sum_ctas_per_rank > 0 ? std::min<int64_t>((int64_t)sum_ctas_per_rank * pl->N, 1 << 20) : pl->rs_grid;
+  const int land_x = landing_ctas_per_rank > 0 ? landing_ctas_per_rank : std::max(1, pl->num_sms * 8 / pl->N);
+  return finish(slot, launch_rs_staged(a, (int)sum_grid, land_x, stream), (cudaStream_t)stream, "rs_staged launch");
 }
 
 tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const* params, int32_t elem_bytes,

@@ -116,6 +116,9 @@ struct RsArgs {
   float* const* shard_tab;          // [N]
   const uint8_t* uniform_phase;     // [P]: 1 if all N gradients of p share addr mod 16
   int32_t N, M, L, P;
+  int64_t S;                        // packed shard length
+  float* inbox;                     // rs_staged only: [M][L][M][L * slice_len] partials
+  int64_t slice_len;                // ceil(S / L)
   BulkLayout bulk;                  // rs_bulk only
   uint8_t order[kOrderTableSize];
 };
@@ -134,6 +137,7 @@ struct AgArgs {
 int launch_rs(const RsArgs& args, int grid, void* stream);
 int launch_ag(const AgArgs& args, int grid, void* stream);
 int launch_rs_bulk(const RsArgs& args, int grid, void* stream);
+int launch_rs_staged(const RsArgs& args, int sum_grid, int land_grid_x, void* stream);
 BulkLayout rs_bulk_layout(int N, int M, int L, int smem_budget);
 int rs_bulk_setup(int L, int smem_bytes);  // raises the kernel's dynamic shared-memory limit
 // Resident CTAs per SM of each kernel (occupancy), for grid sizing.

@@ -62,6 +62,8 @@ def _load():
         "tide_rs_reduce_noalloc": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
         "tide_plan_set_option": (i32, [vp, i32, i64]),
         "tide_plan_check": (i32, [vp]),
+        "tide_plan_inbox_elems": (i64, [vp]),
+        "tide_rs_staged": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, i32, i32, vp]),
         "tide_rd_rounds": (i32, [i32]),
         "tide_rd_send_count": (i32, [i32, i32]),
         "tide_ag_rd_exchange": (i32, [vp, ctypes.POINTER(vp), i32, vp]),
@@ -147,6 +149,16 @@ def tide_plan_create(shapes, N, M, L):
 
 def tide_plan_destroy(plan):
     _lib.tide_plan_destroy(plan)
+
+
+def tide_plan_inbox_elems(plan):
+    return int(_lib.tide_plan_inbox_elems(plan))
+
+
+def tide_rs_staged(plan, grads, shards, inbox, sum_ctas_per_rank=0, landing_ctas_per_rank=0, stream=None):
+    """Two-stage reduce-scatter through an explicit inbox (same bits as tide_rs_reduce)."""
+    _check(_lib.tide_rs_staged(plan, _ptr_array(grads), _ptr_array(shards), _ptr(inbox), sum_ctas_per_rank,
+                               landing_ctas_per_rank, _stream(stream)))
 
 
 def tide_rd_rounds(M):

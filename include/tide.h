@@ -223,6 +223,31 @@ tide_status tide_ag_place(tide_plan* plan, const void* const* shards, void* cons
 tide_status tide_rs_reduce_noalloc(const tide_plan* plan, const void* const* grads, float* const* shards,
                                    void* stream);
 
+/* ---- Reduce-scatter in the pages' two stages -----------------------------
+ * [Endgame] "Reduce-scatter: two levels of addition, the last one done by
+ * NVSwitch"; [Abstract] Figure 6.  Same result as tide_rs_reduce, bit for
+ * bit, computed the way the pages split it:
+ *   stage 1 (summing CTAs): for every destination rank r = n_d*L + l_d and
+ *   source node n_s, the fp32 sum of n_s's L local copies (l ascending) is
+ *   written to the inbox slot where the Latin square lands it: destination
+ *   GPU g = (s - c) mod L, c = (n_d - n_s) mod M, for slice s;
+ *   stage 2 (landing CTAs): each destination element adds its slice's
+ *   partials from landing GPUs g = 0..L-1 in turn.
+ * The inbox costs 8*M extra bytes of traffic per shard element. */
+
+/* Floats the inbox needs: M * L * M * L * ceil(S / L) (0 when S == 0); -1
+ * for a NULL plan.  Layout [n_d][g][c][L * B], rank l_d's block at l_d * B. */
+int64_t tide_plan_inbox_elems(const tide_plan* plan);
+
+/* grads, shards, stream: as tide_rs_reduce.  inbox: device pointer to
+ * tide_plan_inbox_elems() floats, 4-byte aligned, caller-owned scratch whose
+ * contents are overwritten.  sum_ctas_per_rank / landing_ctas_per_rank: CTAs
+ * of each stage per emulated rank (16 and 4 reproduce the pages' training
+ * budget); 0 picks a grid that fills the GPU.  Errors: as tide_rs_reduce;
+ * INVALID_ARG for a NULL inbox or a negative CTA count. */
+tide_status tide_rs_staged(tide_plan* plan, const void* const* grads, float* const* shards, float* inbox,
+                           int32_t sum_ctas_per_rank, int32_t landing_ctas_per_rank, void* stream);
+
 /* ---- All-gather across nodes by recursive doubling ----------------------
  * [Endgame] "All-gather: parameters land at their final address" and
  * [Abstract] Figure 5: on rail l (GPU l of every node) each node starts with

@@ -69,10 +69,10 @@ def _check_rs_items(plan, geo, M, L):
         assert n > 0 and geo.o[p] <= dst and dst + n <= geo.o[p] + geo.e[p]
         e0 = dst - geo.o[p]
         v = O.valid_elems(geo, p, r)
+        assert O.slice_of(dst, geo.S, L) == O.slice_of(dst + n - 1, geo.S, L)   # one slice per item
         if it["kind"] == 0:
             assert e0 + n <= v
             assert it["src_off"] == r * geo.e[p] + e0     # contributors' rows r*Rp...
-            assert O.slice_of(dst, geo.S, L) == O.slice_of(dst + n - 1, geo.S, L)
         else:
             assert it["kind"] == 1 and e0 >= v
         for x in range(dst, dst + n):
@@ -216,3 +216,18 @@ def test_recursive_doubling_schedule_matches_oracle():
             assert tide.tide_rd_send_count(M, d) == O.rd_send_count(M, d)
         assert tide.tide_rd_send_count(M, O.rd_rounds(M)) == -1
     assert tide.tide_rd_rounds(0) == -1
+
+
+def test_staged_rs_arguments_without_a_gpu():
+    with tide.TidePlan([(8, 64), (4, 64), (12, 64)], 4, 2, 2) as plan:
+        B = -(-plan.S // 2)
+        assert tide.tide_plan_inbox_elems(plan.handle) == 2 * 2 * 2 * 2 * B
+        good = [0x10000 * (i + 1) for i in range(12)]
+        shards = [0x1000000 * (r + 1) for r in range(4)]
+        for inbox, sums, lands, status in [(None, 0, 0, 1), (0x2000002, 0, 0, 2), (0x2000000, -1, 0, 1),
+                                           (0x2000000, 0, -4, 1)]:
+            with pytest.raises(tide.TideError) as err:
+                tide.tide_rs_staged(plan.handle, good, shards, inbox, sums, lands, stream=0)
+            assert err.value.status == status
+    with tide.TidePlan([], 4, 1, 4) as plan:
+        assert tide.tide_plan_inbox_elems(plan.handle) == 0

@@ -399,3 +399,35 @@ def test_ag_by_recursive_doubling_matches_direct_landing(w, elem_bytes):
             torch.cuda.synchronize()
             for p in range(w.P):
                 assert np.array_equal(params[p].cpu().numpy().view(dt), expect[p]), (node, p)
+
+
+@pytest.mark.parametrize("w", [SMALL[0], SMALL[2], SMALL[3], SMALL[4], SMALL[5], SMALL[6]], ids=lambda w: w.name)
+@pytest.mark.parametrize("budget", [(0, 0), (16, 4)], ids=["fill", "pages_16_4"])
+def test_rs_staged_bit_exact_and_inbox(w, budget):
+    """The two-stage reduce-scatter equals the oracle bit for bit, and its
+    inbox holds every node partial where the Latin square lands it."""
+    grads = host_grads(w)
+    geo, expect = oracle_rs(w, grads)
+    inbox_o = O.rs_inbox(geo, grads, w.M, w.L)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        n_inbox = tide.tide_plan_inbox_elems(plan.handle)
+        assert n_inbox == inbox_o.size
+        dev = [[to_dev_u16(grads[r][p])[0] for p in range(w.P)] for r in range(w.N)]
+        inbox = torch.full((n_inbox,), float("nan"), dtype=torch.float32, device=DEV)
+        outs = [f32_guarded(geo.S, GUARD, GUARD) for _ in range(w.N)]
+        flat = [dev[r][p] for r in range(w.N) for p in range(w.P)]
+        tide.tide_rs_staged(plan.handle, flat, [o[0] for o in outs], inbox, *budget)
+        torch.cuda.synchronize()
+        for r in range(w.N):
+            assert np.array_equal(f32_bits(outs[r][0]), expect[r].view(np.uint32)), r
+        got = inbox.cpu().numpy().reshape(inbox_o.shape)
+        B = O.slice_len(geo.S, w.L)
+        for n_dest in range(w.M):
+            for g in range(w.L):
+                for c in range(w.M):
+                    s = (g + c) % w.L                   # the slice that lands on GPU g from index c
+                    lo, hi = s * B, min(geo.S, (s + 1) * B)
+                    for l_dest in range(w.L):
+                        a = got[n_dest, g, c, l_dest * B:l_dest * B + (hi - lo)]
+                        b = inbox_o[n_dest, g, c, l_dest * B:l_dest * B + (hi - lo)]
+                        assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), (n_dest, g, c, l_dest)
