@@ -46,6 +46,10 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--path", choices=["fused", "staged-rs", "rd-ag"], default="fused",
+                    help="fused: the hot path (RS + AG per step); staged-rs: the two-stage reduce-scatter "
+                         "through an inbox; rd-ag: the all-gather by recursive-doubling exchange and stage "
+                         "placement")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     help="llama70b (default), qwen3moe, wan22dit, uneven or tiny")
     ap.add_argument("--row-div", type=int, default=1,
@@ -461,11 +465,118 @@ def run_reference(args, rank, world):
     }
 
 
+def _setup_inputs(args, local_rank, need_grads=True, need_ag=True):
+    import torch
+
+    import fsdp_layout_aware_gb300 as tide
+    from synth import device, gen
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = get_workload(args)
+    plan = tide.TidePlan(w.shapes, w.N, w.M, w.L)
+    stream = torch.cuda.Stream(device=dev)
+    grads, ag_in = [], []
+    with torch.cuda.stream(stream):
+        if need_grads:
+            for r in range(w.N):
+                for p in range(w.P):
+                    t = torch.empty(w.numel(p), dtype=torch.int16, device=dev)
+                    device.fill_bf16(t, w.grad_key(r, p), w.dists[p], w.sigma, stream=stream)
+                    grads.append(t)
+        if need_ag:
+            for r in range(w.N):
+                t = torch.empty(plan.S, dtype=torch.int16, device=dev)
+                device.fill_bf16(t, w.ag_key(r), gen.UNIFORM, stream=stream)
+                ag_in.append(t)
+    stream.synchronize()
+    return w, plan, stream, dev, grads, ag_in
+
+
+def _event_time(fn, K, W, stream):
+    import torch
+    for _ in range(W):
+        fn()
+    stream.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(K):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / K
+
+
+def run_staged_rs(args, local_rank):
+    """The two-stage reduce-scatter (summing kernel into the inbox, landing
+    kernel), filling the GPU and with the pages' 16 + 4 CTAs per rank."""
+    import torch
+
+    import fsdp_layout_aware_gb300 as tide
+    w, plan, stream, dev, grads, _ = _setup_inputs(args, local_rank, need_ag=False)
+    nb = algorithmic_bytes(w, plan)
+    shards = [torch.empty(plan.S, dtype=torch.float32, device=dev) for _ in range(w.N)]
+    inbox = torch.empty(tide.tide_plan_inbox_elems(plan.handle), dtype=torch.float32, device=dev)
+    gp, sp = tide.pointer_array(grads), tide.pointer_array(shards)
+    inbox_bytes = 8 * w.M * w.N * plan.S
+    out = {"path": "staged-rs", "metric": METRIC, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+           "warmup": args.warmup, "dtype": "f32", "data": "synthetic",
+           "config": {"workload": f"{w.name}: {w.notes}", "N": w.N, "M": w.M, "L": w.L,
+                      "rs_bytes_per_step": nb["rs_bytes"], "inbox_extra_bytes_per_step": inbox_bytes}}
+    for name, budget in (("fill", (0, 0)), ("pages_16_4", (16, 4))):
+        t = _event_time(lambda: tide.tide_rs_staged(plan.handle, gp, sp, inbox, *budget, stream=stream),
+                        args.steps, args.warmup, stream)
+        out[name] = {"ms": round(t * 1e3, 4), "GB_s_algorithmic": round(nb["rs_bytes"] / t / 1e9, 1),
+                     "GB_s_with_inbox": round((nb["rs_bytes"] + inbox_bytes) / t / 1e9, 1)}
+    t = _event_time(lambda: plan.rs_reduce(gp, sp, stream), args.steps, args.warmup, stream)
+    out["fused_ms"] = round(t * 1e3, 4)
+    out["value"] = out["fill"]["GB_s_algorithmic"]
+    return out
+
+
+def run_rd_ag(args, local_rank):
+    """The all-gather the pages' way for one destination node: per rail, the
+    recursive-doubling exchange between the M nodes' stage buffers (copy
+    engines), then the strided stage placement into the parameters."""
+    import torch
+
+    import fsdp_layout_aware_gb300 as tide
+    w, plan, stream, dev, _, ag_in = _setup_inputs(args, local_rank, need_grads=False)
+    M, L, S = w.M, w.L, plan.S
+    stages = [torch.empty(M * S, dtype=torch.int16, device=dev) for _ in range(M)]
+    params = [torch.empty(w.N * plan.e[p], dtype=torch.int16, device=dev) for p in range(w.P)]
+    pp = tide.pointer_array(params)
+
+    def step():
+        for rail in range(L):
+            for n in range(M):
+                stages[n][:S].copy_(ag_in[n * L + rail], non_blocking=True)
+            tide.tide_ag_rd_exchange(plan.handle, stages, 2, stream)
+            tide.tide_ag_stage_place(plan.handle, stages[0], 0, rail, pp, 2, stream)
+
+    with torch.cuda.stream(stream):
+        t = _event_time(step, max(1, args.steps // 8), args.warmup, stream)
+        ta = _event_time(lambda: plan.ag_place(tide.pointer_array(ag_in), pp, 2, stream), args.steps, args.warmup,
+                         stream)
+    place_bytes = 4 * w.N * S
+    exch_bytes = L * M * (M - 1) * S * 2 * 2
+    return {"path": "rd-ag", "metric": METRIC, "unit": "GB/s", "n_gpus": 1, "dtype": "bf16 copy", "data": "synthetic",
+            "config": {"workload": f"{w.name}: {w.notes}", "N": w.N, "M": M, "L": L,
+                       "rounds": tide.tide_rd_rounds(M)},
+            "ms_per_step": round(t * 1e3, 4), "placement_bytes": place_bytes, "exchange_bytes": exch_bytes,
+            "value": round((place_bytes + exch_bytes) / t / 1e9, 1),
+            "direct_landing_ms": round(ta * 1e3, 4)}
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         line = run_reference(args, rank, world)
+    elif args.path == "staged-rs":
+        line = run_staged_rs(args, local_rank) if rank == 0 else None
+    elif args.path == "rd-ag":
+        line = run_rd_ag(args, local_rank) if rank == 0 else None
     else:
         line = run_ours(args, rank, world, local_rank)
     if line is not None:

@@ -113,24 +113,50 @@ __global__ void __launch_bounds__(kRsThreads, 4) rs_sum_kernel(const __grid_cons
   }
 }
 
-// Stage 2.  blockIdx.y is the destination rank; the CTAs of one rank stride
-// over its shard.
-__global__ void __launch_bounds__(256) rs_land_kernel(const float* __restrict__ inbox, float* const* shard_tab,
-                                                     int M, int L, int64_t S, int64_t B) {
+// Stage 2.  blockIdx.y is the destination rank.  For each slice, thread 0
+// lists where the slice's partials landed (landing GPUs g ascending) in
+// shared memory; the threads then stream the slice, four outputs each per
+// round, adding the partials in that order.  Keeping the list in shared
+// memory keeps the kernel at about 32 registers, so eight CTAs fit per SM.
+__global__ void __launch_bounds__(256, 8) rs_land_kernel(const float* __restrict__ inbox, float* const* shard_tab,
+                                                        int M, int L, int64_t S, int64_t B) {
+  __shared__ const float* part[kMaxL];
+  __shared__ int n_part;
   const int r = blockIdx.y;
   const int n_dest = r / L, l_dest = r % L;
   float* out = shard_tab[r];
   const int64_t slot = (int64_t)L * B;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < S; x += stride) {
-    const int s = (int)(x / B);
-    const int64_t off = (int64_t)l_dest * B + (x - (int64_t)s * B);
-    float acc = 0.f;
-    for (int g = 0; g < L; ++g) {
-      const int c = ((s - g) % L + L) % L;  // the source whose slice s landed on GPU g
-      if (c < M) acc = __fadd_rn(acc, __ldcs(inbox + ((int64_t)(n_dest * L + g) * M + c) * slot + off));
+  const int64_t step = (int64_t)gridDim.x * blockDim.x * 4;
+  for (int s = 0; s < L; ++s) {
+    const int64_t lo = (int64_t)s * B, hi = min(S, lo + B);
+    if (lo >= hi) break;
+    __syncthreads();  // the previous slice's readers of part[] are done
+    if (threadIdx.x == 0) {
+      int k = 0;
+      for (int g = 0; g < L; ++g) {
+        const int c = ((s - g) % L + L) % L;  // the source whose slice s landed on GPU g
+        if (c < M) part[k++] = inbox + ((int64_t)(n_dest * L + g) * M + c) * slot + (int64_t)l_dest * B - lo;
+      }
+      n_part = k;
     }
-    __stcs(out + x, acc);
+    __syncthreads();
+    const int np = n_part;
+    for (int64_t x0 = lo + (int64_t)blockIdx.x * blockDim.x * 4 + threadIdx.x; x0 < hi; x0 += step) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int j = 0; j < np; ++j) {
+        const float* pj = part[j];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t x = x0 + (int64_t)u * blockDim.x;
+          if (x < hi) acc[u] = __fadd_rn(acc[u], __ldcs(pj + x));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t x = x0 + (int64_t)u * blockDim.x;
+        if (x < hi) __stcs(out + x, acc[u]);
+      }
+    }
   }
 }
 
