@@ -392,3 +392,44 @@ def rs_land(geo, inbox, M, L):
             out[lo:hi] = acc
         shards.append(out)
     return shards
+
+
+# --------------------------------------------------------------------------
+# Variants.
+#   rs_finish: the reduce-scatter result optionally averaged over the N ranks
+#   (divided by N in fp32, correctly rounded) and optionally accumulated into
+#   the shard's previous value (old + result, one fp32 add after the sum).
+#   ag_place_unpadded: the all-gather writing only each parameter's R_p real
+#   rows.  slot_pack: Slot-Reuse -- each rank's bf16 gradients copied into the
+#   all-gather slot it has just vacated, parameter p at offset N * op
+#   ([Endgame] "Reduce-scatter: two levels of addition...", last paragraph;
+#   [Abstract] Figure 7).
+# --------------------------------------------------------------------------
+
+def rs_finish(geo, sums, average=False, old=None):
+    out = []
+    for r in range(geo.N):
+        x = sums[r]
+        if average:
+            x = (x / np.float32(geo.N)).astype(np.float32)
+        if old is not None:
+            x = (old[r] + x).astype(np.float32)
+        out.append(x)
+    return out
+
+
+def ag_place_unpadded(geo, shards):
+    params = ag_place(geo, shards)
+    return [params[p][:geo.rows[p] * geo.Kp[p]] for p in range(geo.P)]
+
+
+def slot_pack(geo, grads):
+    """Each rank's gradients packed into its N*S-element slot at N*op."""
+    slots = []
+    for r in range(geo.N):
+        slot = np.zeros(geo.N * geo.S, dtype=grads[r][0].dtype if geo.P else np.uint16)
+        for p in range(geo.P):
+            n = geo.rows[p] * geo.Kp[p]
+            slot[geo.N * geo.o[p]:geo.N * geo.o[p] + n] = grads[r][p][:n]
+        slots.append(slot)
+    return slots

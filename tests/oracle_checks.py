@@ -336,6 +336,48 @@ def check_staged_reduce_scatter_equals_fused():
                 assert len(set(gpus)) == M
 
 
+def check_average_and_accumulate():
+    """Average = the exact integer sum divided by N, correctly rounded to fp32;
+    accumulate = old + result, exact for integers."""
+    for t, (shapes, M, L) in enumerate(_tiny_groups()):
+        N = M * L
+        geo = O.geometry(shapes, N)
+        grads = _int_grads(shapes, N, seed=500 + t)
+        sums = O.rs_reduce(geo, grads, M, L)
+        avg = O.rs_finish(geo, sums, average=True)
+        old = [np.arange(geo.S, dtype=np.float32) - 7 for _ in range(N)]
+        acc = O.rs_finish(geo, sums, old=old)
+        both = O.rs_finish(geo, sums, average=True, old=old)
+        for r in range(N):
+            exact = sums[r].astype(np.float64)          # integer sums are exact in fp32
+            assert np.array_equal(avg[r], (exact / N).astype(np.float32))
+            assert np.array_equal(acc[r].astype(np.float64), old[r].astype(np.float64) + exact)
+            assert np.array_equal(both[r], (old[r].astype(np.float64) + (exact / N).astype(np.float32)).astype(np.float32))
+
+
+def check_unpadded_gather_and_slot_pack():
+    for t, (shapes, M, L) in enumerate(_tiny_groups()):
+        N = M * L
+        geo = O.geometry(shapes, N)
+        shards = [np.arange(r * geo.S, (r + 1) * geo.S, dtype=np.int64) for r in range(N)]
+        full = O.ag_place(geo, shards)
+        unp = O.ag_place_unpadded(geo, shards)
+        for p, shape in enumerate(shapes):
+            n = int(np.prod(shape)) if len(shape) else 1
+            assert unp[p].size == n and np.array_equal(unp[p], full[p][:n])
+        grads = _int_grads(shapes, N, seed=700 + t)
+        slots = O.slot_pack(geo, grads)
+        for r in range(N):
+            for p, shape in enumerate(shapes):
+                n = int(np.prod(shape)) if len(shape) else 1
+                assert np.array_equal(slots[r][N * geo.o[p]:N * geo.o[p] + n], grads[r][p])
+        # reducing from the slots gives the same shards as reducing in place
+        from_slots = O.rs_reduce(geo, [[slots[r][N * geo.o[p]:N * geo.o[p] + geo.rows[p] * geo.Kp[p]]
+                                        for p in range(geo.P)] for r in range(N)], M, L)
+        direct = O.rs_reduce(geo, grads, M, L)
+        assert all(np.array_equal(a.view(np.uint32), b.view(np.uint32)) for a, b in zip(from_slots, direct))
+
+
 # ------------------------------------------------------ recursive doubling
 
 def check_recursive_doubling_page_facts():

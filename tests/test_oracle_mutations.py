@@ -46,6 +46,10 @@ MUTATIONS = {
     "stage slot rotated the wrong way": ("r = ((node + k) % M) * L + rail", "r = ((node - k) % M) * L + rail"),
     "landing stage adds a wrong source": ("c = (s - g) % L                         # the source",
                                           "c = (s + g) % L                         # the source"),
+    "average divides by M": ("x = (x / np.float32(geo.N)).astype(np.float32)",
+                             "x = (x / np.float32(geo.N - 1 or 1)).astype(np.float32)"),
+    "slot pack at op": ("slot[geo.N * geo.o[p]:geo.N * geo.o[p] + n] = grads[r][p][:n]",
+                        "slot[geo.o[p]:geo.o[p] + n] = grads[r][p][:n]"),
     "AG piece offset": ("block[r * e_p:(r + 1) * e_p] = shards[r][o_p:o_p + e_p]",
                         "block[r * e_p:(r + 1) * e_p] = shards[(r + 1) % geo.N][o_p:o_p + e_p]"),
 }
