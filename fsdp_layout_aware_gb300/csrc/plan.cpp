@@ -85,6 +85,34 @@ void build_ag_items(tide_plan* pl) {
     }
   }
 }
+// The all-gather items of real rows only (an unpadded parameter is the
+// first R_p rows of the padded block, so offsets are unchanged), and the
+// Slot-Reuse packing items: rank r's gradient of p (R_p*Kp elements) copied
+// to offset N*op of rank r's all-gather slot.
+void build_variant_items(tide_plan* pl) {
+  for (const AgItem& it : pl->ag_items) {
+    const int64_t real = pl->rows[it.p] * pl->Kp[it.p];  // elements of the unpadded parameter
+    const int64_t end = std::min<int64_t>(it.dst_off + it.n, real);
+    if (end > it.dst_off) {
+      AgItem c = it;
+      c.n = (int32_t)(end - it.dst_off);
+      pl->ag_items_unpadded.push_back(c);
+    }
+  }
+  const int64_t chunk = kAgChunkBytes / 2;
+  for (int32_t r = 0; r < pl->N; ++r) {
+    for (int32_t p = 0; p < pl->P; ++p) {
+      const int64_t n = pl->rows[p] * pl->Kp[p];
+      for (int64_t e = 0; e < n;) {
+        const int64_t end = std::min(n, (e / chunk + 1) * chunk);
+        pl->pack_items.push_back(AgItem{e, (int64_t)pl->N * pl->o[p] + e, (int32_t)(end - e), r, r * pl->P + p, 0});
+        e = end;
+      }
+    }
+  }
+  pl->slot_grads.assign((size_t)pl->N * pl->P, nullptr);
+}
+
 void build_prefixes(tide_plan* pl) {
   pl->ag_prefix.resize(pl->ag_items.size() + 1);
   pl->ag_prefix[0] = 0;
@@ -231,6 +259,7 @@ tide_status tide_plan_create(const tide_group_desc* d, tide_plan** out_plan) {
     build_order_table(pl);
     build_rs_items(pl);
     build_ag_items(pl);
+    build_variant_items(pl);
     build_prefixes(pl);
   } catch (const std::bad_alloc&) {
     delete pl;

@@ -259,16 +259,6 @@ __device__ void producer(const RsArgs& a, const Smem& m) {
   __syncwarp();
 }
 
-__device__ __forceinline__ void zero_fill_consumers(float* dst, int n, int tid) {
-  const int head = min(n, (int)(((16 - ((uintptr_t)dst & 15)) & 15) >> 2));
-  if (tid < head) dst[tid] = 0.f;
-  const int nv = (n - head) >> 2;
-  float4* d4 = reinterpret_cast<float4*>(dst + head);
-  for (int i = tid; i < nv; i += kConsumers) __stcs(d4 + i, make_float4(0.f, 0.f, 0.f, 0.f));
-  const int t0 = head + (nv << 2);
-  if (tid < n - t0) dst[t0 + tid] = 0.f;
-}
-
 template <int L>
 __device__ void consumers(const RsArgs& a, const Smem& m) {
   const int tid = threadIdx.x;
@@ -315,6 +305,7 @@ __device__ void consumers(const RsArgs& a, const Smem& m) {
         if (tid - lane < nvec) {  // warp-uniform: the shuffles need every lane
           const int delta = (int)(((unsigned)d.ph - (unsigned)((uintptr_t)d.dst >> 2)) & 3u);
           const int e0 = tid * 8 - d.ph;
+          epilogue8(acc2, d.dst, e0, d.n, a.epilogue, a.N);
           if (delta == 0)
             store8_aligned(d.dst, e0, d.n, acc2);
           else
@@ -353,14 +344,14 @@ __device__ void consumers(const RsArgs& a, const Smem& m) {
             const uint32_t node = (k < 4 ? d.ord_lo >> (8 * k) : d.ord_hi >> (8 * (k - 4))) & 0xFFu;
             if (k < M) acc2 = __fadd_rn(acc2, pv[node * 8]);
           }
-          __stcs(d.dst + e, acc2);
+          __stcs(d.dst + e, epilogue1(acc2, d.dst + e, a.epilogue, a.N));
         }
         pb ^= 1;
       }
     } else if (d.kind == TILE_PAD) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&m.empty[stage]);
-      zero_fill_consumers(d.dst, d.n, tid);
+      pad_fill(d.dst, d.n, a.epilogue, tid, kConsumers);
     } else {  // TILE_DIRECT: contributors at different address phases
       __syncwarp();
       if (lane == 0) mbar_arrive(&m.empty[stage]);
@@ -389,7 +380,7 @@ __device__ void consumers(const RsArgs& a, const Smem& m) {
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          if (i < cnt) __stcs(d.dst + e0 + i, acc2[i]);
+          if (i < cnt) __stcs(d.dst + e0 + i, epilogue1(acc2[i], d.dst + e0 + i, a.epilogue, a.N));
       }
     }
     if (++stage == (uint32_t)a.bulk.stages) {

@@ -106,4 +106,41 @@ __device__ __forceinline__ void store8_shifted(float* dst, int e0, int n, int de
   }
 }
 
+// Result variants of the reduce-scatter (tide_plan_set_option): the sum is
+// divided by N (fp32, correctly rounded) when averaging, then added to the
+// shard's previous value when accumulating.
+enum : int { EPI_AVERAGE = 1, EPI_ACCUMULATE = 2 };
+
+__device__ __forceinline__ float epilogue1(float acc, const float* dst, int flags, int N) {
+  if (flags & EPI_AVERAGE) acc = __fdiv_rn(acc, (float)N);
+  if (flags & EPI_ACCUMULATE) acc = __fadd_rn(*dst, acc);
+  return acc;
+}
+
+// Apply the variants to the 8 results of a vector whose lane 0 is element e0
+// of dst (elements outside [0, n) are left alone).
+__device__ __forceinline__ void epilogue8(float (&acc)[8], const float* dst, int e0, int n, int flags, int N) {
+  if (!flags) return;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = e0 + i;
+    if (e >= 0 && e < n) acc[i] = epilogue1(acc[i], dst + e, flags, N);
+  }
+}
+
+// Padding rows: +0.0, or the previous value plus +0.0 when accumulating.
+__device__ __forceinline__ void pad_fill(float* dst, int n, int flags, int tid, int nthreads) {
+  if (!(flags & EPI_ACCUMULATE)) {
+    const int head = min(n, (int)(((16 - ((uintptr_t)dst & 15)) & 15) >> 2));
+    if (tid < head) dst[tid] = 0.f;
+    const int nv = (n - head) >> 2;
+    float4* d4 = reinterpret_cast<float4*>(dst + head);
+    for (int i = tid; i < nv; i += nthreads) __stcs(d4 + i, make_float4(0.f, 0.f, 0.f, 0.f));
+    const int t0 = head + (nv << 2);
+    if (tid < n - t0) dst[t0 + tid] = 0.f;
+  } else {
+    for (int i = tid; i < n; i += nthreads) dst[i] = __fadd_rn(dst[i], 0.f);
+  }
+}
+
 }  // namespace tide

@@ -35,7 +35,7 @@ namespace {
 // extra lanes are never stored.
 template <int L>
 __device__ __forceinline__ void reduce_aligned(const uint16_t* const* src, const uint8_t* ord, int M, float* dst,
-                                               int n) {
+                                               int n, int epi, int N) {
   const int ph = (int)(((uintptr_t)src[0] >> 1) & 7);
   const int nvec = (ph + n + 7) >> 3;
   // elements from a vector's first element to the next 16-byte boundary of dst
@@ -63,6 +63,7 @@ __device__ __forceinline__ void reduce_aligned(const uint16_t* const* src, const
         for (int i = 0; i < 8; ++i) acc2[i] = __fadd_rn(acc2[i], acc1[i]);
       }
     }
+    epilogue8(acc2, dst, e0, n, epi, N);
     if (delta == 0)
       store8_aligned(dst, e0, n, acc2);
     else
@@ -73,7 +74,7 @@ __device__ __forceinline__ void reduce_aligned(const uint16_t* const* src, const
 // Contributors at different address phases: element-wise loads, same order.
 template <int L>
 __device__ __forceinline__ void reduce_unaligned(const uint16_t* const* src, const uint8_t* ord, int M, float* dst,
-                                                 int n) {
+                                                 int n, int epi, int N) {
   const int nvec = (n + 7) >> 3;
   for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
     const int e0 = v * 8;
@@ -98,7 +99,7 @@ __device__ __forceinline__ void reduce_unaligned(const uint16_t* const* src, con
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (i < cnt) __stcs(dst + e0 + i, acc2[i]);
+      if (i < cnt) __stcs(dst + e0 + i, epilogue1(acc2[i], dst + e0 + i, epi, N));
   }
 }
 
@@ -123,16 +124,16 @@ __global__ void __launch_bounds__(kRsThreads, 4) rs_fused_kernel(const __grid_co
     const RsItem item = a.items[it];
     float* dst = a.shard_tab[item.r] + item.dst_off;
     if (item.kind == RS_PAD) {
-      zero_fill(dst, item.n);
+      pad_fill(dst, item.n, a.epilogue, threadIdx.x, blockDim.x);
     } else {
       if ((int)threadIdx.x < a.N)
         src[threadIdx.x] = a.grad_tab[(int64_t)item.p * a.N + threadIdx.x] + item.src_off;
       __syncthreads();
       const uint8_t* ord = a.order + ((item.r / L) * L + item.slice) * a.M;
       if (a.uniform_phase[item.p])
-        reduce_aligned<L>(src, ord, a.M, dst, item.n);
+        reduce_aligned<L>(src, ord, a.M, dst, item.n, a.epilogue, a.N);
       else
-        reduce_unaligned<L>(src, ord, a.M, dst, item.n);
+        reduce_unaligned<L>(src, ord, a.M, dst, item.n, a.epilogue, a.N);
     }
     __syncthreads();  // next_item[slot] is visible; this item's readers of src[] are done
   }

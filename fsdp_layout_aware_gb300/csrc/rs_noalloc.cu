@@ -155,6 +155,7 @@ extern "C" tide_status tide_rs_reduce_noalloc(const tide_plan* pl, const void* c
   a.L = pl->L;
   a.P = pl->P;
   a.S = pl->S;
+  a.epilogue = pl->rs_epilogue;
   a.inbox = nullptr;
   a.slice_len = pl->S > 0 ? (pl->S + pl->L - 1) / pl->L : 0;
   std::memcpy(a.order, pl->order, sizeof(a.order));

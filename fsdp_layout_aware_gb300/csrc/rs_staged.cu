@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kRsThreads, 4) rs_sum_kernel(const __grid_cons
 // round, adding the partials in that order.  Keeping the list in shared
 // memory keeps the kernel at about 32 registers, so eight CTAs fit per SM.
 __global__ void __launch_bounds__(256, 8) rs_land_kernel(const float* __restrict__ inbox, float* const* shard_tab,
-                                                        int M, int L, int64_t S, int64_t B) {
+                                                        int M, int L, int64_t S, int64_t B, int epi) {
   __shared__ const float* part[kMaxL];
   __shared__ int n_part;
   const int r = blockIdx.y;
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(256, 8) rs_land_kernel(const float* __restrict
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int64_t x = x0 + (int64_t)u * blockDim.x;
-        if (x < hi) __stcs(out + x, acc[u]);
+        if (x < hi) __stcs(out + x, epilogue1(acc[u], out + x, epi, M * L));
       }
     }
   }
@@ -182,7 +182,8 @@ int launch_rs_staged(const RsArgs& a, int sum_grid, int land_grid_x, void* strea
     case 8: err = launch_sum_t<8>(a, sum_grid, s); break;
   }
   if (err != cudaSuccess) return err;
-  rs_land_kernel<<<dim3(land_grid_x, a.N), 256, 0, s>>>(a.inbox, a.shard_tab, a.M, a.L, a.S, a.slice_len);
+  rs_land_kernel<<<dim3(land_grid_x, a.N), 256, 0, s>>>(a.inbox, a.shard_tab, a.M, a.L, a.S, a.slice_len,
+                                                        a.epilogue);
   return (int)cudaGetLastError();
 }
 

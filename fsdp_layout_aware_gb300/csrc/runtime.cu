@@ -57,6 +57,13 @@ void release_device_state(tide_plan* pl) {
   }
   if (pl->d_status) cudaFree(pl->d_status);
   pl->d_status = nullptr;
+  for (void* q : {(void*)pl->d_agu_items, (void*)pl->d_agu_units, (void*)pl->d_pack_items, (void*)pl->d_pack_units})
+    if (q) cudaFree(q);
+  pl->d_agu_items = nullptr;
+  pl->d_agu_units = nullptr;
+  pl->d_pack_items = nullptr;
+  pl->d_pack_units = nullptr;
+  pl->agu_units = pl->pack_units = 0;
   pl->d_rs_items = nullptr;
   pl->d_ag_items = nullptr;
   pl->d_ag_units = nullptr;
@@ -135,6 +142,22 @@ tide_status ensure_device(tide_plan* pl) {
   try {
     const std::vector<UnitStart> au = ag_unit_starts(pl, (int64_t)pl->ag_grid * (kAgThreads / 32), 16 << 10, 32);
     pl->ag_units = (int64_t)au.size() - 1;
+    // Unpadded all-gather and Slot-Reuse packing lists.
+    auto upload = [&](const std::vector<AgItem>& v, AgItem** d_items, UnitStart** d_units,
+                      int64_t* n_units) -> cudaError_t {
+      if (v.empty()) return cudaSuccess;
+      const std::vector<UnitStart> u = ag_unit_starts_of(v, (int64_t)pl->ag_grid * (kAgThreads / 32), 16 << 10, 32);
+      *n_units = (int64_t)u.size() - 1;
+      cudaError_t e2 = cudaMalloc(d_items, v.size() * sizeof(AgItem));
+      if (e2 == cudaSuccess) e2 = cudaMemcpy(*d_items, v.data(), v.size() * sizeof(AgItem), cudaMemcpyHostToDevice);
+      if (e2 == cudaSuccess) e2 = cudaMalloc(d_units, u.size() * sizeof(UnitStart));
+      if (e2 == cudaSuccess) e2 = cudaMemcpy(*d_units, u.data(), u.size() * sizeof(UnitStart), cudaMemcpyHostToDevice);
+      return e2;
+    };
+    if ((err = upload(pl->ag_items_unpadded, &pl->d_agu_items, &pl->d_agu_units, &pl->agu_units)) != cudaSuccess)
+      return bail(err, "uploading the unpadded all-gather list");
+    if ((err = upload(pl->pack_items, &pl->d_pack_items, &pl->d_pack_units, &pl->pack_units)) != cudaSuccess)
+      return bail(err, "uploading the Slot-Reuse packing list");
     // Per-rail item lists for tide_ag_stage_place.
     for (int l = 0; l < pl->L; ++l) {
       std::vector<AgItem> ri;
@@ -218,6 +241,17 @@ tide_status tide_plan_set_option(tide_plan* pl, int32_t option, int64_t value) {
     case TIDE_OPT_WAIT_LIMIT_NS:
       if (value <= 0) return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_WAIT_LIMIT_NS must be positive");
       pl->wait_limit_ns = (uint64_t)value;
+      return TIDE_OK;
+    case TIDE_OPT_RS_AVERAGE:
+    case TIDE_OPT_RS_ACCUMULATE: {
+      if (value != 0 && value != 1) return fail(TIDE_ERR_INVALID_ARG, "option value must be 0 or 1");
+      const int bit = option == TIDE_OPT_RS_AVERAGE ? 1 : 2;
+      pl->rs_epilogue = value ? (pl->rs_epilogue | bit) : (pl->rs_epilogue & ~bit);
+      return TIDE_OK;
+    }
+    case TIDE_OPT_AG_UNPADDED:
+      if (value != 0 && value != 1) return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_AG_UNPADDED must be 0 or 1");
+      pl->ag_unpadded = value != 0;
       return TIDE_OK;
     case TIDE_OPT_TEST_DROP_TILE:
       if (value < -1) return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_TEST_DROP_TILE must be >= -1");
@@ -303,6 +337,7 @@ tide_status prepare_rs(tide_plan* pl, const void* const* grads, float* const* sh
   a->L = pl->L;
   a->P = pl->P;
   a->S = pl->S;
+  a->epilogue = pl->rs_epilogue;
   a->inbox = nullptr;
   a->slice_len = pl->S > 0 ? (pl->S + pl->L - 1) / pl->L : 0;
   std::memcpy(a->order, pl->order, sizeof(a->order));
@@ -384,14 +419,70 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
   if ((st = upload_and_mark(slot, ag_table_bytes(pl), s)) != TIDE_OK) return st;
 
   AgArgs a;
-  a.items = pl->d_ag_items;
-  a.units = pl->d_ag_units;
-  a.n_units = pl->ag_units;
-  a.n_items = (int64_t)pl->ag_items.size();
+  if (pl->ag_unpadded) {
+    a.items = pl->d_agu_items;
+    a.n_items = (int64_t)pl->ag_items_unpadded.size();
+    a.units = pl->d_agu_units;
+    a.n_units = pl->agu_units;
+  } else {
+    a.items = pl->d_ag_items;
+    a.n_items = (int64_t)pl->ag_items.size();
+    a.units = pl->d_ag_units;
+    a.n_units = pl->ag_units;
+  }
   a.shard_tab = (const unsigned char* const*)slot->dev;
   a.param_tab = (unsigned char* const*)(slot->dev + (size_t)pl->N * 8);
   a.elem_bytes = elem_bytes;
   return finish(slot, launch_ag(a, pl->ag_grid, stream), s, "ag_place launch");
+}
+
+tide_status tide_slot_pack(tide_plan* pl, const void* const* grads, void* const* slots, void* stream) {
+  clear_error();
+  if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  if (pl->pack_items.empty()) return TIDE_OK;
+  if (!grads || !slots) return fail(TIDE_ERR_INVALID_ARG, "grads or slots array is NULL");
+  for (int32_t r = 0; r < pl->N; ++r) {
+    if (!slots[r]) return fail(TIDE_ERR_INVALID_ARG, "slots[" + std::to_string(r) + "] is NULL");
+    if ((uintptr_t)slots[r] & 1) return fail(TIDE_ERR_ALIGNMENT, "slot pointer not 2-byte aligned");
+    for (int32_t p = 0; p < pl->P; ++p) {
+      if (pl->rows[p] * pl->Kp[p] == 0) continue;
+      const void* g = grads[(size_t)r * pl->P + p];
+      if (!g) return fail(TIDE_ERR_INVALID_ARG, "grads[" + std::to_string(r * pl->P + p) + "] is NULL");
+      if ((uintptr_t)g & 1) return fail(TIDE_ERR_ALIGNMENT, "gradient pointer not 2-byte aligned");
+    }
+  }
+  tide_status st = ensure_device(pl);
+  if (st != TIDE_OK) return st;
+  tide_plan::Slot* slot = nullptr;
+  if ((st = acquire_slot(pl, &slot)) != TIDE_OK) return st;
+  const size_t n_grad = (size_t)pl->N * pl->P;
+  const void** gtab = (const void**)slot->host;  // indexed by r*P + p
+  void** stab = (void**)(slot->host + n_grad * 8);
+  for (size_t i = 0; i < n_grad; ++i) gtab[i] = grads[i];
+  for (int32_t r = 0; r < pl->N; ++r) stab[r] = slots[r];
+  cudaStream_t s = (cudaStream_t)stream;
+  if ((st = upload_and_mark(slot, (n_grad + (size_t)pl->N) * 8, s)) != TIDE_OK) return st;
+  AgArgs a;
+  a.items = pl->d_pack_items;
+  a.n_items = (int64_t)pl->pack_items.size();
+  a.units = pl->d_pack_units;
+  a.n_units = pl->pack_units;
+  a.shard_tab = (const unsigned char* const*)slot->dev;
+  a.param_tab = (unsigned char* const*)(slot->dev + n_grad * 8);
+  a.elem_bytes = 2;
+  return finish(slot, launch_ag(a, pl->ag_grid, stream), s, "slot pack launch");
+}
+
+tide_status tide_rs_reduce_slots(tide_plan* pl, const void* const* slots, float* const* shards, void* stream) {
+  clear_error();
+  if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  if (!slots) return fail(TIDE_ERR_INVALID_ARG, "slots array is NULL");
+  for (int32_t r = 0; r < pl->N; ++r) {
+    if (!slots[r]) return fail(TIDE_ERR_INVALID_ARG, "slots[" + std::to_string(r) + "] is NULL");
+    for (int32_t p = 0; p < pl->P; ++p)
+      pl->slot_grads[(size_t)r * pl->P + p] = (const unsigned char*)slots[r] + (size_t)2 * pl->N * pl->o[p];
+  }
+  return tide_rs_reduce(pl, pl->slot_grads.data(), shards, stream);
 }
 
 tide_status tide_ag_rd_exchange(tide_plan* pl, void* const* stages, int32_t elem_bytes, void* stream) {

@@ -117,6 +117,7 @@ struct RsArgs {
   const uint8_t* uniform_phase;     // [P]: 1 if all N gradients of p share addr mod 16
   int32_t N, M, L, P;
   int64_t S;                        // packed shard length
+  int32_t epilogue;                 // EPI_AVERAGE | EPI_ACCUMULATE (rs_device.cuh)
   float* inbox;                     // rs_staged only: [M][L][M][L * slice_len] partials
   int64_t slice_len;                // ceil(S / L)
   BulkLayout bulk;                  // rs_bulk only
@@ -153,6 +154,9 @@ struct tide_plan {
   int64_t S = 0;
   std::vector<tide::RsItem> rs_items;
   std::vector<tide::AgItem> ag_items;
+  std::vector<tide::AgItem> ag_items_unpadded;  // ag_items restricted to real rows
+  std::vector<tide::AgItem> pack_items;         // Slot-Reuse: r = grad index r*P+p, p = slot rank
+  std::vector<const void*> slot_grads;          // tide_rs_reduce_slots' pointer array (host)
   std::vector<int64_t> ag_prefix;  // all-gather cost prefix sums (load balance)
   uint8_t order[tide::kOrderTableSize] = {};
 
@@ -166,10 +170,19 @@ struct tide_plan {
   int32_t rs_kernel = 0;                   // 0: direct loads (rs_fused), 1: bulk-copy pipeline
   uint64_t wait_limit_ns = 2000000000ull;  // 2 s
   int64_t test_drop_tile = -1;
+  int32_t rs_epilogue = 0;                 // averaging / accumulate bits
+  bool ag_unpadded = false;
   tide::RsItem* d_rs_items = nullptr;
   tide::AgItem* d_ag_items = nullptr;
   tide::UnitStart* d_ag_units = nullptr;
   int64_t ag_units = 0;
+  // Unpadded all-gather and Slot-Reuse packing work lists and units.
+  tide::AgItem* d_agu_items = nullptr;
+  tide::UnitStart* d_agu_units = nullptr;
+  int64_t agu_units = 0;
+  tide::AgItem* d_pack_items = nullptr;
+  tide::UnitStart* d_pack_units = nullptr;
+  int64_t pack_units = 0;
   // Per-rail all-gather work (tide_ag_stage_place): rail l's items (ranks
   // r = n*L + l) and their equal-cost units.
   tide::AgItem* d_rail_items[tide::kMaxL] = {};

@@ -28,6 +28,9 @@ STATUS_NAMES = {
 TIDE_OPT_RS_KERNEL = 1
 TIDE_OPT_WAIT_LIMIT_NS = 2
 TIDE_OPT_TEST_DROP_TILE = 3
+TIDE_OPT_RS_AVERAGE = 4
+TIDE_OPT_RS_ACCUMULATE = 5
+TIDE_OPT_AG_UNPADDED = 6
 ITEM_FIELDS = ("kind", "p", "r", "src_off", "dst_off", "n")
 
 
@@ -62,6 +65,8 @@ def _load():
         "tide_rs_reduce_noalloc": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
         "tide_plan_set_option": (i32, [vp, i32, i64]),
         "tide_plan_check": (i32, [vp]),
+        "tide_slot_pack": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
+        "tide_rs_reduce_slots": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
         "tide_plan_inbox_elems": (i64, [vp]),
         "tide_rs_staged": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, i32, i32, vp]),
         "tide_rd_rounds": (i32, [i32]),
@@ -149,6 +154,16 @@ def tide_plan_create(shapes, N, M, L):
 
 def tide_plan_destroy(plan):
     _lib.tide_plan_destroy(plan)
+
+
+def tide_slot_pack(plan, grads, slots, stream=None):
+    """Slot-Reuse: copy every rank's bf16 gradients into its all-gather slot."""
+    _check(_lib.tide_slot_pack(plan, _ptr_array(grads), _ptr_array(slots), _stream(stream)))
+
+
+def tide_rs_reduce_slots(plan, slots, shards, stream=None):
+    """tide_rs_reduce reading every rank's gradients from its packed slot."""
+    _check(_lib.tide_rs_reduce_slots(plan, _ptr_array(slots), _ptr_array(shards), _stream(stream)))
 
 
 def tide_plan_inbox_elems(plan):

@@ -142,6 +142,14 @@ tide_status tide_plan_level2_order(const tide_plan* plan, int32_t n_dest, int32_
  *                          out records TIDE_ERR_TIMEOUT for tide_plan_check,
  *                          drains its copies and returns; the outputs of that
  *                          call are then undefined.
+ *   TIDE_OPT_RS_AVERAGE, TIDE_OPT_RS_ACCUMULATE, TIDE_OPT_AG_UNPADDED
+ *                          result variants (below); apply to tide_rs_reduce
+ *                          (both kernels), tide_rs_staged,
+ *                          tide_rs_reduce_noalloc and tide_ag_place.  The
+ *                          pages give neither averaging nor an unpadded
+ *                          destination; accumulating follows "accumulate the
+ *                          result straight into the fp32 gradient shard"
+ *                          ([Endgame] "Reduce-scatter...").
  *   TIDE_OPT_TEST_DROP_TILE  test hook: the bulk kernel's producer withholds
  *                          the given tile (counted per CTA from 0), so the
  *                          consumers' wait runs out; -1 (default) disables.
@@ -149,7 +157,14 @@ tide_status tide_plan_level2_order(const tide_plan* plan, int32_t n_dest, int32_
 typedef enum tide_option {
   TIDE_OPT_RS_KERNEL = 1,
   TIDE_OPT_WAIT_LIMIT_NS = 2,
-  TIDE_OPT_TEST_DROP_TILE = 3
+  TIDE_OPT_TEST_DROP_TILE = 3,
+  TIDE_OPT_RS_AVERAGE = 4,     /* 1: every reduce-scatter result is divided
+                                  by N (fp32, correctly rounded) */
+  TIDE_OPT_RS_ACCUMULATE = 5,  /* 1: the result is added to the shard's
+                                  previous value (one fp32 add, after the sum
+                                  and the division) instead of overwriting */
+  TIDE_OPT_AG_UNPADDED = 6     /* 1: tide_ag_place writes only the R_p real
+                                  rows; params[p] then needs R_p*Kp elements */
 } tide_option;
 tide_status tide_plan_set_option(tide_plan* plan, int32_t option, int64_t value);
 
@@ -222,6 +237,23 @@ tide_status tide_ag_place(tide_plan* plan, const void* const* shards, void* cons
  * tables exceed the 8 MiB array (use tide_rs_reduce for such groups). */
 tide_status tide_rs_reduce_noalloc(const tide_plan* plan, const void* const* grads, float* const* shards,
                                    void* stream);
+
+/* ---- Slot-Reuse ------------------------------------------------------------
+ * [Endgame] "Reduce-scatter: two levels of addition...", last paragraph;
+ * [Abstract] Figure 7: gradients are copied into the all-gather slot that has
+ * just been vacated, so their own memory can be freed at once; the
+ * reduce-scatter then reads them from the slot.  A rank's slot is its
+ * gathered parameter group: N*S bf16 elements, parameter p's padded block at
+ * N*op (the tide_ag_place layout).
+ *
+ * tide_slot_pack: slots[r][N*op + e] = grads[r*P + p][e] for e < R_p*Kp
+ * (bf16).  grads as tide_rs_reduce; slots: host array [N] of device pointers
+ * to N*S elements, 2-byte aligned; the padding rows of a slot are left as
+ * they are.  tide_rs_reduce_slots: tide_rs_reduce with rank r's gradient of
+ * p read at slots[r] + N*op (same options, same bits).  Errors: as
+ * tide_rs_reduce. */
+tide_status tide_slot_pack(tide_plan* plan, const void* const* grads, void* const* slots, void* stream);
+tide_status tide_rs_reduce_slots(tide_plan* plan, const void* const* slots, float* const* shards, void* stream);
 
 /* ---- Reduce-scatter in the pages' two stages -----------------------------
  * [Endgame] "Reduce-scatter: two levels of addition, the last one done by

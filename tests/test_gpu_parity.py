@@ -431,3 +431,75 @@ def test_rs_staged_bit_exact_and_inbox(w, budget):
                         a = got[n_dest, g, c, l_dest * B:l_dest * B + (hi - lo)]
                         b = inbox_o[n_dest, g, c, l_dest * B:l_dest * B + (hi - lo)]
                         assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), (n_dest, g, c, l_dest)
+
+
+# --------------------------------------------------------------- variants
+
+@pytest.mark.parametrize("w", [SMALL[0], SMALL[4], SMALL[5], SMALL[6]], ids=lambda w: w.name)
+@pytest.mark.parametrize("kernel", ["fused", "bulk", "staged", "noalloc"])
+@pytest.mark.parametrize("average,accumulate", [(1, 0), (0, 1), (1, 1)])
+def test_rs_average_and_accumulate(w, kernel, average, accumulate):
+    grads = host_grads(w)
+    geo, sums = oracle_rs(w, grads)
+    old_h = [((np.arange(geo.S, dtype=np.float32) % 97) - 48.5) * np.float32(0.25) for _ in range(w.N)]
+    expect = O.rs_finish(geo, sums, average=bool(average), old=old_h if accumulate else None)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        plan.set_option(tide.TIDE_OPT_RS_AVERAGE, average)
+        plan.set_option(tide.TIDE_OPT_RS_ACCUMULATE, accumulate)
+        if kernel == "bulk":
+            plan.set_option(tide.TIDE_OPT_RS_KERNEL, 1)
+        dev = [[to_dev_u16(grads[r][p])[0] for p in range(w.P)] for r in range(w.N)]
+        flat = [dev[r][p] for r in range(w.N) for p in range(w.P)]
+        outs = [torch.from_numpy(o.copy()).to(DEV) for o in old_h]
+        if kernel == "staged":
+            inbox = torch.empty(tide.tide_plan_inbox_elems(plan.handle), dtype=torch.float32, device=DEV)
+            tide.tide_rs_staged(plan.handle, flat, outs, inbox)
+        elif kernel == "noalloc":
+            tide.tide_rs_reduce_noalloc(plan.handle, flat, outs)
+        else:
+            plan.rs_reduce(flat, outs)
+        plan.check()
+        for r in range(w.N):
+            assert np.array_equal(f32_bits(outs[r]), expect[r].view(np.uint32)), r
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_ag_unpadded_bit_exact(w):
+    geo = O.geometry(w.shapes, w.N)
+    rng = np.random.default_rng(23)
+    shards_h = [rng.integers(0, 65535, geo.S, dtype=np.uint16) for _ in range(w.N)]
+    expect = O.ag_place_unpadded(geo, shards_h)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        plan.set_option(tide.TIDE_OPT_AG_UNPADDED, 1)
+        shards = [torch.from_numpy(s.view(np.int16)).to(DEV) for s in shards_h]
+        backs = [torch.full((GUARD + e.size + GUARD,), -7, dtype=torch.int16, device=DEV) for e in expect]
+        plan.ag_place(shards, [b[GUARD:GUARD + e.size] for b, e in zip(backs, expect)], 2)
+        torch.cuda.synchronize()
+        for p, (b, e) in enumerate(zip(backs, expect)):
+            got = b.cpu().numpy()
+            assert np.array_equal(got[GUARD:GUARD + e.size].view(np.uint16), e), p
+            assert (got[:GUARD] == -7).all() and (got[GUARD + e.size:] == -7).all(), p
+
+
+@pytest.mark.parametrize("w", [SMALL[0], SMALL[1], SMALL[4], SMALL[5]], ids=lambda w: w.name)
+def test_slot_reuse_pack_then_reduce(w):
+    """Slot-Reuse: gradients packed into the vacated all-gather slots, then
+    reduced from there -- same shards as reducing in place."""
+    grads = host_grads(w)
+    geo, expect = oracle_rs(w, grads)
+    packed = O.slot_pack(geo, grads)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        dev = [[to_dev_u16(grads[r][p])[0] for p in range(w.P)] for r in range(w.N)]
+        slots = [torch.full((w.N * geo.S,), 0x5A5A, dtype=torch.int16, device=DEV) for _ in range(w.N)]
+        tide.tide_slot_pack(plan.handle, [dev[r][p] for r in range(w.N) for p in range(w.P)], slots)
+        outs = [torch.empty(geo.S, dtype=torch.float32, device=DEV) for _ in range(w.N)]
+        tide.tide_rs_reduce_slots(plan.handle, slots, outs)
+        torch.cuda.synchronize()
+        for r in range(w.N):
+            got = u16_of(slots[r])
+            mask = np.zeros(w.N * geo.S, dtype=bool)
+            for p in range(w.P):
+                mask[w.N * geo.o[p]:w.N * geo.o[p] + geo.rows[p] * geo.Kp[p]] = True
+            assert np.array_equal(got[mask], packed[r][mask]), r
+            assert (got[~mask] == 0x5A5A).all(), "padding rows of a slot stay untouched"
+            assert np.array_equal(f32_bits(outs[r]), expect[r].view(np.uint32)), r
