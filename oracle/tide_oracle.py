@@ -31,7 +31,9 @@ its use below):
   R3  op is the plain prefix sum of the per-rank piece sizes, no alignment gap.
   R4  the reduction is a plain sum (no averaging), fp32 round-to-nearest-even,
       every accumulator starting from +0.0.
-  R5  level 2 adds the node partials in landing-GPU order g = 0..L-1.
+  R5  level 2 adds the node partials in landing-GPU order g = 0..L-1; with
+      more nodes than GPUs per node, batch by batch (batches of L relative
+      indices, batch sums added in ascending batch order).
   R6  slice s of a destination node is block s of each of its ranks' packed
       shards, cut into L contiguous blocks of ceil(S / L) elements.
   R8  level 1 adds the L local contributions in ascending local index l.
@@ -45,7 +47,7 @@ import numpy as np
 __all__ = [
     "Geometry", "geometry", "rank_major_offset", "param_major_offset", "valid_elems",
     "owner_of_row", "relative_index", "landing_gpu", "handled_slice", "slice_len",
-    "slice_of", "level2_order", "bf16_to_f32", "rs_reduce", "ag_place", "rs_element",
+    "slice_of", "level2_order", "level2_batches", "bf16_to_f32", "rs_reduce", "ag_place", "rs_element",
     "ag_element",
 ]
 
@@ -155,22 +157,31 @@ def slice_of(x, S, L):
     return x // slice_len(S, L)
 
 
-def level2_order(s, n_dest, M, L):
-    """Source nodes of slice s in the order their partials are added (Reading R5).
+def level2_batches(s, n_dest, M, L):
+    """Source nodes of slice s in the order their partials are added, batch
+    by batch (Reading R5).
 
-    The destination's GPUs are visited g = 0, 1, ..., L-1; GPU g holds the
-    partial of the source whose slice s lands on it.  With M < L some GPUs hold
-    nothing for slice s.  More than L sources need the batched scheme of the
-    same section, which this oracle does not cover.
+    Relative indices are taken in batches of L -- batch b holds c in
+    [b*L, (b+1)*L) -- because one read-and-add sums at most one partial per
+    destination GPU; with M <= L there is a single batch.  Within a batch the
+    destination's GPUs are visited g = 0, 1, ..., L-1, GPU g holding the
+    partial of the batch's source whose slice s lands on it (none when c >= M).
     """
-    if M > L:
-        raise NotImplementedError("more nodes than GPUs per node needs source batching")
-    order = []
-    for g in range(L):
-        for n_src in range(M):
-            if landing_gpu(s, relative_index(n_dest, n_src, M), L) == g:
-                order.append(n_src)
-    return order
+    batches = []
+    for b in range(-(-M // L)):
+        order = []
+        for g in range(L):
+            for n_src in range(M):
+                c = relative_index(n_dest, n_src, M)
+                if b * L <= c < (b + 1) * L and landing_gpu(s, c, L) == g:
+                    order.append(n_src)
+        batches.append(order)
+    return batches
+
+
+def level2_order(s, n_dest, M, L):
+    """All source nodes of slice s in addition order (batches concatenated)."""
+    return [n for batch in level2_batches(s, n_dest, M, L) for n in batch]
 
 
 # --------------------------------------------------------------------------
@@ -221,8 +232,11 @@ def rs_reduce(geo, grads, M, L):
                     return grads[src_rank][p][src0:src0 + count]
 
                 acc2 = np.zeros(b - a, dtype=np.float32)      # Reading R4
-                for n_src in level2_order(s, n_dest, M, L):  # level 2, Reading R5
-                    acc2 = acc2 + _node_partial(grad_slice_of, n_src, L, b - a)
+                for batch in level2_batches(s, n_dest, M, L):  # level 2, Reading R5
+                    bsum = np.zeros(b - a, dtype=np.float32)
+                    for n_src in batch:
+                        bsum = bsum + _node_partial(grad_slice_of, n_src, L, b - a)
+                    acc2 = acc2 + bsum
                 out[o_p + a:o_p + b] = acc2
                 a = b
         shards.append(out)
@@ -243,11 +257,14 @@ def rs_element(geo, M, L, r, x, grad_at):
     s = slice_of(x, geo.S, L)
     idx = np.array([r * geo.e[p] + e], dtype=np.int64)
     acc2 = np.float32(0.0)
-    for n_src in level2_order(s, r // L, M, L):
-        acc1 = np.float32(0.0)
-        for l in range(L):
-            acc1 = np.float32(acc1 + bf16_to_f32(grad_at(n_src * L + l, p, idx))[0])
-        acc2 = np.float32(acc2 + acc1)
+    for batch in level2_batches(s, r // L, M, L):
+        bsum = np.float32(0.0)
+        for n_src in batch:
+            acc1 = np.float32(0.0)
+            for l in range(L):
+                acc1 = np.float32(acc1 + bf16_to_f32(grad_at(n_src * L + l, p, idx))[0])
+            bsum = np.float32(bsum + acc1)
+        acc2 = np.float32(acc2 + bsum)
     return acc2
 
 
@@ -385,10 +402,13 @@ def rs_land(geo, inbox, M, L):
             if lo >= hi:
                 continue
             acc = np.zeros(hi - lo, dtype=np.float32)
-            for g in range(L):
-                c = (s - g) % L                         # the source whose slice s lands on GPU g
-                if c < M:
-                    acc = acc + inbox[n_dest, g, c, l_dest * B:l_dest * B + (hi - lo)]
+            for b in range(-(-M // L)):                 # one read-and-add per batch of L sources
+                bsum = np.zeros(hi - lo, dtype=np.float32)
+                for g in range(L):
+                    c = b * L + (s - g) % L             # the batch's source whose slice s lands on GPU g
+                    if c < M:
+                        bsum = bsum + inbox[n_dest, g, c, l_dest * B:l_dest * B + (hi - lo)]
+                acc = acc + bsum
             out[lo:hi] = acc
         shards.append(out)
     return shards

@@ -154,6 +154,33 @@ def check_level2_order_cases():
             assert O.level2_order(s, case["n_dest"], case["M"], case["L"]) == expect
 
 
+def check_level2_batches_cases():
+    for case in _golden("level2_order_cases.json")["batched_cases"]:
+        for s, expect in enumerate(case["batches_by_slice"]):
+            assert O.level2_batches(s, case["n_dest"], case["M"], case["L"]) == expect
+    # with M <= L there is one batch, the landing-GPU order
+    for case in _golden("level2_order_cases.json")["cases"]:
+        for s, expect in enumerate(case["order_by_slice"]):
+            assert O.level2_batches(s, case["n_dest"], case["M"], case["L"]) == [expect]
+
+
+def check_level2_batches_property():
+    """Every source appears once per slice; a batch never puts two sources on
+    one landing GPU; batch b holds exactly relative indices [bL, bL+L) < M."""
+    for L in range(1, 9):
+        for M in range(1, 3 * L + 2):
+            for n_dest in range(M):
+                for s in range(L):
+                    bs = O.level2_batches(s, n_dest, M, L)
+                    flat = [n for b in bs for n in b]
+                    assert sorted(flat) == list(range(M))
+                    for b, batch in enumerate(bs):
+                        cs = sorted(O.relative_index(n_dest, n, M) for n in batch)
+                        assert cs == list(range(b * L, min(M, (b + 1) * L)))
+                        gpus = [O.landing_gpu(s, O.relative_index(n_dest, n, M), L) for n in batch]
+                        assert len(set(gpus)) == len(gpus) and gpus == sorted(gpus)
+
+
 def check_level2_order_cancellation():
     """Order-sensitive sums whose fp32 results were worked out by hand."""
     for g in _golden("level2_order_cases.json")["cancellations"]:

@@ -23,13 +23,15 @@ MUTATIONS = {
     "param-major transposed": ("return geo.N * geo.o[p] + r * geo.e[p]",
                                "return r * geo.S + geo.o[p]"),
     "dropped local term": ("    for l in range(L):\n        acc1", "    for l in range(L - 1):\n        acc1"),
-    "wrong sign at level 2": ("acc2 = acc2 + _node_partial", "acc2 = acc2 - _node_partial"),
+    "wrong sign at level 2": ("bsum = bsum + _node_partial", "bsum = bsum - _node_partial"),
     "source row index": ("src0 = r * e_p + a", "src0 = r * geo.Rp[p] + a"),
     "source rank transposed": ("return grads[src_rank][p][src0:src0 + count]",
                                "return grads[(src_rank % L) * M + src_rank // L][p][src0:src0 + count]"),
     "bf16 widening shift": ("<< np.uint32(16)).view", "<< np.uint32(15)).view"),
-    "ascending node order": ("                order.append(n_src)\n    return order",
-                             "                order.append(n_src)\n    return sorted(order)"),
+    "ascending node order": ("                    order.append(n_src)\n        batches.append(order)",
+                             "                    order.append(n_src)\n        batches.append(sorted(order))"),
+    "flat level 2 across batches": ("                    acc2 = acc2 + bsum\n                out[o_p + a:o_p + b] = acc2",
+                                    "                    acc2 = bsum\n                out[o_p + a:o_p + b] = acc2"),
     "slice length floor": ("return -(-S // L) if S > 0 else 0", "return S // L if S > 0 else 0"),
     "padding not zeroed": ("out[o_p + v:o_p + e_p] = np.float32(0.0)",
                            "out[o_p + v:o_p + e_p] = np.float32(1.0)"),
@@ -39,13 +41,16 @@ MUTATIONS = {
     # +0.0 absorbs it); starting both at the first term (-0.0 here) does.
     "accumulators start at first term": [
         ("acc1 = np.zeros(count, dtype=np.float32)", "acc1 = np.full(count, -0.0, dtype=np.float32)"),
-        ("acc2 = np.zeros(b - a, dtype=np.float32)", "acc2 = np.full(b - a, -0.0, dtype=np.float32)")],
+        ("acc2 = np.zeros(b - a, dtype=np.float32)      # Reading R4",
+         "acc2 = np.full(b - a, -0.0, dtype=np.float32)      # Reading R4"),
+        ("bsum = np.zeros(b - a, dtype=np.float32)\n                    for n_src in batch:\n                        bsum = bsum + _node_partial",
+         "bsum = np.full(b - a, -0.0, dtype=np.float32)\n                    for n_src in batch:\n                        bsum = bsum + _node_partial")],
     "recursive doubling sends 2^d": ("return min(2 ** d, M - 2 ** d)", "return 2 ** d"),
     "recursive doubling from the lower node": ("have[n] = have[n] + sent[(n + 2 ** d) % M]",
                                                "have[n] = have[n] + sent[(n - 2 ** d) % M]"),
     "stage slot rotated the wrong way": ("r = ((node + k) % M) * L + rail", "r = ((node - k) % M) * L + rail"),
-    "landing stage adds a wrong source": ("c = (s - g) % L                         # the source",
-                                          "c = (s + g) % L                         # the source"),
+    "landing stage adds a wrong source": ("c = b * L + (s - g) % L             # the batch's source",
+                                          "c = b * L + (s + g) % L             # the batch's source"),
     "average divides by M": ("x = (x / np.float32(geo.N)).astype(np.float32)",
                              "x = (x / np.float32(geo.N - 1 or 1)).astype(np.float32)"),
     "slot pack at op": ("slot[geo.N * geo.o[p]:geo.N * geo.o[p] + n] = grads[r][p][:n]",
