@@ -26,16 +26,21 @@ bool add_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_add_overflow
 // levels of addition, the last one done by NVSwitch" in "The Endgame of FSDP
 // Communication"; the preprint's Figure 6(b)).  Slice s from the source with
 // relative index c = (n_dest - n_src) mod M lands on destination GPU
-// (s - c) mod L, so GPU g holds c = (s - g) mod L, if that c is below M.  The
-// partials are added in landing-GPU order g = 0..L-1.
+// (s - c) mod L, so within batch b GPU g holds c = b*L + (s - g) mod L, if that
+// c is below M.  The partials are added in landing-GPU order g = 0..L-1, batch
+// after batch.
 void build_order_table(tide_plan* pl) {
   const int M = pl->M, L = pl->L;
   for (int n_dest = 0; n_dest < M; ++n_dest) {
     for (int s = 0; s < L; ++s) {
       int k = 0;
-      for (int g = 0; g < L; ++g) {
-        const int c = ((s - g) % L + L) % L;
-        if (c < M) pl->order[(n_dest * L + s) * M + k++] = (uint8_t)(((n_dest - c) % M + M) % M);
+      // With M > L the sources go in batches of L relative indices (one
+      // read-and-add sums at most one partial per destination GPU).
+      for (int b = 0; b * L < M; ++b) {
+        for (int g = 0; g < L; ++g) {
+          const int c = b * L + ((s - g) % L + L) % L;
+          if (c < M) pl->order[(n_dest * L + s) * M + k++] = (uint8_t)(((n_dest - c) % M + M) % M);
+        }
       }
     }
   }
@@ -200,9 +205,8 @@ tide_status tide_plan_create(const tide_group_desc* d, tide_plan** out_plan) {
   if (d->P > 0 && (!d->ndim || !d->dims)) return fail(TIDE_ERR_INVALID_ARG, "ndim or dims is NULL");
   if (d->L < 1 || d->L > kMaxL) return fail(TIDE_ERR_INVALID_ARG, "L must be in [1, 8]");
   if (d->M < 1) return fail(TIDE_ERR_INVALID_ARG, "M must be >= 1");
+  if (d->M > kMaxM) return fail(TIDE_ERR_INVALID_ARG, "M must be at most 32");
   if ((int64_t)d->M * d->L != d->N) return fail(TIDE_ERR_INVALID_ARG, "N must equal M*L");
-  if (d->M > d->L)
-    return fail(TIDE_ERR_UNIMPLEMENTED, "M > L needs batched source inboxes (not built)");
 
   tide_plan* pl = new (std::nothrow) tide_plan();
   if (!pl) return fail(TIDE_ERR_OUT_OF_MEMORY, "plan allocation failed");

@@ -338,11 +338,17 @@ __device__ void consumers(const RsArgs& a, const Smem& m) {
         for (int e = tid; e < d.n; e += kConsumers) {
           const int x = e + d.ph;
           const float* pv = part + (x >> 3) * PS + (x & 7);
-          float acc2 = 0.f;
+          float acc2 = 0.f, bsum = 0.f;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t node = (k < 4 ? d.ord_lo >> (8 * k) : d.ord_hi >> (8 * (k - 4))) & 0xFFu;
-            if (k < M) acc2 = __fadd_rn(acc2, pv[node * 8]);
+            if (k < M) {
+              bsum = __fadd_rn(bsum, pv[node * 8]);
+              if ((k + 1) % L == 0 || k + 1 == M) {  // end of a batch of L sources
+                acc2 = __fadd_rn(acc2, bsum);
+                bsum = 0.f;
+              }
+            }
           }
           __stcs(d.dst + e, epilogue1(acc2, d.dst + e, a.epilogue, a.N));
         }
@@ -360,9 +366,9 @@ __device__ void consumers(const RsArgs& a, const Smem& m) {
       consumer_barrier();
       for (int e0 = tid * 8; e0 < d.n; e0 += kConsumers * 8) {
         const int cnt = min(8, d.n - e0);
-        float acc2[8];
+        float acc2[8], bsum[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc2[i] = 0.f;
+        for (int i = 0; i < 8; ++i) acc2[i] = bsum[i] = 0.f;
         for (int k = 0; k < M; ++k) {
           const int node = (int)(((k < 4 ? d.ord_lo >> (8 * k) : d.ord_hi >> (8 * (k - 4)))) & 0xFFu);
           float acc1[8];
@@ -376,7 +382,14 @@ __device__ void consumers(const RsArgs& a, const Smem& m) {
               if (i < cnt) acc1[i] = __fadd_rn(acc1[i], __uint_as_float((uint32_t)__ldcs(s + i) << 16));
           }
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc2[i] = __fadd_rn(acc2[i], acc1[i]);
+          for (int i = 0; i < 8; ++i) bsum[i] = __fadd_rn(bsum[i], acc1[i]);
+          if ((k + 1) % L == 0 || k + 1 == M) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              acc2[i] = __fadd_rn(acc2[i], bsum[i]);
+              bsum[i] = 0.f;
+            }
+          }
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i)

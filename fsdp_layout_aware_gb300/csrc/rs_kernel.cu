@@ -49,6 +49,9 @@ __device__ __forceinline__ void reduce_aligned(const uint16_t* const* src, const
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc2[i] = 0.f;
     if (v < nvec) {
+      float bsum[8];  // the current batch's read-and-add (batches of L sources)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) bsum[i] = 0.f;
       for (int k = 0; k < M; ++k) {
         const int node = ord[k];
         uint4 x[L];
@@ -60,7 +63,14 @@ __device__ __forceinline__ void reduce_aligned(const uint16_t* const* src, const
 #pragma unroll
         for (int l = 0; l < L; ++l) add_bf16x8(acc1, x[l]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc2[i] = __fadd_rn(acc2[i], acc1[i]);
+        for (int i = 0; i < 8; ++i) bsum[i] = __fadd_rn(bsum[i], acc1[i]);
+        if ((k + 1) % L == 0 || k + 1 == M) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            acc2[i] = __fadd_rn(acc2[i], bsum[i]);
+            bsum[i] = 0.f;
+          }
+        }
       }
     }
     epilogue8(acc2, dst, e0, n, epi, N);
@@ -79,9 +89,9 @@ __device__ __forceinline__ void reduce_unaligned(const uint16_t* const* src, con
   for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
     const int e0 = v * 8;
     const int cnt = min(8, n - e0);
-    float acc2[8];
+    float acc2[8], bsum[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc2[i] = 0.f;
+    for (int i = 0; i < 8; ++i) acc2[i] = bsum[i] = 0.f;
     for (int k = 0; k < M; ++k) {
       const int node = ord[k];
       float acc1[8];
@@ -95,7 +105,14 @@ __device__ __forceinline__ void reduce_unaligned(const uint16_t* const* src, con
           if (i < cnt) acc1[i] = __fadd_rn(acc1[i], bf16_to_f32(__ldcs(s + i)));
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc2[i] = __fadd_rn(acc2[i], acc1[i]);
+      for (int i = 0; i < 8; ++i) bsum[i] = __fadd_rn(bsum[i], acc1[i]);
+      if ((k + 1) % L == 0 || k + 1 == M) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          acc2[i] = __fadd_rn(acc2[i], bsum[i]);
+          bsum[i] = 0.f;
+        }
+      }
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i)

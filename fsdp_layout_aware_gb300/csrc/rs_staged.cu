@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(kRsThreads, 4) rs_sum_kernel(const __grid_cons
 // memory keeps the kernel at about 32 registers, so eight CTAs fit per SM.
 __global__ void __launch_bounds__(256, 8) rs_land_kernel(const float* __restrict__ inbox, float* const* shard_tab,
                                                         int M, int L, int64_t S, int64_t B, int epi) {
-  __shared__ const float* part[kMaxL];
+  __shared__ const float* part[kMaxM];
   __shared__ int n_part;
   const int r = blockIdx.y;
   const int n_dest = r / L, l_dest = r % L;
@@ -133,22 +133,31 @@ __global__ void __launch_bounds__(256, 8) rs_land_kernel(const float* __restrict
     __syncthreads();  // the previous slice's readers of part[] are done
     if (threadIdx.x == 0) {
       int k = 0;
-      for (int g = 0; g < L; ++g) {
-        const int c = ((s - g) % L + L) % L;  // the source whose slice s landed on GPU g
-        if (c < M) part[k++] = inbox + ((int64_t)(n_dest * L + g) * M + c) * slot + (int64_t)l_dest * B - lo;
+      for (int b = 0; b * L < M; ++b) {  // batches of L sources, each a read-and-add
+        for (int g = 0; g < L; ++g) {
+          const int c = b * L + ((s - g) % L + L) % L;  // the batch's source whose slice s landed on GPU g
+          if (c < M) part[k++] = inbox + ((int64_t)(n_dest * L + g) * M + c) * slot + (int64_t)l_dest * B - lo;
+        }
       }
       n_part = k;
     }
     __syncthreads();
     const int np = n_part;
     for (int64_t x0 = lo + (int64_t)blockIdx.x * blockDim.x * 4 + threadIdx.x; x0 < hi; x0 += step) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc[4] = {0.f, 0.f, 0.f, 0.f}, bsum[4] = {0.f, 0.f, 0.f, 0.f};
       for (int j = 0; j < np; ++j) {
         const float* pj = part[j];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int64_t x = x0 + (int64_t)u * blockDim.x;
-          if (x < hi) acc[u] = __fadd_rn(acc[u], __ldcs(pj + x));
+          if (x < hi) bsum[u] = __fadd_rn(bsum[u], __ldcs(pj + x));
+        }
+        if ((j + 1) % L == 0 || j + 1 == np) {  // end of a batch
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            acc[u] = __fadd_rn(acc[u], bsum[u]);
+            bsum[u] = 0.f;
+          }
         }
       }
 #pragma unroll

@@ -356,6 +356,8 @@ tide_status tide_rs_reduce(tide_plan* pl, const void* const* grads, float* const
   clear_error();
   if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
   if (pl->rs_items.empty()) return TIDE_OK;  // S == 0: nothing to write
+  if (pl->rs_kernel == 1 && pl->M > 8)
+    return fail(TIDE_ERR_UNIMPLEMENTED, "the bulk-copy kernel handles at most 8 nodes (TIDE_OPT_RS_KERNEL = 0 does)");
   RsArgs a;
   tide_plan::Slot* slot = nullptr;
   tide_status st = prepare_rs(pl, grads, shards, stream, &a, &slot);

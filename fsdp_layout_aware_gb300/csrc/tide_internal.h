@@ -13,7 +13,8 @@ namespace tide {
 
 // Largest supported group: ranks and GPUs per NVSwitch domain.
 constexpr int kMaxL = 8;                 // at most eight GPUs per domain
-constexpr int kMaxN = kMaxL * kMaxL;     // M <= L, so N <= 64
+constexpr int kMaxM = 32;                // nodes (more than L: sources go in batches of L)
+constexpr int kMaxN = kMaxL * kMaxM;     // ranks
 constexpr int kMaxNdim = 8;
 
 // Work-item kinds (RS_VALID / RS_PAD for the reduce-scatter list, AG for the
@@ -82,8 +83,10 @@ TIDE_HD inline int32_t ag_split(const AgItem& it, int64_t rel) {
 }
 
 // Level-2 order table: order[(n_dest * L + s) * M + k] is the k-th source node
-// whose partial is added for slice s of destination node n_dest.
-constexpr int kOrderTableSize = kMaxL * kMaxL * kMaxL;
+// whose partial is added for slice s of destination node n_dest.  The M
+// entries run batch by batch (batches of L relative indices; every batch but
+// the last is full), so a batch ends after every L entries and at the last.
+constexpr int kOrderTableSize = kMaxM * kMaxL * kMaxM;
 
 // Kernel argument blocks (passed by value as __grid_constant__).
 // Start of a unit: item index and first element of that item.  Unit u spans

@@ -70,9 +70,9 @@ typedef enum tide_status {
  *   dims  the P shapes concatenated, dim 0 first; every dim >= 0
  *   M, L  nodes and GPUs per node: 1 <= L <= 8 (at most eight GPUs per
  *         NVSwitch domain, [Endgame] "Where I think it falls short"),
- *         1 <= M <= L (more nodes than GPUs per node needs the batched
- *         inbox scheme of [Endgame] "Reduce-scatter: two levels of
- *         addition...", which returns TIDE_ERR_UNIMPLEMENTED)
+ *         1 <= M <= 32.  With M > L the level-2 sum runs in batches of L
+ *         sources ([Endgame] "Reduce-scatter: two levels of addition...":
+ *         more machines than a read-and-add can take go in batches)
  *   N     must equal M*L.
  * The descriptor is copied; the caller may free it after tide_plan_create. */
 typedef struct tide_group_desc {
@@ -89,8 +89,8 @@ typedef struct tide_plan tide_plan;  /* opaque; owned by the library */
 /* Build the geometry (Kp, Rp, e_p, op, S) and the per-CTA work lists of a
  * group.  Host-only: touches no GPU.  On success *out_plan owns host memory
  * until tide_plan_destroy.  Errors: INVALID_ARG (null pointer, N != M*L,
- * L or M out of range, negative dim, ndim > 8), UNIMPLEMENTED (M > L),
- * OVERFLOW (N*S or a shape product beyond int64), OUT_OF_MEMORY. */
+ * L or M out of range, negative dim, ndim > 8), OVERFLOW (N*S or a shape
+ * product beyond int64), OUT_OF_MEMORY. */
 tide_status tide_plan_create(const tide_group_desc* desc, tide_plan** out_plan);
 
 /* Release a plan and its host and device state.  NULL-safe.  Waits for the
@@ -121,7 +121,8 @@ tide_status tide_plan_get_items(const tide_plan* plan, int32_t which, int64_t* o
 
 /* Level-2 summation order used by tide_rs_reduce for slice s (0 <= s < L)
  * of destination node n_dest (0 <= n_dest < M): writes the M source node
- * numbers, in the order their fp32 partials are added, to out[0..M).  The
+ * numbers, in the order their fp32 partials are added, to out[0..M) (batch
+ * after batch when M > L: a batch ends after every L entries).  The
  * order is the Latin-square landing order of [Endgame] "Reduce-scatter: two
  * levels of addition, the last one done by NVSwitch" and [Abstract]
  * Figure 6(b): destination GPU g = 0..L-1 holds the partial of the source
@@ -136,7 +137,8 @@ tide_status tide_plan_level2_order(const tide_plan* plan, int32_t n_dest, int32_
  *                          memory with bulk copies (TMA).  Both add in the
  *                          same order and give bit-identical results; the
  *                          bulk path pays one copy request per contributor
- *                          window, so it suits groups with few ranks.
+ *                          window, so it suits groups with few ranks; it
+ *                          takes at most 8 nodes (UNIMPLEMENTED beyond).
  *   TIDE_OPT_WAIT_LIMIT_NS bound, in nanoseconds, on every wait inside the
  *                          bulk-copy kernel (default 2e9).  A kernel that runs
  *                          out records TIDE_ERR_TIMEOUT for tide_plan_check,
@@ -192,7 +194,9 @@ tide_status tide_plan_check(tide_plan* plan);
  *            GPU g = 0..L-1 they land on under the Latin-square placement:
  *            slice s = (op+e) / ceil(S/L); GPU g holds the partial of the
  *            source whose relative index c = (n_d - n) mod M satisfies
- *            (s - c) mod L == g.
+ *            (s - c) mod L == g.  When M > L, relative indices go in batches
+ *            [b*L, b*L + L): each batch is summed that way from +0.0 and the
+ *            batch sums are added in ascending b.
  * and +0.0 for a padding row.  The result is bit-identical to that order.
  * Errors: INVALID_ARG (null plan/arrays/pointer), ALIGNMENT, CUDA,
  * OUT_OF_MEMORY (first call's device set-up), DEVICE_MISMATCH. */

@@ -45,6 +45,10 @@ GROUPS = [
     ([(1, 9), (16, 8), (31, 3), (0, 5)], 4, 4),
     ([(49, 3), (97, 4095), (1, 1), (48, 1), (47, 1)], 6, 8),
     ([(100000, 3), (3, 70001)], 3, 5),
+    # more nodes than GPUs per node: level-2 sources in batches of L
+    ([(13, 5), (2, 7), (17,), (6, 6)], 4, 2),
+    ([(9, 3), (33, 2), (1,)], 7, 3),
+    ([(41, 5), (3, 9)], 12, 8),
 ]
 
 
@@ -122,7 +126,7 @@ def test_workload_geometry_matches_oracle(cfg):
 
 def test_all_level2_orders_small_groups():
     for L in range(1, 9):
-        for M in range(1, L + 1):
+        for M in list(range(1, 2 * L + 2)) + [32]:
             with tide.TidePlan([(2 * M * L, 3)], M * L, M, L) as plan:
                 for n_dest in range(M):
                     for s in range(L):
@@ -133,7 +137,7 @@ def test_all_level2_orders_small_groups():
     ([(4, 4)], 4, 2, 3, 1),      # N != M*L
     ([(4, 4)], 18, 2, 9, 1),     # L > 8
     ([(4, 4)], 0, 0, 4, 1),      # M < 1
-    ([(4, 4)], 8, 4, 2, 6),      # M > L: batched inboxes not built
+    ([(4, 4)], 66, 33, 2, 1),    # M > 32
     ([(-1, 4)], 4, 1, 4, 1),     # negative dim
     ([(1,) * 9], 4, 1, 4, 1),    # ndim > 8
     ([(4, 1 << 40, 1 << 40)], 4, 1, 4, 3),   # row length overflow
