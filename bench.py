@@ -46,10 +46,14 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--path", choices=["fused", "staged-rs", "rd-ag"], default="fused",
+    ap.add_argument("--path", choices=["fused", "staged-rs", "rd-ag", "variants"], default="fused",
                     help="fused: the hot path (RS + AG per step); staged-rs: the two-stage reduce-scatter "
                          "through an inbox; rd-ag: the all-gather by recursive-doubling exchange and stage "
-                         "placement")
+                         "placement; variants: averaging / accumulating RS, Slot-Reuse pack + RS from "
+                         "slots, unpadded AG")
+    ap.add_argument("--nodes", type=int, default=0,
+                    help="regroup the workload's N ranks as this many nodes of N / nodes GPUs (e.g. 16 for "
+                         "wan22dit as 16 x 4: more nodes than GPUs per node)")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     help="llama70b (default), qwen3moe, wan22dit, uneven or tiny")
     ap.add_argument("--row-div", type=int, default=1,
@@ -190,6 +194,10 @@ def get_workload(args):
     w = configs.get(args.workload)
     if args.row_div > 1:
         w = configs.scaled(w, row_div=args.row_div, name=f"{w.name}_rows{args.row_div}")
+    if args.nodes:
+        if w.N % args.nodes:
+            raise SystemExit(f"--nodes {args.nodes} does not divide N = {w.N}")
+        w = configs.scaled(w, M=args.nodes, L=w.N // args.nodes, name=f"{w.name}_{args.nodes}x{w.N // args.nodes}")
     return w
 
 
@@ -568,6 +576,51 @@ def run_rd_ag(args, local_rank):
             "direct_landing_ms": round(ta * 1e3, 4)}
 
 
+def run_variants(args, local_rank):
+    """The listed variants, each timed alone on the workload: the reduce-scatter
+    averaged over N and/or accumulated into the previous shard, Slot-Reuse
+    (pack into the vacated all-gather slot, then the reduce-scatter reading
+    the slots), and the all-gather writing only the real rows."""
+    import torch
+
+    import fsdp_layout_aware_gb300 as tide
+    w, plan, stream, dev, grads, ag_in = _setup_inputs(args, local_rank)
+    nb = algorithmic_bytes(w, plan)
+    N, S, G = w.N, plan.S, nb["G"]
+    shards = [torch.zeros(S, dtype=torch.float32, device=dev) for _ in range(N)]
+    gp, sp, ap = tide.pointer_array(grads), tide.pointer_array(shards), tide.pointer_array(ag_in)
+    params = [torch.empty(N * plan.e[p], dtype=torch.int16, device=dev) for p in range(w.P)]
+    pp = tide.pointer_array(params)
+    res = {}
+
+    def timed(name, fn, nbytes, setup=None):
+        with torch.cuda.stream(stream):
+            t = _event_time(fn, args.steps, args.warmup, stream)
+        res[name] = {"ms": round(t * 1e3, 4), "bytes": nbytes, "GB_s": round(nbytes / t / 1e9, 1)}
+
+    timed("rs_plain", lambda: plan.rs_reduce(gp, sp, stream), nb["rs_bytes"])
+    plan.set_option(tide.TIDE_OPT_RS_AVERAGE, 1)
+    timed("rs_average", lambda: plan.rs_reduce(gp, sp, stream), nb["rs_bytes"])
+    plan.set_option(tide.TIDE_OPT_RS_ACCUMULATE, 1)
+    timed("rs_average_accumulate", lambda: plan.rs_reduce(gp, sp, stream), nb["rs_bytes"] + 4 * N * S)
+    plan.set_option(tide.TIDE_OPT_RS_AVERAGE, 0)
+    plan.set_option(tide.TIDE_OPT_RS_ACCUMULATE, 0)
+    plan.set_option(tide.TIDE_OPT_AG_UNPADDED, 1)
+    timed("ag_unpadded", lambda: plan.ag_place(ap, pp, 2, stream), 4 * G)
+    plan.set_option(tide.TIDE_OPT_AG_UNPADDED, 0)
+    del params, pp
+    # Slot-Reuse: every rank's slot is its N*S-element all-gather destination
+    slots = [torch.empty(N * S, dtype=torch.int16, device=dev) for _ in range(N)]
+    slp = tide.pointer_array(slots)
+    timed("slot_pack", lambda: tide.tide_slot_pack(plan.handle, gp, slp, stream), 4 * N * G)
+    timed("rs_from_slots", lambda: tide.tide_rs_reduce_slots(plan.handle, slp, sp, stream), nb["rs_bytes"])
+    plan.check()
+    return {"path": "variants", "metric": METRIC, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "dtype": "f32 sums of bf16", "data": "synthetic",
+            "config": {"workload": f"{w.name}: {w.notes}", "N": N, "M": w.M, "L": w.L, "G": G, "S": S},
+            "value": res["rs_average_accumulate"]["GB_s"], "variants": res}
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local_rank = dist_env()
@@ -577,6 +630,8 @@ def main(argv=None):
         line = run_staged_rs(args, local_rank) if rank == 0 else None
     elif args.path == "rd-ag":
         line = run_rd_ag(args, local_rank) if rank == 0 else None
+    elif args.path == "variants":
+        line = run_variants(args, local_rank) if rank == 0 else None
     else:
         line = run_ours(args, rank, world, local_rank)
     if line is not None:

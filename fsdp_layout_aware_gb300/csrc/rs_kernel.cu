@@ -33,9 +33,8 @@ namespace {
 // granules may extend past the item's range; they never leave the 16-byte
 // granule of a valid element, so they stay inside mapped memory, and the
 // extra lanes are never stored.
-template <int L>
-__device__ __forceinline__ void reduce_aligned(const uint16_t* const* src, const uint8_t* ord, int M, float* dst,
-                                               int n, int epi, int N) {
+template <int L, bool kBatched>
+__device__ __forceinline__ void reduce_aligned(const uint16_t* const* src, int M, float* dst, int n, int epi, int N) {
   const int ph = (int)(((uintptr_t)src[0] >> 1) & 7);
   const int nvec = (ph + n + 7) >> 3;
   // elements from a vector's first element to the next 16-byte boundary of dst
@@ -49,27 +48,33 @@ __device__ __forceinline__ void reduce_aligned(const uint16_t* const* src, const
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc2[i] = 0.f;
     if (v < nvec) {
-      float bsum[8];  // the current batch's read-and-add (batches of L sources)
+      // With M <= L there is one batch and acc2 is its sum (+0.0 + b == b:
+      // a sum started at +0.0 is never -0.0), so only M > L keeps a batch sum.
+      float bsum[kBatched ? 8 : 1];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) bsum[i] = 0.f;
+      for (int i = 0; i < (kBatched ? 8 : 1); ++i) bsum[i] = 0.f;
       for (int k = 0; k < M; ++k) {
-        const int node = ord[k];
         uint4 x[L];
 #pragma unroll
-        for (int l = 0; l < L; ++l) x[l] = __ldcs(reinterpret_cast<const uint4*>(src[node * L + l] + e0));
+        for (int l = 0; l < L; ++l) x[l] = __ldcs(reinterpret_cast<const uint4*>(src[k * L + l] + e0));
         float acc1[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc1[i] = 0.f;
 #pragma unroll
         for (int l = 0; l < L; ++l) add_bf16x8(acc1, x[l]);
+        if constexpr (kBatched) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) bsum[i] = __fadd_rn(bsum[i], acc1[i]);
-        if ((k + 1) % L == 0 || k + 1 == M) {
+          for (int i = 0; i < 8; ++i) bsum[i] = __fadd_rn(bsum[i], acc1[i]);
+          if ((k + 1) % L == 0 || k + 1 == M) {  // end of a batch of L sources
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            acc2[i] = __fadd_rn(acc2[i], bsum[i]);
-            bsum[i] = 0.f;
+            for (int i = 0; i < 8; ++i) {
+              acc2[i] = __fadd_rn(acc2[i], bsum[i]);
+              bsum[i] = 0.f;
+            }
           }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc2[i] = __fadd_rn(acc2[i], acc1[i]);
         }
       }
     }
@@ -82,9 +87,9 @@ __device__ __forceinline__ void reduce_aligned(const uint16_t* const* src, const
 }
 
 // Contributors at different address phases: element-wise loads, same order.
-template <int L>
-__device__ __forceinline__ void reduce_unaligned(const uint16_t* const* src, const uint8_t* ord, int M, float* dst,
-                                                 int n, int epi, int N) {
+template <int L, bool kBatched>
+__device__ __forceinline__ void reduce_unaligned(const uint16_t* const* src, int M, float* dst, int n, int epi,
+                                                 int N) {
   const int nvec = (n + 7) >> 3;
   for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
     const int e0 = v * 8;
@@ -93,25 +98,29 @@ __device__ __forceinline__ void reduce_unaligned(const uint16_t* const* src, con
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc2[i] = bsum[i] = 0.f;
     for (int k = 0; k < M; ++k) {
-      const int node = ord[k];
       float acc1[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc1[i] = 0.f;
 #pragma unroll
       for (int l = 0; l < L; ++l) {
-        const uint16_t* s = src[node * L + l] + e0;
+        const uint16_t* s = src[k * L + l] + e0;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           if (i < cnt) acc1[i] = __fadd_rn(acc1[i], bf16_to_f32(__ldcs(s + i)));
       }
+      if constexpr (kBatched) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) bsum[i] = __fadd_rn(bsum[i], acc1[i]);
-      if ((k + 1) % L == 0 || k + 1 == M) {
+        for (int i = 0; i < 8; ++i) bsum[i] = __fadd_rn(bsum[i], acc1[i]);
+        if ((k + 1) % L == 0 || k + 1 == M) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          acc2[i] = __fadd_rn(acc2[i], bsum[i]);
-          bsum[i] = 0.f;
+          for (int i = 0; i < 8; ++i) {
+            acc2[i] = __fadd_rn(acc2[i], bsum[i]);
+            bsum[i] = 0.f;
+          }
         }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc2[i] = __fadd_rn(acc2[i], acc1[i]);
       }
     }
 #pragma unroll
@@ -125,7 +134,7 @@ __device__ __forceinline__ void reduce_unaligned(const uint16_t* const* src, con
 // whatever the items' sizes, and at any moment the CTAs are on neighbouring
 // items, so the contributors are read in nearly address order across the GPU.
 // Without a counter (noalloc entry point) CTA b takes items b, b+G, b+2G, ...
-template <int L>
+template <int L, bool kBatched>
 __global__ void __launch_bounds__(kRsThreads, 4) rs_fused_kernel(const __grid_constant__ RsArgs a) {
   __shared__ const uint16_t* src[kMaxN];
   __shared__ long long next_item[2];
@@ -143,30 +152,40 @@ __global__ void __launch_bounds__(kRsThreads, 4) rs_fused_kernel(const __grid_co
     if (item.kind == RS_PAD) {
       pad_fill(dst, item.n, a.epilogue, threadIdx.x, blockDim.x);
     } else {
-      if ((int)threadIdx.x < a.N)
-        src[threadIdx.x] = a.grad_tab[(int64_t)item.p * a.N + threadIdx.x] + item.src_off;
+      // src[k * L + l]: contributor l of the k-th node in level-2 order
+      if ((int)threadIdx.x < a.N) {
+        const int k = (int)threadIdx.x / L, l = (int)threadIdx.x % L;
+        const int node = a.order[((item.r / L) * L + item.slice) * a.M + k];
+        src[threadIdx.x] = a.grad_tab[(int64_t)item.p * a.N + node * L + l] + item.src_off;
+      }
       __syncthreads();
-      const uint8_t* ord = a.order + ((item.r / L) * L + item.slice) * a.M;
       if (a.uniform_phase[item.p])
-        reduce_aligned<L>(src, ord, a.M, dst, item.n, a.epilogue, a.N);
+        reduce_aligned<L, kBatched>(src, a.M, dst, item.n, a.epilogue, a.N);
       else
-        reduce_unaligned<L>(src, ord, a.M, dst, item.n, a.epilogue, a.N);
+        reduce_unaligned<L, kBatched>(src, a.M, dst, item.n, a.epilogue, a.N);
     }
     __syncthreads();  // next_item[slot] is visible; this item's readers of src[] are done
   }
 }
 
+// M > L (sources in batches) takes its own instantiation, so the usual
+// M <= L kernel keeps its registers for loads in flight.
 template <int L>
 int launch_rs_t(const RsArgs& a, int grid, cudaStream_t s) {
-  rs_fused_kernel<L><<<grid, kRsThreads, 0, s>>>(a);
+  if (a.M > L)
+    rs_fused_kernel<L, true><<<grid, kRsThreads, 0, s>>>(a);
+  else
+    rs_fused_kernel<L, false><<<grid, kRsThreads, 0, s>>>(a);
   return (int)cudaGetLastError();
 }
 
 template <int L>
 int occupancy_t() {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, rs_fused_kernel<L>, kRsThreads, 0) != cudaSuccess) return 0;
-  return n;
+  int n = 0, nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, rs_fused_kernel<L, false>, kRsThreads, 0) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, rs_fused_kernel<L, true>, kRsThreads, 0) != cudaSuccess)
+    return 0;
+  return n < nb ? n : nb;
 }
 
 }  // namespace
