@@ -34,6 +34,8 @@ its use below):
   R5  level 2 adds the node partials in landing-GPU order g = 0..L-1; with
       more nodes than GPUs per node, batch by batch (batches of L relative
       indices, batch sums added in ascending batch order).
+  R14 the alternative order ``RELATIVE``: within each batch the partials are
+      added in ascending relative index c = (n_dest - n_src) mod M instead.
   R6  slice s of a destination node is block s of each of its ranks' packed
       shards, cut into L contiguous blocks of ceil(S / L) elements.
   R8  level 1 adds the L local contributions in ascending local index l.
@@ -47,8 +49,8 @@ import numpy as np
 __all__ = [
     "Geometry", "geometry", "rank_major_offset", "param_major_offset", "valid_elems",
     "owner_of_row", "relative_index", "landing_gpu", "handled_slice", "slice_len",
-    "slice_of", "level2_order", "level2_batches", "bf16_to_f32", "rs_reduce", "ag_place", "rs_element",
-    "ag_element",
+    "slice_of", "level2_order", "level2_batches", "LANDING", "RELATIVE", "bf16_to_f32", "rs_reduce",
+    "ag_place", "rs_element", "ag_element",
 ]
 
 
@@ -157,31 +159,42 @@ def slice_of(x, S, L):
     return x // slice_len(S, L)
 
 
-def level2_batches(s, n_dest, M, L):
+LANDING = "landing"    # Reading R5: landing-GPU order within a batch
+RELATIVE = "relative"  # Reading R14: ascending relative index within a batch
+
+
+def level2_batches(s, n_dest, M, L, order=LANDING):
     """Source nodes of slice s in the order their partials are added, batch
-    by batch (Reading R5).
+    by batch (Reading R5; Reading R14 with ``order=RELATIVE``).
 
     Relative indices are taken in batches of L -- batch b holds c in
     [b*L, (b+1)*L) -- because one read-and-add sums at most one partial per
     destination GPU; with M <= L there is a single batch.  Within a batch the
     destination's GPUs are visited g = 0, 1, ..., L-1, GPU g holding the
-    partial of the batch's source whose slice s lands on it (none when c >= M).
+    partial of the batch's source whose slice s lands on it (none when c >= M);
+    or, in the RELATIVE reading, the batch's sources are taken by ascending c.
     """
+    if order not in (LANDING, RELATIVE):
+        raise ValueError(order)
     batches = []
     for b in range(-(-M // L)):
-        order = []
-        for g in range(L):
-            for n_src in range(M):
-                c = relative_index(n_dest, n_src, M)
-                if b * L <= c < (b + 1) * L and landing_gpu(s, c, L) == g:
-                    order.append(n_src)
-        batches.append(order)
+        batch = []
+        if order == LANDING:
+            for g in range(L):
+                for n_src in range(M):
+                    c = relative_index(n_dest, n_src, M)
+                    if b * L <= c < (b + 1) * L and landing_gpu(s, c, L) == g:
+                        batch.append(n_src)
+        else:
+            for c in range(b * L, min(M, (b + 1) * L)):
+                batch += [n_src for n_src in range(M) if relative_index(n_dest, n_src, M) == c]
+        batches.append(batch)
     return batches
 
 
-def level2_order(s, n_dest, M, L):
+def level2_order(s, n_dest, M, L, order=LANDING):
     """All source nodes of slice s in addition order (batches concatenated)."""
-    return [n for batch in level2_batches(s, n_dest, M, L) for n in batch]
+    return [n for batch in level2_batches(s, n_dest, M, L, order) for n in batch]
 
 
 # --------------------------------------------------------------------------
@@ -205,10 +218,11 @@ def _node_partial(grad_slice_of, n_src, L, count):
     return acc1
 
 
-def rs_reduce(geo, grads, M, L):
+def rs_reduce(geo, grads, M, L, order=LANDING):
     """Reduce-scatter of grads[rank][p] (uint16 bf16 bits, R_p*Kp row-major).
 
     Returns N float32 arrays of S elements: rank r's packed fp32 gradient shard.
+    ``order`` picks the level-2 reading (R5 or R14).
     """
     N = geo.N
     if N != M * L:
@@ -232,7 +246,7 @@ def rs_reduce(geo, grads, M, L):
                     return grads[src_rank][p][src0:src0 + count]
 
                 acc2 = np.zeros(b - a, dtype=np.float32)      # Reading R4
-                for batch in level2_batches(s, n_dest, M, L):  # level 2, Reading R5
+                for batch in level2_batches(s, n_dest, M, L, order):  # level 2, Reading R5
                     bsum = np.zeros(b - a, dtype=np.float32)
                     for n_src in batch:
                         bsum = bsum + _node_partial(grad_slice_of, n_src, L, b - a)
@@ -243,7 +257,7 @@ def rs_reduce(geo, grads, M, L):
     return shards
 
 
-def rs_element(geo, M, L, r, x, grad_at):
+def rs_element(geo, M, L, r, x, grad_at, order=LANDING):
     """One element of rank r's packed fp32 shard at position x, from scratch.
 
     ``grad_at(src_rank, p, idx)`` returns the bf16 bits of contributor
@@ -257,7 +271,7 @@ def rs_element(geo, M, L, r, x, grad_at):
     s = slice_of(x, geo.S, L)
     idx = np.array([r * geo.e[p] + e], dtype=np.int64)
     acc2 = np.float32(0.0)
-    for batch in level2_batches(s, r // L, M, L):
+    for batch in level2_batches(s, r // L, M, L, order):
         bsum = np.float32(0.0)
         for n_src in batch:
             acc1 = np.float32(0.0)
@@ -389,8 +403,9 @@ def rs_inbox(geo, grads, M, L):
     return inbox
 
 
-def rs_land(geo, inbox, M, L):
-    """Stage 2: each destination rank's shard from the landed partials."""
+def rs_land(geo, inbox, M, L, order=LANDING):
+    """Stage 2: each destination rank's shard from the landed partials
+    (landing GPUs in turn; with ``order=RELATIVE``, relative indices in turn)."""
     N, S = geo.N, geo.S
     B = slice_len(S, L)
     shards = []
@@ -404,9 +419,14 @@ def rs_land(geo, inbox, M, L):
             acc = np.zeros(hi - lo, dtype=np.float32)
             for b in range(-(-M // L)):                 # one read-and-add per batch of L sources
                 bsum = np.zeros(hi - lo, dtype=np.float32)
-                for g in range(L):
-                    c = b * L + (s - g) % L             # the batch's source whose slice s lands on GPU g
-                    if c < M:
+                if order == LANDING:
+                    for g in range(L):
+                        c = b * L + (s - g) % L             # the batch's source whose slice s lands on GPU g
+                        if c < M:
+                            bsum = bsum + inbox[n_dest, g, c, l_dest * B:l_dest * B + (hi - lo)]
+                else:
+                    for c in range(b * L, min(M, (b + 1) * L)):
+                        g = landing_gpu(s, c, L)            # where relative index c's slice s landed
                         bsum = bsum + inbox[n_dest, g, c, l_dest * B:l_dest * B + (hi - lo)]
                 acc = acc + bsum
             out[lo:hi] = acc

@@ -54,6 +54,8 @@ def _tiny_groups():
         ([(9, 5), (40, 3), (2, 2)], 3, 4),
         ([(16, 8)], 4, 4),
         ([(23, 3), (5, 5), (0, 4)], 2, 3),
+        ([(19, 5), (3, 7), (40,)], 4, 2),      # more nodes than GPUs per node
+        ([(31, 2), (6, 3)], 5, 2),
     ]
     return groups
 
@@ -181,9 +183,32 @@ def check_level2_batches_property():
                         assert len(set(gpus)) == len(gpus) and gpus == sorted(gpus)
 
 
+def check_relative_order_cases():
+    """The alternative level-2 reading: ascending relative index per batch."""
+    for case in _golden("level2_order_cases.json")["relative_order"]["cases"]:
+        for s, expect in enumerate(case["batches_by_slice"]):
+            assert O.level2_batches(s, case["n_dest"], case["M"], case["L"], O.RELATIVE) == expect
+    for L in range(1, 9):
+        for M in range(1, 3 * L + 2):
+            for n_dest in range(M):
+                for s in range(L):
+                    bs = O.level2_batches(s, n_dest, M, L, O.RELATIVE)
+                    assert [len(b) for b in bs] == [len(b) for b in O.level2_batches(s, n_dest, M, L)]
+                    cs = [O.relative_index(n_dest, n, M) for b in bs for n in b]
+                    assert cs == list(range(M))
+
+
+def check_relative_order_cancellation():
+    _check_cancellations(_golden("level2_order_cases.json")["relative_order"]["cancellations"], O.RELATIVE)
+
+
 def check_level2_order_cancellation():
     """Order-sensitive sums whose fp32 results were worked out by hand."""
-    for g in _golden("level2_order_cases.json")["cancellations"]:
+    _check_cancellations(_golden("level2_order_cases.json")["cancellations"], O.LANDING)
+
+
+def _check_cancellations(groups, order):
+    for g in groups:
         M, L = g["M"], g["L"]
         N = M * L
         R, K = g["shape"]
@@ -193,15 +218,17 @@ def check_level2_order_cancellation():
             bits = gen.f32_to_bf16_bits(np.full(K, v, dtype=np.float32))
             for row in g["planted_rows"]:
                 grads[n * L][0][row * K:(row + 1) * K] = bits
-        out = O.rs_reduce(geo, grads, M, L)
+        out = O.rs_reduce(geo, grads, M, L, order)
         for r in range(N):
             expect = np.array(g["expected_shard"].get(str(r), [g["other_ranks"]] * geo.S),
                               dtype=np.float32)
             assert np.array_equal(out[r], expect), (r, out[r], expect)
-        # the single-element form agrees
+        # the single-element form and the two-stage form agree
+        landed = O.rs_land(geo, O.rs_inbox(geo, grads, M, L), M, L, order)
         for r in range(N):
+            assert np.array_equal(landed[r], out[r]), r
             for x in range(geo.S):
-                val = O.rs_element(geo, M, L, r, x, lambda k, p, idx: grads[k][p][idx])
+                val = O.rs_element(geo, M, L, r, x, lambda k, p, idx: grads[k][p][idx], order)
                 assert val == out[r][x]
 
 
@@ -351,16 +378,18 @@ def check_staged_reduce_scatter_equals_fused():
                                                                           dtype=np.uint64), gen.OUTLIER)
                   for p, s in enumerate(shapes)] for r in range(N)]
         inbox = O.rs_inbox(geo, grads, M, L)
-        staged = O.rs_land(geo, inbox, M, L)
-        fused = O.rs_reduce(geo, grads, M, L)
-        for r in range(N):
-            assert np.array_equal(staged[r].view(np.uint32), fused[r].view(np.uint32)), r
-        # each (dest node, slice, source) partial occupies exactly one landing GPU
-        B = O.slice_len(geo.S, L)
+        for order in (O.LANDING, O.RELATIVE):
+            staged = O.rs_land(geo, inbox, M, L, order)
+            fused = O.rs_reduce(geo, grads, M, L, order)
+            for r in range(N):
+                assert np.array_equal(staged[r].view(np.uint32), fused[r].view(np.uint32)), (order, r)
+        # within a batch of L relative indices each partial of a slice lands on its own GPU
         for n_dest in range(M):
             for s in range(L):
-                gpus = [O.landing_gpu(s, O.relative_index(n_dest, n, M), L) for n in range(M)]
-                assert len(set(gpus)) == M
+                for b in range(-(-M // L)):
+                    cs = range(b * L, min(M, (b + 1) * L))
+                    gpus = [O.landing_gpu(s, c, L) for c in cs]
+                    assert len(set(gpus)) == len(cs)
 
 
 def check_average_and_accumulate():

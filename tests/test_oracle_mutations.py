@@ -28,8 +28,8 @@ MUTATIONS = {
     "source rank transposed": ("return grads[src_rank][p][src0:src0 + count]",
                                "return grads[(src_rank % L) * M + src_rank // L][p][src0:src0 + count]"),
     "bf16 widening shift": ("<< np.uint32(16)).view", "<< np.uint32(15)).view"),
-    "ascending node order": ("                    order.append(n_src)\n        batches.append(order)",
-                             "                    order.append(n_src)\n        batches.append(sorted(order))"),
+    "ascending node order": ("                        batch.append(n_src)\n        else:",
+                             "                        batch.append(n_src)\n            batch.sort()\n        else:"),
     "flat level 2 across batches": ("                    acc2 = acc2 + bsum\n                out[o_p + a:o_p + b] = acc2",
                                     "                    acc2 = bsum\n                out[o_p + a:o_p + b] = acc2"),
     "slice length floor": ("return -(-S // L) if S > 0 else 0", "return S // L if S > 0 else 0"),
@@ -51,6 +51,10 @@ MUTATIONS = {
     "stage slot rotated the wrong way": ("r = ((node + k) % M) * L + rail", "r = ((node - k) % M) * L + rail"),
     "landing stage adds a wrong source": ("c = b * L + (s - g) % L             # the batch's source",
                                           "c = b * L + (s + g) % L             # the batch's source"),
+    "relative order descending": ("            for c in range(b * L, min(M, (b + 1) * L)):\n                batch +=",
+                                  "            for c in reversed(range(b * L, min(M, (b + 1) * L))):\n                batch +="),
+    "relative landing stage reads the wrong GPU": ("g = landing_gpu(s, c, L)            # where relative index",
+                                                   "g = landing_gpu(s, c + 1, L)            # where relative index"),
     "average divides by M": ("x = (x / np.float32(geo.N)).astype(np.float32)",
                              "x = (x / np.float32(geo.N - 1 or 1)).astype(np.float32)"),
     "slot pack at op": ("slot[geo.N * geo.o[p]:geo.N * geo.o[p] + n] = grads[r][p][:n]",
