@@ -22,13 +22,15 @@ thread_local std::string g_last_error;
 bool mul_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_mul_overflow(a, b, out); }
 bool add_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_add_overflow(a, b, out); }
 
+}  // namespace
+
 // Level-2 order for slice s of destination node n_dest ("Reduce-scatter: two
 // levels of addition, the last one done by NVSwitch" in "The Endgame of FSDP
 // Communication"; the preprint's Figure 6(b)).  Slice s from the source with
 // relative index c = (n_dest - n_src) mod M lands on destination GPU
 // (s - c) mod L, so within batch b GPU g holds c = b*L + (s - g) mod L, if that
 // c is below M.  The partials are added in landing-GPU order g = 0..L-1, batch
-// after batch.
+// after batch; with TIDE_SUM_RELATIVE, by ascending c within each batch.
 void build_order_table(tide_plan* pl) {
   const int M = pl->M, L = pl->L;
   for (int n_dest = 0; n_dest < M; ++n_dest) {
@@ -37,14 +39,16 @@ void build_order_table(tide_plan* pl) {
       // With M > L the sources go in batches of L relative indices (one
       // read-and-add sums at most one partial per destination GPU).
       for (int b = 0; b * L < M; ++b) {
-        for (int g = 0; g < L; ++g) {
-          const int c = b * L + ((s - g) % L + L) % L;
+        for (int j = 0; j < L; ++j) {
+          const int c = pl->sum_order == TIDE_SUM_RELATIVE ? b * L + j : b * L + ((s - j) % L + L) % L;
           if (c < M) pl->order[(n_dest * L + s) * M + k++] = (uint8_t)(((n_dest - c) % M + M) % M);
         }
       }
     }
   }
 }
+
+namespace {
 
 void build_rs_items(tide_plan* pl) {
   const int64_t S = pl->S;

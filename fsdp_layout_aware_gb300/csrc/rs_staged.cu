@@ -12,7 +12,8 @@
 //
 // Stage 2, the landing CTAs (the NVSwitch read-and-add plus the CTAs that
 // accumulate into the shard): every destination element adds the partials of
-// its slice from landing GPUs g = 0..L-1 in turn and stores the sum.
+// its slice in the plan's level-2 order (by default landing GPUs g = 0..L-1
+// in turn), batch by batch when M > L, and stores the sum.
 //
 // The additions happen in the same order as in rs_fused, so the shards are
 // bit-identical; the price is 8*M extra bytes per shard element (every
@@ -113,57 +114,64 @@ __global__ void __launch_bounds__(kRsThreads, 4) rs_sum_kernel(const __grid_cons
   }
 }
 
-// Stage 2.  blockIdx.y is the destination rank.  For each slice, thread 0
-// lists where the slice's partials landed (landing GPUs g ascending) in
-// shared memory; the threads then stream the slice, four outputs each per
-// round, adding the partials in that order.  Keeping the list in shared
-// memory keeps the kernel at about 32 registers, so eight CTAs fit per SM.
-__global__ void __launch_bounds__(256, 8) rs_land_kernel(const float* __restrict__ inbox, float* const* shard_tab,
-                                                        int M, int L, int64_t S, int64_t B, int epi) {
+// Stage 2.  blockIdx.y is the destination rank.  For each slice, the first
+// M threads list where the slice's partials landed, in the plan's level-2
+// order, in shared memory; the threads then stream the slice, four outputs
+// each per round, adding the partials in that order.  Keeping the list in
+// shared memory keeps the kernel at 32 registers, so eight CTAs fit per SM
+// (five when M > L, where the batch sums take 48 registers).
+template <bool kBatched>
+__global__ void __launch_bounds__(256, kBatched ? 5 : 8) rs_land_kernel(const __grid_constant__ RsArgs a) {
   __shared__ const float* part[kMaxM];
-  __shared__ int n_part;
+  const int M = a.M, L = a.L;
+  const int64_t S = a.S, B = a.slice_len;
   const int r = blockIdx.y;
   const int n_dest = r / L, l_dest = r % L;
-  float* out = shard_tab[r];
+  float* out = a.shard_tab[r];
   const int64_t slot = (int64_t)L * B;
   const int64_t step = (int64_t)gridDim.x * blockDim.x * 4;
   for (int s = 0; s < L; ++s) {
     const int64_t lo = (int64_t)s * B, hi = min(S, lo + B);
     if (lo >= hi) break;
     __syncthreads();  // the previous slice's readers of part[] are done
-    if (threadIdx.x == 0) {
-      int k = 0;
-      for (int b = 0; b * L < M; ++b) {  // batches of L sources, each a read-and-add
-        for (int g = 0; g < L; ++g) {
-          const int c = b * L + ((s - g) % L + L) % L;  // the batch's source whose slice s landed on GPU g
-          if (c < M) part[k++] = inbox + ((int64_t)(n_dest * L + g) * M + c) * slot + (int64_t)l_dest * B - lo;
-        }
-      }
-      n_part = k;
+    if ((int)threadIdx.x < M) {
+      const int k = threadIdx.x;
+      const int node = a.order[(n_dest * L + s) * M + k];
+      const int c = ((n_dest - node) % M + M) % M;  // relative index of the k-th source
+      const int g = ((s - c) % L + L) % L;            // the GPU its slice s landed on
+      part[k] = a.inbox + ((int64_t)(n_dest * L + g) * M + c) * slot + (int64_t)l_dest * B - lo;
     }
     __syncthreads();
-    const int np = n_part;
+    const int np = M;
     for (int64_t x0 = lo + (int64_t)blockIdx.x * blockDim.x * 4 + threadIdx.x; x0 < hi; x0 += step) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f}, bsum[4] = {0.f, 0.f, 0.f, 0.f};
+      // With M <= L there is one batch and acc is its sum directly.
+      float acc[4] = {0.f, 0.f, 0.f, 0.f}, bsum[kBatched ? 4 : 1] = {0.f};
       for (int j = 0; j < np; ++j) {
         const float* pj = part[j];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int64_t x = x0 + (int64_t)u * blockDim.x;
-          if (x < hi) bsum[u] = __fadd_rn(bsum[u], __ldcs(pj + x));
+          if (x < hi) {
+            if constexpr (kBatched)
+              bsum[u] = __fadd_rn(bsum[u], __ldcs(pj + x));
+            else
+              acc[u] = __fadd_rn(acc[u], __ldcs(pj + x));
+          }
         }
-        if ((j + 1) % L == 0 || j + 1 == np) {  // end of a batch
+        if constexpr (kBatched) {
+          if ((j + 1) % L == 0 || j + 1 == np) {  // end of a batch
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            acc[u] = __fadd_rn(acc[u], bsum[u]);
-            bsum[u] = 0.f;
+            for (int u = 0; u < 4; ++u) {
+              acc[u] = __fadd_rn(acc[u], bsum[u]);
+              bsum[u] = 0.f;
+            }
           }
         }
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int64_t x = x0 + (int64_t)u * blockDim.x;
-        if (x < hi) __stcs(out + x, epilogue1(acc[u], out + x, epi, M * L));
+        if (x < hi) __stcs(out + x, epilogue1(acc[u], out + x, a.epilogue, M * L));
       }
     }
   }
@@ -191,8 +199,10 @@ int launch_rs_staged(const RsArgs& a, int sum_grid, int land_grid_x, void* strea
     case 8: err = launch_sum_t<8>(a, sum_grid, s); break;
   }
   if (err != cudaSuccess) return err;
-  rs_land_kernel<<<dim3(land_grid_x, a.N), 256, 0, s>>>(a.inbox, a.shard_tab, a.M, a.L, a.S, a.slice_len,
-                                                        a.epilogue);
+  if (a.M > a.L)
+    rs_land_kernel<true><<<dim3(land_grid_x, a.N), 256, 0, s>>>(a);
+  else
+    rs_land_kernel<false><<<dim3(land_grid_x, a.N), 256, 0, s>>>(a);
   return (int)cudaGetLastError();
 }
 

@@ -253,6 +253,12 @@ tide_status tide_plan_set_option(tide_plan* pl, int32_t option, int64_t value) {
       if (value != 0 && value != 1) return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_AG_UNPADDED must be 0 or 1");
       pl->ag_unpadded = value != 0;
       return TIDE_OK;
+    case TIDE_OPT_SUM_ORDER:
+      if (value != TIDE_SUM_LANDING && value != TIDE_SUM_RELATIVE)
+        return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_SUM_ORDER must be TIDE_SUM_LANDING or TIDE_SUM_RELATIVE");
+      pl->sum_order = (int32_t)value;
+      build_order_table(pl);  // read by every later call (passed by value at launch)
+      return TIDE_OK;
     case TIDE_OPT_TEST_DROP_TILE:
       if (value < -1) return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_TEST_DROP_TILE must be >= -1");
       pl->test_drop_tile = value;
@@ -389,7 +395,9 @@ tide_status tide_rs_staged(tide_plan* pl, const void* const* grads, float* const
   a.inbox = inbox;
   const int64_t sum_grid =
       sum_ctas_per_rank > 0 ? std::min<int64_t>((int64_t)sum_ctas_per_rank * pl->N, 1 << 20) : pl->rs_grid;
-  const int land_x = landing_ctas_per_rank > 0 ? landing_ctas_per_rank : std::max(1, pl->num_sms * 8 / pl->N);
+  const int land_per_sm = pl->M > pl->L ? 5 : 8;  // resident landing CTAs per SM (48 / 32 registers)
+  const int land_x =
+      landing_ctas_per_rank > 0 ? landing_ctas_per_rank : std::max(1, pl->num_sms * land_per_sm / pl->N);
   return finish(slot, launch_rs_staged(a, (int)sum_grid, land_x, stream), (cudaStream_t)stream, "rs_staged launch");
 }
 

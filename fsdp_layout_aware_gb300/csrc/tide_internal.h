@@ -174,6 +174,7 @@ struct tide_plan {
   uint64_t wait_limit_ns = 2000000000ull;  // 2 s
   int64_t test_drop_tile = -1;
   int32_t rs_epilogue = 0;                 // averaging / accumulate bits
+  int32_t sum_order = TIDE_SUM_LANDING;    // level-2 reading (order table)
   bool ag_unpadded = false;
   tide::RsItem* d_rs_items = nullptr;
   tide::AgItem* d_ag_items = nullptr;
@@ -212,4 +213,6 @@ std::vector<UnitStart> ag_unit_starts_of(const std::vector<AgItem>& items, int64
 // Thread-local error reporting (plan.cpp).
 tide_status fail(tide_status st, const std::string& msg);
 void clear_error();
+// Fills plan->order for the plan's sum_order (plan.cpp).
+void build_order_table(tide_plan* pl);
 }  // namespace tide

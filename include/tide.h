@@ -122,11 +122,12 @@ tide_status tide_plan_get_items(const tide_plan* plan, int32_t which, int64_t* o
 /* Level-2 summation order used by tide_rs_reduce for slice s (0 <= s < L)
  * of destination node n_dest (0 <= n_dest < M): writes the M source node
  * numbers, in the order their fp32 partials are added, to out[0..M) (batch
- * after batch when M > L: a batch ends after every L entries).  The
- * order is the Latin-square landing order of [Endgame] "Reduce-scatter: two
- * levels of addition, the last one done by NVSwitch" and [Abstract]
+ * after batch when M > L: a batch ends after every L entries).  By default
+ * the order is the Latin-square landing order of [Endgame] "Reduce-scatter:
+ * two levels of addition, the last one done by NVSwitch" and [Abstract]
  * Figure 6(b): destination GPU g = 0..L-1 holds the partial of the source
- * with relative index c = (s - g) mod L, if c < M.  Errors: INVALID_ARG. */
+ * with relative index c = (s - g) mod L, if c < M; TIDE_OPT_SUM_ORDER selects
+ * the other reading.  Errors: INVALID_ARG. */
 tide_status tide_plan_level2_order(const tide_plan* plan, int32_t n_dest, int32_t s, int32_t* out);
 
 /* Plan options, set before or between calls (never while a call of the
@@ -152,6 +153,8 @@ tide_status tide_plan_level2_order(const tide_plan* plan, int32_t n_dest, int32_
  *                          destination; accumulating follows "accumulate the
  *                          result straight into the fp32 gradient shard"
  *                          ([Endgame] "Reduce-scatter...").
+ *   TIDE_OPT_SUM_ORDER     the level-2 addition order (tide_sum_order,
+ *                          below); default TIDE_SUM_LANDING.
  *   TIDE_OPT_TEST_DROP_TILE  test hook: the bulk kernel's producer withholds
  *                          the given tile (counted per CTA from 0), so the
  *                          consumers' wait runs out; -1 (default) disables.
@@ -165,9 +168,22 @@ typedef enum tide_option {
   TIDE_OPT_RS_ACCUMULATE = 5,  /* 1: the result is added to the shard's
                                   previous value (one fp32 add, after the sum
                                   and the division) instead of overwriting */
-  TIDE_OPT_AG_UNPADDED = 6     /* 1: tide_ag_place writes only the R_p real
+  TIDE_OPT_AG_UNPADDED = 6,    /* 1: tide_ag_place writes only the R_p real
                                   rows; params[p] then needs R_p*Kp elements */
+  TIDE_OPT_SUM_ORDER = 7       /* level-2 addition order, a tide_sum_order */
 } tide_option;
+
+/* Orders for TIDE_OPT_SUM_ORDER.  The pages do not say in which order the
+ * NVSwitch read-and-add combines the partials ([Endgame] "Reduce-scatter:
+ * two levels of addition..."), so two readings are offered; both keep the
+ * batches of L relative indices, and both are exact and deterministic.
+ *   TIDE_SUM_LANDING   (default) by the destination GPU g = 0..L-1 the
+ *                      partial lands on, as described under tide_rs_reduce;
+ *   TIDE_SUM_RELATIVE  by ascending relative index c = (n_d - n) mod M
+ *                      (the same for every slice).
+ * Applies to every reduce-scatter entry point; tide_plan_level2_order
+ * reports the order in force. */
+typedef enum tide_sum_order { TIDE_SUM_LANDING = 0, TIDE_SUM_RELATIVE = 1 } tide_sum_order;
 tide_status tide_plan_set_option(tide_plan* plan, int32_t option, int64_t value);
 
 /* Synchronise the device the plan runs on and report whether any of the

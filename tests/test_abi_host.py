@@ -131,6 +131,12 @@ def test_all_level2_orders_small_groups():
                 for n_dest in range(M):
                     for s in range(L):
                         assert plan.level2_order(n_dest, s) == O.level2_order(s, n_dest, M, L)
+                plan.set_option(tide.TIDE_OPT_SUM_ORDER, tide.TIDE_SUM_RELATIVE)
+                for n_dest in range(M):
+                    for s in range(L):
+                        assert plan.level2_order(n_dest, s) == O.level2_order(s, n_dest, M, L, O.RELATIVE)
+                plan.set_option(tide.TIDE_OPT_SUM_ORDER, tide.TIDE_SUM_LANDING)
+                assert plan.level2_order(0, L - 1) == O.level2_order(L - 1, 0, M, L)
 
 
 @pytest.mark.parametrize("shapes,N,M,L,status", [
@@ -197,7 +203,7 @@ def test_plan_options_validate_without_a_gpu():
         plan.set_option(tide.TIDE_OPT_TEST_DROP_TILE, -1)
         plan.check()   # never ran on a device: nothing to report
         for opt, val in [(tide.TIDE_OPT_RS_KERNEL, 2), (tide.TIDE_OPT_WAIT_LIMIT_NS, 0),
-                         (tide.TIDE_OPT_TEST_DROP_TILE, -2), (99, 0)]:
+                         (tide.TIDE_OPT_TEST_DROP_TILE, -2), (tide.TIDE_OPT_SUM_ORDER, 2), (99, 0)]:
             with pytest.raises(tide.TideError) as err:
                 plan.set_option(opt, val)
             assert err.value.status == 1

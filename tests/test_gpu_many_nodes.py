@@ -1,4 +1,5 @@
-"""GPU parity with more nodes than GPUs per node (M > L).
+"""GPU parity with more nodes than GPUs per node (M > L), and of the
+alternative level-2 reading (ascending relative index).
 
 The level-2 sum then runs in batches of L source nodes, one read-and-add per
 batch, and the batch sums are added in ascending batch order ("Reduce-scatter:
@@ -126,6 +127,59 @@ def test_rs_many_nodes_bit_exact(w, kernel, oracle_cache):
             plan.rs_reduce(flat, shards)
         plan.check()
         _assert_equal(w, outs, expect)
+
+
+ORDER_CASES = [
+    configs.Workload("ragged_3x4", 12, 3, 4, [(5, 3), (1,), (7, 2, 2), (), (13, 5), (100, 33), (1031, 257)],
+                     [gen.NORMAL if p % 2 else gen.OUTLIER for p in range(7)], sigma=1e-3, seed=406),
+    configs.scaled(configs.get(4), row_div=1024, name="wan22dit_rows/1024"),
+    CASES[1], CASES[3],   # (with L = 2 the two readings coincide: a batch of two adds a + b either way)
+]
+
+
+def _relative(w, cache):
+    key = ("relative", w.name)
+    if key not in cache:
+        grads, geo, landing = _inputs(w, cache)
+        cache[key] = O.rs_reduce(geo, grads, w.M, w.L, O.RELATIVE)
+    return cache[key]
+
+
+@pytest.mark.parametrize("w", ORDER_CASES, ids=lambda w: w.name)
+@pytest.mark.parametrize("kernel", ["fused", "staged", "noalloc", "bulk"])
+def test_rs_relative_order_bit_exact(w, kernel, oracle_cache):
+    """TIDE_OPT_SUM_ORDER = TIDE_SUM_RELATIVE: every kernel follows the
+    ascending-relative-index reading bit for bit, and the cases are ones where
+    the two readings give different bits."""
+    grads, geo, landing = _inputs(w, oracle_cache)
+    expect = _relative(w, oracle_cache)
+    assert any(not np.array_equal(expect[r].view(np.uint32), landing[r].view(np.uint32)) for r in range(w.N))
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        plan.set_option(tide.TIDE_OPT_SUM_ORDER, tide.TIDE_SUM_RELATIVE)
+        flat = _flat_list(w, _device(w, grads))
+        outs = [f32_guarded(geo.S, GUARD, GUARD) for _ in range(w.N)]
+        shards = [o[0] for o in outs]
+        if kernel == "bulk":
+            if w.M > 8:
+                pytest.skip("the bulk kernel takes at most 8 nodes")
+            plan.set_option(tide.TIDE_OPT_RS_KERNEL, 1)
+            plan.rs_reduce(flat, shards)
+        elif kernel == "staged":
+            inbox = torch.full((tide.tide_plan_inbox_elems(plan.handle),), float("nan"), dtype=torch.float32,
+                               device=DEV)
+            tide.tide_rs_staged(plan.handle, flat, shards, inbox)
+        elif kernel == "noalloc":
+            tide.tide_rs_reduce_noalloc(plan.handle, flat, shards)
+        else:
+            plan.rs_reduce(flat, shards)
+        plan.check()
+        _assert_equal(w, outs, expect)
+        # switching back restores the default reading on the same plan
+        plan.set_option(tide.TIDE_OPT_SUM_ORDER, tide.TIDE_SUM_LANDING)
+        if kernel == "fused":
+            plan.rs_reduce(flat, shards)
+            plan.check()
+            _assert_equal(w, outs, landing)
 
 
 @pytest.mark.parametrize("w", [CASES[0], CASES[3]], ids=lambda w: w.name)
