@@ -64,7 +64,8 @@ def _flat(w, grads, monkeypatch):
     missed the batch boundaries would produce."""
     orig = O.level2_batches
     with monkeypatch.context() as m:
-        m.setattr(O, "level2_batches", lambda s, n, M, L: [[x for b in orig(s, n, M, L) for x in b]])
+        m.setattr(O, "level2_batches",
+                  lambda s, n, M, L, order=O.LANDING: [[x for b in orig(s, n, M, L, order) for x in b]])
         return O.rs_reduce(O.geometry(w.shapes, w.N), grads, w.M, w.L)
 
 
