@@ -25,6 +25,17 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 v) {
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
+// Next work item from the launch's shared counter.  Every CTA keeps taking
+// items until it draws an index >= n_items, so a launch of G CTAs draws
+// exactly n_items + G values; the CTA that draws the last one knows that no
+// other draw follows and sets the counter back to zero, ready for the next
+// launch that reads the same pointer table.
+__device__ __forceinline__ long long take_item(unsigned long long* counter, int64_t n_items) {
+  const unsigned long long v = atomicAdd(counter, 1ull);
+  if (v == (unsigned long long)n_items + gridDim.x - 1) atomicExch(counter, 0ull);
+  return (long long)v;
+}
+
 // Padding rows of a destination piece: +0.0 everywhere.
 __device__ __forceinline__ void zero_fill(float* dst, int n) {
   const int head = min(n, (int)(((16 - ((uintptr_t)dst & 15)) & 15) >> 2));

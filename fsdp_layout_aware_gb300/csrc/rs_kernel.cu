@@ -139,14 +139,12 @@ __global__ void __launch_bounds__(kRsThreads, 4) rs_fused_kernel(const __grid_co
   __shared__ const uint16_t* src[kMaxN];
   __shared__ long long next_item[2];
   unsigned long long* counter = a.counter;
-  if (threadIdx.x == 0)
-    next_item[0] = counter ? (long long)atomicAdd(counter, 1ull) : (long long)blockIdx.x;
+  if (threadIdx.x == 0) next_item[0] = counter ? take_item(counter, a.n_items) : (long long)blockIdx.x;
   __syncthreads();
   int slot = 0;
   for (int64_t it = next_item[0]; it < a.n_items; it = next_item[slot]) {
     slot ^= 1;
-    if (threadIdx.x == 0)
-      next_item[slot] = counter ? (long long)atomicAdd(counter, 1ull) : (long long)(it + gridDim.x);
+    if (threadIdx.x == 0) next_item[slot] = counter ? take_item(counter, a.n_items) : (long long)(it + gridDim.x);
     const RsItem item = a.items[it];
     float* dst = a.shard_tab[item.r] + item.dst_off;
     if (item.kind == RS_PAD) {

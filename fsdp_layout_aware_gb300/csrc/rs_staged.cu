@@ -90,12 +90,12 @@ template <int L>
 __global__ void __launch_bounds__(kRsThreads, 4) rs_sum_kernel(const __grid_constant__ RsArgs a) {
   __shared__ const uint16_t* src[kMaxN];
   __shared__ long long next_item[2];
-  if (threadIdx.x == 0) next_item[0] = (long long)atomicAdd(a.counter, 1ull);
+  if (threadIdx.x == 0) next_item[0] = take_item(a.counter, a.n_items);
   __syncthreads();
   int slot = 0;
   for (int64_t it = next_item[0]; it < a.n_items; it = next_item[slot]) {
     slot ^= 1;
-    if (threadIdx.x == 0) next_item[slot] = (long long)atomicAdd(a.counter, 1ull);
+    if (threadIdx.x == 0) next_item[slot] = take_item(a.counter, a.n_items);
     const RsItem item = a.items[it];
     if (item.kind == RS_PAD) {
       // padding rows: every source's partial is +0.0

@@ -45,6 +45,7 @@ void release_device_state(tide_plan* pl) {
     if (s.dev) cudaFree(s.dev);
     s = tide_plan::Slot();
   }
+  for (int k = 0; k < tide_plan::kTableKinds; ++k) pl->cached_slot[k] = -1;
   if (pl->d_rs_items) cudaFree(pl->d_rs_items);
   if (pl->d_ag_items) cudaFree(pl->d_ag_items);
   if (pl->d_ag_units) cudaFree(pl->d_ag_units);
@@ -103,6 +104,7 @@ tide_status ensure_device(tide_plan* pl) {
       return bail(err, "cudaMemcpy(ag items)");
   }
   pl->slot_bytes = align_up(std::max(rs_table_bytes(pl), ag_table_bytes(pl)), 256);
+  pl->table_scratch.assign(pl->slot_bytes, 0);
   for (auto& s : pl->ring) {
     if ((err = cudaHostAlloc((void**)&s.host, pl->slot_bytes, cudaHostAllocDefault)) != cudaSuccess)
       return bail(err, "cudaHostAlloc(pointer ring)");
@@ -202,8 +204,49 @@ tide_status acquire_slot(tide_plan* pl, tide_plan::Slot** out) {
   return TIDE_OK;
 }
 
-tide_status upload_and_mark(tide_plan::Slot* s, size_t bytes, cudaStream_t stream) {
+enum TableKind { TABLE_RS = 0, TABLE_AG = 1, TABLE_PACK = 2, TABLE_STAGE = 3 };
+
+// Puts the pointer table just built in pl->table_scratch (its first `bytes`)
+// on the device.  If the previous table of this kind is byte-for-byte the
+// same, its slot has not taken other content since, and its last use was on
+// this stream (stream order) or has finished, that device copy is used as it
+// is: persistent buffers cost no upload per call.  Otherwise the next ring
+// slot is taken (waiting for its last use) and the table uploaded.  A reused
+// RS table is valid because the kernels leave their work counter at zero.
+tide_status commit_table(tide_plan* pl, TableKind kind, size_t bytes, cudaStream_t stream, tide_plan::Slot** out) {
+  const unsigned char* tab = pl->table_scratch.data();
+  const int c = pl->cached_slot[kind];
+  if (c >= 0) {
+    tide_plan::Slot& s = pl->ring[c];
+    if (s.gen == pl->cached_gen[kind] && s.bytes == bytes && std::memcmp(s.host, tab, bytes) == 0) {
+      bool usable = !s.in_flight || s.stream == (void*)stream;
+      if (!usable) {
+        const cudaError_t q = cudaEventQuery((cudaEvent_t)s.done);
+        if (q == cudaSuccess) {
+          s.in_flight = false;
+          usable = true;
+        } else if (q != cudaErrorNotReady) {
+          return cuda_fail(q, "cudaEventQuery(pointer-table slot)");
+        }
+      }
+      if (usable) {
+        s.stream = (void*)stream;
+        *out = &s;
+        return TIDE_OK;
+      }
+    }
+  }
+  tide_plan::Slot* s = nullptr;
+  tide_status st = acquire_slot(pl, &s);
+  if (st != TIDE_OK) return st;
+  std::memcpy(s->host, tab, bytes);
   TIDE_CUDA(cudaMemcpyAsync(s->dev, s->host, bytes, cudaMemcpyHostToDevice, stream), "pointer-table upload");
+  s->gen = ++pl->next_gen;
+  s->bytes = bytes;
+  s->stream = (void*)stream;
+  pl->cached_slot[kind] = (int)(s - pl->ring);
+  pl->cached_gen[kind] = s->gen;
+  *out = s;
   return TIDE_OK;
 }
 
@@ -308,14 +351,15 @@ tide_status prepare_rs(tide_plan* pl, const void* const* grads, float* const* sh
   tide_status st = ensure_device(pl);
   if (st != TIDE_OK) return st;
   tide_plan::Slot* slot = nullptr;
-  if ((st = acquire_slot(pl, &slot)) != TIDE_OK) return st;
 
   // Pointer table: [P][N] gradients, [N] shards, [P] phase flags, work counter.
+  unsigned char* tab = pl->table_scratch.data();
   const size_t n_grad = (size_t)pl->P * pl->N;
-  const uint16_t** gtab = (const uint16_t**)slot->host;
-  float** stab = (float**)(slot->host + n_grad * 8);
+  const uint16_t** gtab = (const uint16_t**)tab;
+  float** stab = (float**)(tab + n_grad * 8);
   const size_t flags_at = align_up(n_grad * 8 + (size_t)pl->N * 8, 16);
-  uint8_t* flags = slot->host + flags_at;
+  uint8_t* flags = tab + flags_at;
+  std::memset(tab + n_grad * 8 + (size_t)pl->N * 8, 0, flags_at - (n_grad * 8 + (size_t)pl->N * 8));
   for (int32_t p = 0; p < pl->P; ++p) {
     const uintptr_t phase0 = (uintptr_t)grads[p] & 15;
     uint8_t uniform = 1;
@@ -328,9 +372,9 @@ tide_status prepare_rs(tide_plan* pl, const void* const* grads, float* const* sh
   }
   for (int32_t r = 0; r < pl->N; ++r) stab[r] = shards[r];
   const size_t counter_at = flags_at + align_up((size_t)pl->P, 16);
-  *(unsigned long long*)(slot->host + counter_at) = 0;  // the kernels' work counter starts at item 0
+  std::memset(flags + pl->P, 0, counter_at + 8 - (flags_at + pl->P));  // pad bytes; work counter = 0
   const size_t bytes = counter_at + 8;
-  if ((st = upload_and_mark(slot, bytes, (cudaStream_t)stream)) != TIDE_OK) return st;
+  if ((st = commit_table(pl, TABLE_RS, bytes, (cudaStream_t)stream, &slot)) != TIDE_OK) return st;
 
   a->items = pl->d_rs_items;
   a->n_items = (int64_t)pl->rs_items.size();
@@ -420,13 +464,12 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
   tide_status st = ensure_device(pl);
   if (st != TIDE_OK) return st;
   tide_plan::Slot* slot = nullptr;
-  if ((st = acquire_slot(pl, &slot)) != TIDE_OK) return st;
-  const void** stab = (const void**)slot->host;
-  void** ptab = (void**)(slot->host + (size_t)pl->N * 8);
+  const void** stab = (const void**)pl->table_scratch.data();
+  void** ptab = (void**)(pl->table_scratch.data() + (size_t)pl->N * 8);
   for (int32_t r = 0; r < pl->N; ++r) stab[r] = shards[r];
   for (int32_t p = 0; p < pl->P; ++p) ptab[p] = params[p];
   cudaStream_t s = (cudaStream_t)stream;
-  if ((st = upload_and_mark(slot, ag_table_bytes(pl), s)) != TIDE_OK) return st;
+  if ((st = commit_table(pl, TABLE_AG, ag_table_bytes(pl), s, &slot)) != TIDE_OK) return st;
 
   AgArgs a;
   if (pl->ag_unpadded) {
@@ -464,14 +507,13 @@ tide_status tide_slot_pack(tide_plan* pl, const void* const* grads, void* const*
   tide_status st = ensure_device(pl);
   if (st != TIDE_OK) return st;
   tide_plan::Slot* slot = nullptr;
-  if ((st = acquire_slot(pl, &slot)) != TIDE_OK) return st;
   const size_t n_grad = (size_t)pl->N * pl->P;
-  const void** gtab = (const void**)slot->host;  // indexed by r*P + p
-  void** stab = (void**)(slot->host + n_grad * 8);
+  const void** gtab = (const void**)pl->table_scratch.data();  // indexed by r*P + p
+  void** stab = (void**)(pl->table_scratch.data() + n_grad * 8);
   for (size_t i = 0; i < n_grad; ++i) gtab[i] = grads[i];
   for (int32_t r = 0; r < pl->N; ++r) stab[r] = slots[r];
   cudaStream_t s = (cudaStream_t)stream;
-  if ((st = upload_and_mark(slot, (n_grad + (size_t)pl->N) * 8, s)) != TIDE_OK) return st;
+  if ((st = commit_table(pl, TABLE_PACK, (n_grad + (size_t)pl->N) * 8, s, &slot)) != TIDE_OK) return st;
   AgArgs a;
   a.items = pl->d_pack_items;
   a.n_items = (int64_t)pl->pack_items.size();
@@ -539,10 +581,9 @@ tide_status tide_ag_stage_place(tide_plan* pl, const void* stage, int32_t node, 
   if (st != TIDE_OK) return st;
   if (pl->rail_n_items[rail] == 0) return TIDE_OK;
   tide_plan::Slot* slot = nullptr;
-  if ((st = acquire_slot(pl, &slot)) != TIDE_OK) return st;
   // Shard table indexed by rank: rank ((node + k) mod M) * L + rail reads slot k.
-  const unsigned char** stab = (const unsigned char**)slot->host;
-  void** ptab = (void**)(slot->host + (size_t)pl->N * 8);
+  const unsigned char** stab = (const unsigned char**)pl->table_scratch.data();
+  void** ptab = (void**)(pl->table_scratch.data() + (size_t)pl->N * 8);
   for (int32_t r = 0; r < pl->N; ++r) stab[r] = nullptr;
   for (int32_t k = 0; k < pl->M; ++k) {
     const int32_t r = ((node + k) % pl->M) * pl->L + rail;
@@ -550,7 +591,7 @@ tide_status tide_ag_stage_place(tide_plan* pl, const void* stage, int32_t node, 
   }
   for (int32_t p = 0; p < pl->P; ++p) ptab[p] = params[p];
   cudaStream_t s = (cudaStream_t)stream;
-  if ((st = upload_and_mark(slot, ag_table_bytes(pl), s)) != TIDE_OK) return st;
+  if ((st = commit_table(pl, TABLE_STAGE, ag_table_bytes(pl), s, &slot)) != TIDE_OK) return st;
   AgArgs a;
   a.items = pl->d_rail_items[rail];
   a.n_items = pl->rail_n_items[rail];

@@ -114,7 +114,8 @@ struct BulkLayout {
 struct RsArgs {
   const RsItem* items;
   int64_t n_items;
-  unsigned long long* counter;      // next item to take (zero at launch); NULL: round-robin
+  unsigned long long* counter;      // next item to take: zero at launch, and the kernel leaves it
+                                    // zero (see take_item); NULL: round-robin
   const uint16_t* const* grad_tab;  // [P][N]: contributor src's gradient of p
   float* const* shard_tab;          // [N]
   const uint8_t* uniform_phase;     // [P]: 1 if all N gradients of p share addr mod 16
@@ -199,9 +200,19 @@ struct tide_plan {
     unsigned char* dev = nullptr;
     void* done = nullptr;   // cudaEvent_t
     bool in_flight = false;
+    uint64_t gen = 0;        // bumped whenever the slot takes new content
+    size_t bytes = 0;        // bytes of the last upload (host copy == device copy)
+    void* stream = nullptr;  // stream of the slot's last use
   } ring[kRing];
   int next_slot = 0;
   size_t slot_bytes = 0;
+  // Pointer tables are built in table_scratch; a call whose table equals the
+  // previous one of its kind reuses that slot's device copy (no upload).
+  static constexpr int kTableKinds = 4;  // RS, AG, Slot-Reuse pack, stage placement
+  std::vector<unsigned char> table_scratch;
+  int cached_slot[kTableKinds] = {-1, -1, -1, -1};
+  uint64_t cached_gen[kTableKinds] = {};
+  uint64_t next_gen = 0;
 };
 
 namespace tide {
