@@ -116,9 +116,10 @@ tide_status ensure_device(tide_plan* pl) {
   }
   if ((err = cudaMalloc(&pl->d_status, sizeof(int))) != cudaSuccess) return bail(err, "cudaMalloc(status)");
   if ((err = cudaMemset(pl->d_status, 0, sizeof(int))) != cudaSuccess) return bail(err, "cudaMemset(status)");
-  {
-    // Bulk-copy pipeline: one CTA per SM with as many stages as the opt-in
-    // shared memory allows (a little is left for the static allocations).
+  if (pl->M <= 8) {
+    // Bulk-copy pipeline (M <= 8 only): one CTA per SM with as many stages as
+    // the opt-in shared memory allows (a little is left for the static
+    // allocations).
     int optin = 0;
     if ((err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
       return bail(err, "cudaDeviceGetAttribute(smem)");
