@@ -46,6 +46,12 @@ void release_device_state(tide_plan* pl) {
     s = tide_plan::Slot();
   }
   for (int k = 0; k < tide_plan::kTableKinds; ++k) pl->cached_slot[k] = -1;
+  for (auto& s : pl->captured) {
+    if (s.host) cudaFreeHost(s.host);
+    if (s.dev) cudaFree(s.dev);
+    s = tide_plan::Slot();
+  }
+  pl->n_captured = 0;
   if (pl->d_rs_items) cudaFree(pl->d_rs_items);
   if (pl->d_ag_items) cudaFree(pl->d_ag_items);
   if (pl->d_ag_units) cudaFree(pl->d_ag_units);
@@ -113,6 +119,13 @@ tide_status ensure_device(tide_plan* pl) {
     if ((err = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess)
       return bail(err, "cudaEventCreate");
     s.done = ev;
+  }
+  for (auto& s : pl->captured) {
+    if ((err = cudaHostAlloc((void**)&s.host, pl->slot_bytes, cudaHostAllocDefault)) != cudaSuccess)
+      return bail(err, "cudaHostAlloc(captured tables)");
+    if ((err = cudaMalloc((void**)&s.dev, pl->slot_bytes)) != cudaSuccess)
+      return bail(err, "cudaMalloc(captured tables)");
+    s.fixed = true;
   }
   if ((err = cudaMalloc(&pl->d_status, sizeof(int))) != cudaSuccess) return bail(err, "cudaMalloc(status)");
   if ((err = cudaMemset(pl->d_status, 0, sizeof(int))) != cudaSuccess) return bail(err, "cudaMemset(status)");
@@ -216,6 +229,22 @@ enum TableKind { TABLE_RS = 0, TABLE_AG = 1, TABLE_PACK = 2, TABLE_STAGE = 3 };
 // RS table is valid because the kernels leave their work counter at zero.
 tide_status commit_table(tide_plan* pl, TableKind kind, size_t bytes, cudaStream_t stream, tide_plan::Slot** out) {
   const unsigned char* tab = pl->table_scratch.data();
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  TIDE_CUDA(cudaStreamIsCapturing(stream, &cap), "cudaStreamIsCapturing");
+  if (cap != cudaStreamCaptureStatusNone) {
+    // Graph capture: no event queries or waits (not capturable); the table
+    // goes to a slot of its own and the upload becomes a node of the graph.
+    if (cap != cudaStreamCaptureStatusActive) return fail(TIDE_ERR_CUDA, "stream capture was invalidated");
+    if (pl->n_captured == tide_plan::kCaptureSlots)
+      return fail(TIDE_ERR_INVALID_ARG, "more than " + std::to_string(tide_plan::kCaptureSlots) +
+                                            " calls of this plan captured into CUDA graphs");
+    tide_plan::Slot* s = &pl->captured[pl->n_captured++];
+    std::memcpy(s->host, tab, bytes);
+    TIDE_CUDA(cudaMemcpyAsync(s->dev, s->host, bytes, cudaMemcpyHostToDevice, stream), "pointer-table upload");
+    s->bytes = bytes;
+    *out = s;
+    return TIDE_OK;
+  }
   const int c = pl->cached_slot[kind];
   if (c >= 0) {
     tide_plan::Slot& s = pl->ring[c];
@@ -253,6 +282,7 @@ tide_status commit_table(tide_plan* pl, TableKind kind, size_t bytes, cudaStream
 
 tide_status finish(tide_plan::Slot* s, int launch_err, cudaStream_t stream, const char* what) {
   if (launch_err != cudaSuccess) return cuda_fail((cudaError_t)launch_err, what);
+  if (s->fixed) return TIDE_OK;  // captured: the slot is never recycled
   TIDE_CUDA(cudaEventRecord((cudaEvent_t)s->done, stream), "cudaEventRecord");
   s->in_flight = true;
   return TIDE_OK;

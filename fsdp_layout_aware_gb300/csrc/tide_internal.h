@@ -203,7 +203,14 @@ struct tide_plan {
     uint64_t gen = 0;        // bumped whenever the slot takes new content
     size_t bytes = 0;        // bytes of the last upload (host copy == device copy)
     void* stream = nullptr;  // stream of the slot's last use
+    bool fixed = false;      // a captured call's table: never rewritten
   } ring[kRing];
+  // Tables of calls made while their stream was being captured into a CUDA
+  // graph: each keeps its slot until the plan is destroyed, so every replay
+  // of the graph reads (and re-uploads) exactly the table of the capture.
+  static constexpr int kCaptureSlots = 8;
+  Slot captured[kCaptureSlots];
+  int n_captured = 0;
   int next_slot = 0;
   size_t slot_bytes = 0;
   // Pointer tables are built in table_scratch; a call whose table equals the

@@ -38,8 +38,19 @@
  *   - A plan may be used from one host thread at a time.  Its device state
  *     (work lists, pointer-table ring) is created on the device current at
  *     the first compute call and that device only; the first compute call
- *     therefore allocates and synchronises, and should come before any CUDA
+ *     therefore allocates and synchronises, and must come before any CUDA
  *     graph capture.  Later calls are stream-ordered and never allocate.
+ *   - Each call passes its pointer arrays to the kernels through a device
+ *     table.  A call whose table equals the previous one of the same kind
+ *     reuses it (no upload), so unchanged buffers cost no host-to-device
+ *     copy per call.
+ *   - CUDA graphs: a call made while `stream` is being captured takes one of
+ *     8 table slots reserved per plan and keeps it until tide_plan_destroy;
+ *     every replay re-uploads that fixed table, so it uses the pointers
+ *     given at capture (the data behind them may change between replays).
+ *     A ninth captured call returns TIDE_ERR_INVALID_ARG.  The plan must
+ *     outlive its graphs.  tide_rs_reduce_noalloc cannot be captured (it
+ *     copies from pageable memory).
  *   - Outputs must not overlap inputs or each other.
  */
 #ifndef TIDE_H
