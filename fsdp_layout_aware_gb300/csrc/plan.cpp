@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <iterator>
 #include <new>
 
 #include "tide_internal.h"
@@ -46,6 +47,27 @@ void build_order_table(tide_plan* pl) {
       }
     }
   }
+}
+
+tide_status check_overlap(const std::vector<ByteRange>& inputs, std::vector<ByteRange> outputs) {
+  auto describe = [](const ByteRange& r) { return std::string(r.what) + "[" + std::to_string(r.index) + "]"; };
+  outputs.erase(std::remove_if(outputs.begin(), outputs.end(), [](const ByteRange& r) { return r.hi <= r.lo; }),
+                outputs.end());
+  std::sort(outputs.begin(), outputs.end(), [](const ByteRange& a, const ByteRange& b) { return a.lo < b.lo; });
+  for (size_t i = 1; i < outputs.size(); ++i)
+    if (outputs[i].lo < outputs[i - 1].hi)
+      return fail(TIDE_ERR_INVALID_ARG, "outputs " + describe(outputs[i - 1]) + " and " + describe(outputs[i]) +
+                                            " overlap");
+  for (const ByteRange& in : inputs) {
+    if (in.hi <= in.lo) continue;
+    // Outputs are sorted and disjoint: only the last one starting before
+    // in.hi can reach into [in.lo, in.hi).
+    auto it = std::lower_bound(outputs.begin(), outputs.end(), in.hi,
+                               [](const ByteRange& o, uintptr_t v) { return o.lo < v; });
+    if (it != outputs.begin() && std::prev(it)->hi > in.lo)
+      return fail(TIDE_ERR_INVALID_ARG, "output " + describe(*std::prev(it)) + " overlaps input " + describe(in));
+  }
+  return TIDE_OK;
 }
 
 namespace {

@@ -92,6 +92,18 @@ extern "C" tide_status tide_rs_reduce_noalloc(const tide_plan* pl, const void* c
       if ((uintptr_t)g & 1) return fail(TIDE_ERR_ALIGNMENT, "gradient pointer not 2-byte aligned");
     }
   }
+  if (pl->check_overlap) {
+    std::vector<ByteRange> in, out;
+    for (int32_t r = 0; r < pl->N; ++r) {
+      for (int32_t p = 0; p < pl->P; ++p) {
+        const uintptr_t g = (uintptr_t)grads[(size_t)r * pl->P + p];
+        in.push_back({g, g + (uintptr_t)(2 * pl->rows[p] * pl->Kp[p]), "grads", (int64_t)r * pl->P + p});
+      }
+      out.push_back({(uintptr_t)shards[r], (uintptr_t)(shards[r] + pl->S), "shards", r});
+    }
+    const tide_status st = check_overlap(in, out);
+    if (st != TIDE_OK) return st;
+  }
 
   // Scratch layout: items | caller's [r][p] pointers | [p][r] table | shards | flags.
   const size_t n_ptr = (size_t)pl->N * pl->P;

@@ -333,6 +333,10 @@ tide_status tide_plan_set_option(tide_plan* pl, int32_t option, int64_t value) {
       pl->sum_order = (int32_t)value;
       build_order_table(pl);  // read by every later call (passed by value at launch)
       return TIDE_OK;
+    case TIDE_OPT_CHECK_OVERLAP:
+      if (value != 0 && value != 1) return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_CHECK_OVERLAP must be 0 or 1");
+      pl->check_overlap = value != 0;
+      return TIDE_OK;
     case TIDE_OPT_TEST_DROP_TILE:
       if (value < -1) return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_TEST_DROP_TILE must be >= -1");
       pl->test_drop_tile = value;
@@ -364,8 +368,26 @@ tide_status tide_plan_check(tide_plan* pl) {
 namespace {
 // Validate a reduce-scatter call, set up the device on first use, fill and
 // upload the call's pointer table, and return the kernel arguments.
+// Byte ranges for TIDE_OPT_CHECK_OVERLAP.
+void add_grad_ranges(const tide_plan* pl, const void* const* grads, std::vector<ByteRange>* v) {
+  for (int32_t r = 0; r < pl->N; ++r)
+    for (int32_t p = 0; p < pl->P; ++p) {
+      const uintptr_t g = (uintptr_t)grads[(size_t)r * pl->P + p];
+      v->push_back({g, g + (uintptr_t)(2 * pl->rows[p] * pl->Kp[p]), "grads", (int64_t)r * pl->P + p});
+    }
+}
+void add_ranges(const void* const* ptrs, int32_t n, size_t bytes, const char* what, std::vector<ByteRange>* v) {
+  for (int32_t i = 0; i < n; ++i) v->push_back({(uintptr_t)ptrs[i], (uintptr_t)ptrs[i] + bytes, what, i});
+}
+void add_param_ranges(const tide_plan* pl, void* const* params, int32_t eb, bool unpadded, std::vector<ByteRange>* v) {
+  for (int32_t p = 0; p < pl->P; ++p) {
+    const int64_t n = unpadded ? pl->rows[p] * pl->Kp[p] : (int64_t)pl->N * pl->e[p];
+    v->push_back({(uintptr_t)params[p], (uintptr_t)params[p] + (uintptr_t)(n * eb), "params", p});
+  }
+}
+
 tide_status prepare_rs(tide_plan* pl, const void* const* grads, float* const* shards, void* stream, RsArgs* a,
-                       tide_plan::Slot** out_slot) {
+                       tide_plan::Slot** out_slot, const float* inbox = nullptr) {
   if (!grads || !shards) return fail(TIDE_ERR_INVALID_ARG, "grads or shards array is NULL");
   for (int32_t r = 0; r < pl->N; ++r) {
     if (!shards[r]) return fail(TIDE_ERR_INVALID_ARG, "shards[" + std::to_string(r) + "] is NULL");
@@ -378,6 +400,14 @@ tide_status prepare_rs(tide_plan* pl, const void* const* grads, float* const* sh
       if (!g) return fail(TIDE_ERR_INVALID_ARG, "grads[" + std::to_string(r * pl->P + p) + "] is NULL");
       if ((uintptr_t)g & 1) return fail(TIDE_ERR_ALIGNMENT, "gradient pointer not 2-byte aligned");
     }
+  }
+  if (pl->check_overlap) {
+    std::vector<ByteRange> in, out;
+    add_grad_ranges(pl, grads, &in);
+    add_ranges((const void* const*)shards, pl->N, (size_t)pl->S * 4, "shards", &out);
+    if (inbox) out.push_back({(uintptr_t)inbox, (uintptr_t)(inbox + tide_plan_inbox_elems(pl)), "inbox", 0});
+    tide_status st = check_overlap(in, out);
+    if (st != TIDE_OK) return st;
   }
   tide_status st = ensure_device(pl);
   if (st != TIDE_OK) return st;
@@ -465,7 +495,7 @@ tide_status tide_rs_staged(tide_plan* pl, const void* const* grads, float* const
   if ((uintptr_t)inbox & 3) return fail(TIDE_ERR_ALIGNMENT, "inbox not 4-byte aligned");
   RsArgs a;
   tide_plan::Slot* slot = nullptr;
-  tide_status st = prepare_rs(pl, grads, shards, stream, &a, &slot);
+  tide_status st = prepare_rs(pl, grads, shards, stream, &a, &slot, inbox);
   if (st != TIDE_OK) return st;
   a.inbox = inbox;
   const int64_t sum_grid =
@@ -491,6 +521,13 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
     if (pl->e[p] == 0) continue;
     if (!params[p]) return fail(TIDE_ERR_INVALID_ARG, "params[" + std::to_string(p) + "] is NULL");
     if ((uintptr_t)params[p] % elem_bytes) return fail(TIDE_ERR_ALIGNMENT, "param pointer not element-aligned");
+  }
+  if (pl->check_overlap) {
+    std::vector<ByteRange> in, out;
+    add_ranges(shards, pl->N, (size_t)pl->S * elem_bytes, "shards", &in);
+    add_param_ranges(pl, params, elem_bytes, pl->ag_unpadded, &out);
+    tide_status st = check_overlap(in, out);
+    if (st != TIDE_OK) return st;
   }
   tide_status st = ensure_device(pl);
   if (st != TIDE_OK) return st;
@@ -534,6 +571,13 @@ tide_status tide_slot_pack(tide_plan* pl, const void* const* grads, void* const*
       if (!g) return fail(TIDE_ERR_INVALID_ARG, "grads[" + std::to_string(r * pl->P + p) + "] is NULL");
       if ((uintptr_t)g & 1) return fail(TIDE_ERR_ALIGNMENT, "gradient pointer not 2-byte aligned");
     }
+  }
+  if (pl->check_overlap) {
+    std::vector<ByteRange> in, out;
+    add_grad_ranges(pl, grads, &in);
+    add_ranges((const void* const*)slots, pl->N, (size_t)2 * pl->N * pl->S, "slots", &out);
+    tide_status st = check_overlap(in, out);
+    if (st != TIDE_OK) return st;
   }
   tide_status st = ensure_device(pl);
   if (st != TIDE_OK) return st;
@@ -607,6 +651,13 @@ tide_status tide_ag_stage_place(tide_plan* pl, const void* stage, int32_t node, 
     if (pl->e[p] == 0) continue;
     if (!params[p]) return fail(TIDE_ERR_INVALID_ARG, "params[" + std::to_string(p) + "] is NULL");
     if ((uintptr_t)params[p] % elem_bytes) return fail(TIDE_ERR_ALIGNMENT, "param pointer not element-aligned");
+  }
+  if (pl->check_overlap) {
+    std::vector<ByteRange> in, out;
+    in.push_back({(uintptr_t)stage, (uintptr_t)stage + (uintptr_t)pl->M * pl->S * elem_bytes, "stage", 0});
+    add_param_ranges(pl, params, elem_bytes, false, &out);
+    tide_status st = check_overlap(in, out);
+    if (st != TIDE_OK) return st;
   }
   tide_status st = ensure_device(pl);
   if (st != TIDE_OK) return st;

@@ -176,6 +176,7 @@ struct tide_plan {
   int64_t test_drop_tile = -1;
   int32_t rs_epilogue = 0;                 // averaging / accumulate bits
   int32_t sum_order = TIDE_SUM_LANDING;    // level-2 reading (order table)
+  bool check_overlap = false;              // TIDE_OPT_CHECK_OVERLAP
   bool ag_unpadded = false;
   tide::RsItem* d_rs_items = nullptr;
   tide::AgItem* d_ag_items = nullptr;
@@ -233,4 +234,13 @@ tide_status fail(tide_status st, const std::string& msg);
 void clear_error();
 // Fills plan->order for the plan's sum_order (plan.cpp).
 void build_order_table(tide_plan* pl);
+// A byte range [lo, hi) a call reads or writes, named for error messages.
+struct ByteRange {
+  uintptr_t lo, hi;
+  const char* what;
+  int64_t index;
+};
+// INVALID_ARG if two outputs overlap or an output overlaps an input (inputs
+// may overlap each other); empty ranges are ignored (plan.cpp).
+tide_status check_overlap(const std::vector<ByteRange>& inputs, std::vector<ByteRange> outputs);
 }  // namespace tide

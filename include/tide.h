@@ -51,7 +51,8 @@
  *     A ninth captured call returns TIDE_ERR_INVALID_ARG.  The plan must
  *     outlive its graphs.  tide_rs_reduce_noalloc cannot be captured (it
  *     copies from pageable memory).
- *   - Outputs must not overlap inputs or each other.
+ *   - Outputs must not overlap inputs or each other (undefined results
+ *     otherwise; TIDE_OPT_CHECK_OVERLAP turns on a host-side check).
  */
 #ifndef TIDE_H
 #define TIDE_H
@@ -181,7 +182,12 @@ typedef enum tide_option {
                                   and the division) instead of overwriting */
   TIDE_OPT_AG_UNPADDED = 6,    /* 1: tide_ag_place writes only the R_p real
                                   rows; params[p] then needs R_p*Kp elements */
-  TIDE_OPT_SUM_ORDER = 7       /* level-2 addition order, a tide_sum_order */
+  TIDE_OPT_SUM_ORDER = 7,      /* level-2 addition order, a tide_sum_order */
+  TIDE_OPT_CHECK_OVERLAP = 8   /* 1: every call first checks on the host that
+                                  no output byte range overlaps an input or
+                                  another output (INVALID_ARG, naming the
+                                  pair); costs O(n log n) host time in the
+                                  number of pointers; default 0 */
 } tide_option;
 
 /* Orders for TIDE_OPT_SUM_ORDER.  The pages do not say in which order the

@@ -241,3 +241,86 @@ def test_staged_rs_arguments_without_a_gpu():
             assert err.value.status == status
     with tide.TidePlan([], 4, 1, 4) as plan:
         assert tide.tide_plan_inbox_elems(plan.handle) == 0
+
+
+def _overlap_status(fn):
+    with pytest.raises(tide.TideError) as err:
+        fn()
+    return err.value.status, str(err.value)
+
+
+# Both overlap tests pass fake pointers; a case the check missed would go on
+# to launch kernels on them, so they run only where there is no device.
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers must never reach a device")
+def test_overlap_check_rejects_before_any_device_work():
+    """TIDE_OPT_CHECK_OVERLAP: outputs overlapping inputs or each other are
+    rejected on the host, before any CUDA call."""
+    shapes = [(8, 64), (4, 64), (12, 64)]          # N = 4: S = 2*64 + 64 + 3*64 = 384
+    with tide.TidePlan(shapes, 4, 2, 2) as plan:
+        plan.set_option(tide.TIDE_OPT_CHECK_OVERLAP, 1)
+        S = plan.S
+        grads = [0x100000 * (i + 1) for i in range(12)]             # 1 MiB apart, each <= 1.5 KiB
+        shards = [0x4000000 + 0x10000 * r for r in range(4)]
+        # a shard starting inside rank 1's gradient of parameter 2
+        bad = list(shards)
+        bad[3] = grads[1 * 3 + 2] + 64
+        st, msg = _overlap_status(lambda: plan.rs_reduce(grads, bad, stream=0))
+        assert st == 1 and "overlaps input grads[5]" in msg
+        # two shards overlapping each other (4*S bytes each)
+        bad = list(shards)
+        bad[2] = shards[1] + 4 * S - 4
+        st, msg = _overlap_status(lambda: plan.rs_reduce(grads, bad, stream=0))
+        assert st == 1 and "shards[1]" in msg and "shards[2]" in msg
+        # the staged inbox overlapping a shard
+        st, msg = _overlap_status(lambda: tide.tide_rs_staged(plan.handle, grads, shards, shards[0] + 16, 0, 0, 0))
+        assert st == 1 and "inbox" in msg
+        # the no-alloc entry point checks too
+        bad = list(shards)
+        bad[0] = grads[0]
+        st, _ = _overlap_status(lambda: tide.tide_rs_reduce_noalloc(plan.handle, grads, bad, stream=0))
+        assert st == 1
+        # all-gather: parameter 2's block (4 ranks x 3 rows x 64 x 2 bytes)
+        # reaching 8 bytes into shard 0
+        ag_in = [0x8000000 + 0x10000 * r for r in range(4)]          # 2*S bytes each
+        params = [0x9000000, 0x9100000, ag_in[0] - 4 * 3 * 64 * 2 + 8]
+        st, msg = _overlap_status(lambda: plan.ag_place(ag_in, params, 2, stream=0))
+        assert st == 1 and "params[2]" in msg and "shards[0]" in msg
+        # Slot-Reuse pack: a slot over a gradient
+        slots = [0xA000000 + 0x100000 * r for r in range(4)]
+        slots[1] = grads[7] - 8
+        st, msg = _overlap_status(lambda: tide.tide_slot_pack(plan.handle, grads, slots, 0))
+        assert st == 1 and "slots[1]" in msg
+        # stage placement: a parameter inside the stage buffer
+        stage = 0xB000000
+        st, msg = _overlap_status(lambda: tide.tide_ag_stage_place(plan.handle, stage, 0, 0,
+                                                                   [stage + 2, 0xC000000, 0xD000000], 2, 0))
+        assert st == 1 and "stage" in msg
+        plan.set_option(tide.TIDE_OPT_CHECK_OVERLAP, 0)
+    # a padded parameter (10 rows over 4 ranks: 12 padded rows, 1536 bytes)
+    # whose real rows (1280 bytes) end where shard 0 starts
+    with tide.TidePlan([(10, 64), (4, 64), (12, 64)], 4, 2, 2) as plan:
+        plan.set_option(tide.TIDE_OPT_CHECK_OVERLAP, 1)
+        ag_in = [0x8000000 + 0x10000 * r for r in range(4)]
+        params = [ag_in[0] - 10 * 64 * 2, 0x9000000, 0x9100000]
+        st, msg = _overlap_status(lambda: plan.ag_place(ag_in, params, 2, stream=0))
+        assert st == 1 and "params[0]" in msg
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers must never reach a device")
+def test_overlap_check_lets_disjoint_and_shared_inputs_through():
+    """Inputs may overlap each other; disjoint outputs pass the check and the
+    call goes on (to the missing device: status 5)."""
+    with tide.TidePlan([(8, 64), (4, 64), (12, 64)], 4, 2, 2) as plan:
+        plan.set_option(tide.TIDE_OPT_CHECK_OVERLAP, 1)
+        grads = [0x100000] * 12                                      # every rank reads one buffer
+        shards = [0x4000000 + 0x10000 * r for r in range(4)]
+        st, _ = _overlap_status(lambda: plan.rs_reduce(grads, shards, stream=0))
+        assert st == 5
+    # the unpadded destination of the padded parameter above stops in time
+    with tide.TidePlan([(10, 64), (4, 64), (12, 64)], 4, 2, 2) as plan:
+        plan.set_option(tide.TIDE_OPT_CHECK_OVERLAP, 1)
+        plan.set_option(tide.TIDE_OPT_AG_UNPADDED, 1)
+        ag_in = [0x8000000 + 0x10000 * r for r in range(4)]
+        params = [ag_in[0] - 10 * 64 * 2, 0x9000000, 0x9100000]
+        st, _ = _overlap_status(lambda: plan.ag_place(ag_in, params, 2, stream=0))
+        assert st == 5

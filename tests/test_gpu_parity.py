@@ -503,3 +503,26 @@ def test_slot_reuse_pack_then_reduce(w):
             assert np.array_equal(got[mask], packed[r][mask]), r
             assert (got[~mask] == 0x5A5A).all(), "padding rows of a slot stay untouched"
             assert np.array_equal(f32_bits(outs[r]), expect[r].view(np.uint32)), r
+
+
+def test_overlap_check_on_real_buffers():
+    """With TIDE_OPT_CHECK_OVERLAP on, disjoint torch buffers run exactly as
+    before and a shard placed inside a gradient tensor is refused."""
+    w = SMALL[5]
+    grads = host_grads(w)
+    geo, expect = oracle_rs(w, grads)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        plan.set_option(tide.TIDE_OPT_CHECK_OVERLAP, 1)
+        dev = [[to_dev_u16(grads[r][p])[0] for p in range(w.P)] for r in range(w.N)]
+        flat = [dev[r][p] for r in range(w.N) for p in range(w.P)]
+        outs = [torch.empty(geo.S, dtype=torch.float32, device=DEV) for _ in range(w.N)]
+        plan.rs_reduce(flat, outs)
+        plan.check()
+        for r in range(w.N):
+            assert np.array_equal(f32_bits(outs[r]), expect[r].view(np.uint32)), r
+        big = max(range(len(flat)), key=lambda i: flat[i].numel())
+        inside = flat[big].view(torch.float32)[:geo.S] if flat[big].numel() >= 2 * geo.S else None
+        if inside is not None:
+            with pytest.raises(tide.TideError) as err:
+                plan.rs_reduce(flat, [inside] + outs[1:])
+            assert err.value.status == 1
