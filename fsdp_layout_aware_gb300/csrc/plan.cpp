@@ -8,7 +8,6 @@
 // gap-free prefix sum of the per-rank pieces e_p = Rp*Kp.
 
 #include <algorithm>
-#include <climits>
 #include <cstdio>
 #include <cstring>
 #include <iterator>
@@ -101,22 +100,6 @@ void build_rs_items(tide_plan* pl) {
       }
     }
   }
-}
-
-// rs_fused work units: an item larger than one CTA round is a unit of its
-// own; runs of small items are grouped, up to kRsBundle per unit (one per
-// warp), keeping list order.
-void build_rs_units(tide_plan* pl) {
-  const int64_t n = (int64_t)pl->rs_items.size();
-  pl->rs_units.clear();
-  for (int64_t i = 0; i < n;) {
-    pl->rs_units.push_back((int32_t)i);
-    int64_t j = i + 1;
-    if (pl->rs_items[i].n <= kRsSmallItem)
-      while (j < n && j - i < kRsBundle && pl->rs_items[j].n <= kRsSmallItem) ++j;
-    i = j;
-  }
-  pl->rs_units.push_back((int32_t)n);
 }
 
 void build_ag_items(tide_plan* pl) {
@@ -305,11 +288,6 @@ tide_status tide_plan_create(const tide_group_desc* d, tide_plan** out_plan) {
     }
     build_order_table(pl);
     build_rs_items(pl);
-    if (pl->rs_items.size() > (size_t)INT32_MAX) {
-      delete pl;
-      return fail(TIDE_ERR_OVERFLOW, "more than 2^31 reduce-scatter work items");
-    }
-    build_rs_units(pl);
     build_ag_items(pl);
     build_variant_items(pl);
     build_prefixes(pl);

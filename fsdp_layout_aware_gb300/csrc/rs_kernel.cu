@@ -33,11 +33,8 @@ namespace {
 // granules may extend past the item's range; they never leave the 16-byte
 // granule of a valid element, so they stay inside mapped memory, and the
 // extra lanes are never stored.
-// tid / nthr: this thread's index among the nthr threads (a whole CTA, or one
-// warp) sharing the item.
 template <int L, bool kBatched>
-__device__ __forceinline__ void reduce_aligned(const uint16_t* const* src, int M, float* dst, int n, int epi, int N,
-                                               int tid, int nthr) {
+__device__ __forceinline__ void reduce_aligned(const uint16_t* const* src, int M, float* dst, int n, int epi, int N) {
   const int ph = (int)(((uintptr_t)src[0] >> 1) & 7);
   const int nvec = (ph + n + 7) >> 3;
   // elements from a vector's first element to the next 16-byte boundary of dst
@@ -45,7 +42,7 @@ __device__ __forceinline__ void reduce_aligned(const uint16_t* const* src, int M
   const int lane = threadIdx.x & 31;
   // The loop condition is uniform per warp (the warp's first vector), so all
   // 32 lanes reach the shuffles in store8_shifted.
-  for (int v = tid; v - lane < nvec; v += nthr) {
+  for (int v = threadIdx.x; v - lane < nvec; v += blockDim.x) {
     const int e0 = v * 8 - ph;
     float acc2[8];
 #pragma unroll
@@ -91,10 +88,10 @@ __device__ __forceinline__ void reduce_aligned(const uint16_t* const* src, int M
 
 // Contributors at different address phases: element-wise loads, same order.
 template <int L, bool kBatched>
-__device__ __forceinline__ void reduce_unaligned(const uint16_t* const* src, int M, float* dst, int n, int epi, int N,
-                                                 int tid, int nthr) {
+__device__ __forceinline__ void reduce_unaligned(const uint16_t* const* src, int M, float* dst, int n, int epi,
+                                                 int N) {
   const int nvec = (n + 7) >> 3;
-  for (int v = tid; v < nvec; v += nthr) {
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
     const int e0 = v * 8;
     const int cnt = min(8, n - e0);
     float acc2[8], bsum[8];
@@ -132,72 +129,40 @@ __device__ __forceinline__ void reduce_unaligned(const uint16_t* const* src, int
   }
 }
 
-// src[k * L + l] = contributor l of the k-th node in the item's level-2 order,
-// written by the nthr threads sharing the item.
-template <int L>
-__device__ __forceinline__ void fill_sources(const RsArgs& a, const RsItem& item, const uint16_t** src, int tid,
-                                             int nthr) {
-  const uint8_t* ord = a.order + ((item.r / L) * L + item.slice) * a.M;
-  for (int t = tid; t < a.N; t += nthr) {
-    const int node = ord[t / L];
-    src[t] = a.grad_tab[(int64_t)item.p * a.N + node * L + t % L] + item.src_off;
-  }
-}
-
-template <int L, bool kBatched>
-__device__ __forceinline__ void run_item(const RsArgs& a, const RsItem& item, const uint16_t* const* src, int tid,
-                                         int nthr) {
-  float* dst = a.shard_tab[item.r] + item.dst_off;
-  if (a.uniform_phase[item.p])
-    reduce_aligned<L, kBatched>(src, a.M, dst, item.n, a.epilogue, a.N, tid, nthr);
-  else
-    reduce_unaligned<L, kBatched>(src, a.M, dst, item.n, a.epilogue, a.N, tid, nthr);
-}
-
-// CTAs take work units in list order from a shared counter (one atomicAdd per
-// unit, issued one unit ahead so its latency is hidden): the work balances
+// CTAs take items in list order from a shared counter (one atomicAdd per
+// item, issued one item ahead so its latency is hidden): the work balances
 // whatever the items' sizes, and at any moment the CTAs are on neighbouring
 // items, so the contributors are read in nearly address order across the GPU.
-// A unit is one item, reduced by the whole CTA, or a run of up to eight small
-// items, one per warp.  Without a counter (noalloc entry point) CTA b takes
-// units b, b+G, b+2G, ...
+// Without a counter (noalloc entry point) CTA b takes items b, b+G, b+2G, ...
 template <int L, bool kBatched>
 __global__ void __launch_bounds__(kRsThreads, 4) rs_fused_kernel(const __grid_constant__ RsArgs a) {
-  __shared__ const uint16_t* src[kRsBundle][kMaxN];  // one pointer table per warp; the CTA uses [0]
-  __shared__ long long next_unit[2];
+  __shared__ const uint16_t* src[kMaxN];
+  __shared__ long long next_item[2];
   unsigned long long* counter = a.counter;
-  const int64_t n_units = a.units ? a.n_units : a.n_items;
-  if (threadIdx.x == 0) next_unit[0] = counter ? take_item(counter, n_units) : (long long)blockIdx.x;
+  if (threadIdx.x == 0) next_item[0] = counter ? take_item(counter, a.n_items) : (long long)blockIdx.x;
   __syncthreads();
   int slot = 0;
-  for (int64_t u = next_unit[0]; u < n_units; u = next_unit[slot]) {
+  for (int64_t it = next_item[0]; it < a.n_items; it = next_item[slot]) {
     slot ^= 1;
-    if (threadIdx.x == 0) next_unit[slot] = counter ? take_item(counter, n_units) : (long long)(u + gridDim.x);
-    const int64_t lo = a.units ? a.units[u] : u;
-    const int64_t hi = a.units ? a.units[u + 1] : u + 1;
-    if (hi - lo == 1) {
-      const RsItem item = a.items[lo];
-      if (item.kind == RS_PAD) {
-        pad_fill(a.shard_tab[item.r] + item.dst_off, item.n, a.epilogue, threadIdx.x, blockDim.x);
-      } else {
-        fill_sources<L>(a, item, src[0], threadIdx.x, blockDim.x);
-        __syncthreads();
-        run_item<L, kBatched>(a, item, src[0], threadIdx.x, blockDim.x);
-      }
+    if (threadIdx.x == 0) next_item[slot] = counter ? take_item(counter, a.n_items) : (long long)(it + gridDim.x);
+    const RsItem item = a.items[it];
+    float* dst = a.shard_tab[item.r] + item.dst_off;
+    if (item.kind == RS_PAD) {
+      pad_fill(dst, item.n, a.epilogue, threadIdx.x, blockDim.x);
     } else {
-      const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-      if (lo + w < hi) {
-        const RsItem item = a.items[lo + w];
-        if (item.kind == RS_PAD) {
-          pad_fill(a.shard_tab[item.r] + item.dst_off, item.n, a.epilogue, lane, 32);
-        } else {
-          fill_sources<L>(a, item, src[w], lane, 32);
-          __syncwarp();
-          run_item<L, kBatched>(a, item, src[w], lane, 32);
-        }
+      // src[k * L + l]: contributor l of the k-th node in level-2 order
+      if ((int)threadIdx.x < a.N) {
+        const int k = (int)threadIdx.x / L, l = (int)threadIdx.x % L;
+        const int node = a.order[((item.r / L) * L + item.slice) * a.M + k];
+        src[threadIdx.x] = a.grad_tab[(int64_t)item.p * a.N + node * L + l] + item.src_off;
       }
+      __syncthreads();
+      if (a.uniform_phase[item.p])
+        reduce_aligned<L, kBatched>(src, a.M, dst, item.n, a.epilogue, a.N);
+      else
+        reduce_unaligned<L, kBatched>(src, a.M, dst, item.n, a.epilogue, a.N);
     }
-    __syncthreads();  // next_unit[slot] is visible; this unit's readers of src[] are done
+    __syncthreads();  // next_item[slot] is visible; this item's readers of src[] are done
   }
 }
 

@@ -158,9 +158,7 @@ extern "C" tide_status tide_rs_reduce_noalloc(const tide_plan* pl, const void* c
   RsArgs a;
   a.items = (const RsItem*)base;
   a.counter = nullptr;  // round-robin item order: nothing in the array needs zeroing
-  a.units = nullptr;    // one item per work unit
   a.n_items = (int64_t)pl->rs_items.size();
-  a.n_units = a.n_items;
   a.grad_tab = (const uint16_t* const*)(base + off_gtab);
   a.shard_tab = (float* const*)(base + off_shards);
   a.uniform_phase = base + off_flags;

@@ -53,8 +53,6 @@ void release_device_state(tide_plan* pl) {
   }
   pl->n_captured = 0;
   if (pl->d_rs_items) cudaFree(pl->d_rs_items);
-  if (pl->d_rs_units) cudaFree(pl->d_rs_units);
-  pl->d_rs_units = nullptr;
   if (pl->d_ag_items) cudaFree(pl->d_ag_items);
   if (pl->d_ag_units) cudaFree(pl->d_ag_units);
   for (int l = 0; l < kMaxL; ++l) {
@@ -104,10 +102,6 @@ tide_status ensure_device(tide_plan* pl) {
     if ((err = cudaMalloc(&pl->d_rs_items, bytes)) != cudaSuccess) return bail(err, "cudaMalloc(rs items)");
     if ((err = cudaMemcpy(pl->d_rs_items, pl->rs_items.data(), bytes, cudaMemcpyHostToDevice)) != cudaSuccess)
       return bail(err, "cudaMemcpy(rs items)");
-    const size_t ubytes = pl->rs_units.size() * sizeof(int32_t);
-    if ((err = cudaMalloc(&pl->d_rs_units, ubytes)) != cudaSuccess) return bail(err, "cudaMalloc(rs units)");
-    if ((err = cudaMemcpy(pl->d_rs_units, pl->rs_units.data(), ubytes, cudaMemcpyHostToDevice)) != cudaSuccess)
-      return bail(err, "cudaMemcpy(rs units)");
   }
   if (!pl->ag_items.empty()) {
     const size_t bytes = pl->ag_items.size() * sizeof(AgItem);
@@ -445,8 +439,6 @@ tide_status prepare_rs(tide_plan* pl, const void* const* grads, float* const* sh
 
   a->items = pl->d_rs_items;
   a->n_items = (int64_t)pl->rs_items.size();
-  a->units = pl->d_rs_units;
-  a->n_units = (int64_t)pl->rs_units.size() - 1;
   a->counter = (unsigned long long*)(slot->dev + counter_at);
   a->grad_tab = (const uint16_t* const*)slot->dev;
   a->shard_tab = (float* const*)(slot->dev + n_grad * 8);

@@ -51,11 +51,6 @@ static_assert(sizeof(AgItem) == 32, "AgItem layout");
 constexpr int kRsThreads = 256;
 constexpr int64_t kRsChunk = 8192;
 constexpr int64_t kRsPadChunk = 32768;
-// RS items of at most one CTA round (kRsThreads * 8 elements) are grouped into
-// work units of up to kRsBundle consecutive items, one item per warp, so a
-// small piece does not hold a whole CTA for a partial round.
-constexpr int kRsSmallItem = kRsThreads * 8;
-constexpr int kRsBundle = kRsThreads / 32;
 constexpr int kAgThreads = 256;
 constexpr int64_t kAgChunkBytes = 65536;
 
@@ -119,8 +114,6 @@ struct BulkLayout {
 struct RsArgs {
   const RsItem* items;
   int64_t n_items;
-  const int32_t* units;             // rs_fused: [n_units + 1] first item of each work unit;
-  int64_t n_units;                  // NULL: one item per unit
   unsigned long long* counter;      // next item to take: zero at launch, and the kernel leaves it
                                     // zero (see take_item); NULL: round-robin
   const uint16_t* const* grad_tab;  // [P][N]: contributor src's gradient of p
@@ -164,7 +157,6 @@ struct tide_plan {
   std::vector<int64_t> rows, Kp, Rp, e, o;
   int64_t S = 0;
   std::vector<tide::RsItem> rs_items;
-  std::vector<int32_t> rs_units;           // first item of each rs_fused work unit, then the item count
   std::vector<tide::AgItem> ag_items;
   std::vector<tide::AgItem> ag_items_unpadded;  // ag_items restricted to real rows
   std::vector<tide::AgItem> pack_items;         // Slot-Reuse: r = grad index r*P+p, p = slot rank
@@ -187,7 +179,6 @@ struct tide_plan {
   bool check_overlap = false;              // TIDE_OPT_CHECK_OVERLAP
   bool ag_unpadded = false;
   tide::RsItem* d_rs_items = nullptr;
-  int32_t* d_rs_units = nullptr;
   tide::AgItem* d_ag_items = nullptr;
   tide::UnitStart* d_ag_units = nullptr;
   int64_t ag_units = 0;
