@@ -79,31 +79,8 @@ extern "C" tide_status tide_rs_reduce_noalloc(const tide_plan* pl, const void* c
   clear_error();
   if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
   if (pl->rs_items.empty()) return TIDE_OK;
-  if (!grads || !shards) return fail(TIDE_ERR_INVALID_ARG, "grads or shards array is NULL");
-  for (int32_t r = 0; r < pl->N; ++r) {
-    if (!shards[r]) return fail(TIDE_ERR_INVALID_ARG, "shards[" + std::to_string(r) + "] is NULL");
-    if ((uintptr_t)shards[r] & 3) return fail(TIDE_ERR_ALIGNMENT, "shard pointer not 4-byte aligned");
-  }
-  for (int32_t p = 0; p < pl->P; ++p) {
-    if (pl->e[p] == 0) continue;
-    for (int32_t r = 0; r < pl->N; ++r) {
-      const void* g = grads[(size_t)r * pl->P + p];
-      if (!g) return fail(TIDE_ERR_INVALID_ARG, "grads[" + std::to_string(r * pl->P + p) + "] is NULL");
-      if ((uintptr_t)g & 1) return fail(TIDE_ERR_ALIGNMENT, "gradient pointer not 2-byte aligned");
-    }
-  }
-  if (pl->check_overlap) {
-    std::vector<ByteRange> in, out;
-    for (int32_t r = 0; r < pl->N; ++r) {
-      for (int32_t p = 0; p < pl->P; ++p) {
-        const uintptr_t g = (uintptr_t)grads[(size_t)r * pl->P + p];
-        in.push_back({g, g + (uintptr_t)(2 * pl->rows[p] * pl->Kp[p]), "grads", (int64_t)r * pl->P + p});
-      }
-      out.push_back({(uintptr_t)shards[r], (uintptr_t)(shards[r] + pl->S), "shards", r});
-    }
-    const tide_status st = check_overlap(in, out);
-    if (st != TIDE_OK) return st;
-  }
+  const tide_status st = check_rs_call(pl, grads, shards, nullptr);
+  if (st != TIDE_OK) return st;
 
   // Scratch layout: items | caller's [r][p] pointers | [p][r] table | shards | flags.
   const size_t n_ptr = (size_t)pl->N * pl->P;

@@ -386,8 +386,10 @@ void add_param_ranges(const tide_plan* pl, void* const* params, int32_t eb, bool
   }
 }
 
-tide_status prepare_rs(tide_plan* pl, const void* const* grads, float* const* shards, void* stream, RsArgs* a,
-                       tide_plan::Slot** out_slot, const float* inbox = nullptr) {
+}  // namespace
+
+tide_status tide::check_rs_call(const tide_plan* pl, const void* const* grads, float* const* shards,
+                                const float* inbox) {
   if (!grads || !shards) return fail(TIDE_ERR_INVALID_ARG, "grads or shards array is NULL");
   for (int32_t r = 0; r < pl->N; ++r) {
     if (!shards[r]) return fail(TIDE_ERR_INVALID_ARG, "shards[" + std::to_string(r) + "] is NULL");
@@ -406,10 +408,18 @@ tide_status prepare_rs(tide_plan* pl, const void* const* grads, float* const* sh
     add_grad_ranges(pl, grads, &in);
     add_ranges((const void* const*)shards, pl->N, (size_t)pl->S * 4, "shards", &out);
     if (inbox) out.push_back({(uintptr_t)inbox, (uintptr_t)(inbox + tide_plan_inbox_elems(pl)), "inbox", 0});
-    tide_status st = check_overlap(in, out);
-    if (st != TIDE_OK) return st;
+    return check_overlap(in, out);
   }
-  tide_status st = ensure_device(pl);
+  return TIDE_OK;
+}
+
+namespace {
+
+tide_status prepare_rs(tide_plan* pl, const void* const* grads, float* const* shards, void* stream, RsArgs* a,
+                       tide_plan::Slot** out_slot, const float* inbox = nullptr) {
+  tide_status st = check_rs_call(pl, grads, shards, inbox);
+  if (st != TIDE_OK) return st;
+  st = ensure_device(pl);
   if (st != TIDE_OK) return st;
   tide_plan::Slot* slot = nullptr;
 

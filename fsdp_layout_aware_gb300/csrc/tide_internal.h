@@ -232,6 +232,9 @@ std::vector<UnitStart> ag_unit_starts_of(const std::vector<AgItem>& items, int64
 // Thread-local error reporting (plan.cpp).
 tide_status fail(tide_status st, const std::string& msg);
 void clear_error();
+// Argument checks shared by every reduce-scatter entry point: null and
+// misaligned pointers, and the overlap check when it is on (runtime.cu).
+tide_status check_rs_call(const tide_plan* pl, const void* const* grads, float* const* shards, const float* inbox);
 // Fills plan->order for the plan's sum_order (plan.cpp).
 void build_order_table(tide_plan* pl);
 // A byte range [lo, hi) a call reads or writes, named for error messages.
