@@ -224,15 +224,18 @@ tide_status tide_plan_check(tide_plan* plan);
  *   level 1: part_n = fp32 sum over l = 0..L-1 of grads[n*L+l][p][r*e_p + e]
  *            for every source node n (round-to-nearest-even, from +0.0);
  *   level 2: the M partials added, from +0.0, in the order of the destination
- *            GPU g = 0..L-1 they land on under the Latin-square placement:
+ *            GPU g = 0..L-1 they land on under the Latin-square placement
+ *            (the default TIDE_SUM_LANDING; see TIDE_OPT_SUM_ORDER):
  *            slice s = (op+e) / ceil(S/L); GPU g holds the partial of the
  *            source whose relative index c = (n_d - n) mod M satisfies
  *            (s - c) mod L == g.  When M > L, relative indices go in batches
  *            [b*L, b*L + L): each batch is summed that way from +0.0 and the
  *            batch sums are added in ascending b.
  * and +0.0 for a padding row.  The result is bit-identical to that order.
- * Errors: INVALID_ARG (null plan/arrays/pointer), ALIGNMENT, CUDA,
- * OUT_OF_MEMORY (first call's device set-up), DEVICE_MISMATCH. */
+ * Errors: INVALID_ARG (null plan/arrays/pointer; overlapping buffers when
+ * TIDE_OPT_CHECK_OVERLAP is on), ALIGNMENT, CUDA, OUT_OF_MEMORY (first call's
+ * device set-up), DEVICE_MISMATCH, UNIMPLEMENTED (the bulk-copy kernel with
+ * more than 8 nodes). */
 tide_status tide_rs_reduce(tide_plan* plan, const void* const* grads, float* const* shards,
                            void* stream);
 
@@ -301,7 +304,8 @@ tide_status tide_rs_reduce_slots(tide_plan* plan, const void* const* slots, floa
  *   written to the inbox slot where the Latin square lands it: destination
  *   GPU g = (s - c) mod L, c = (n_d - n_s) mod M, for slice s;
  *   stage 2 (landing CTAs): each destination element adds its slice's
- *   partials from landing GPUs g = 0..L-1 in turn.
+ *   partials in the plan's level-2 order (by default from landing GPUs
+ *   g = 0..L-1 in turn), batch by batch when M > L.
  * The inbox costs 8*M extra bytes of traffic per shard element. */
 
 /* Floats the inbox needs: M * L * M * L * ceil(S / L) (0 when S == 0); -1
