@@ -154,15 +154,17 @@ tide_status ensure_device(tide_plan* pl) {
   pl->rs_grid = (int)std::min<int64_t>((int64_t)pl->num_sms * rs_occ, std::max<int64_t>(1, pl->rs_items.size()));
   pl->ag_grid = (int)std::min<int64_t>((int64_t)pl->num_sms * ag_occ,
                                        std::max<int64_t>(1, ((int64_t)pl->ag_items.size() + 7) / 8));
-  // Equal-cost all-gather units: about 16 KiB each, at most 32 per warp.
+  // Equal-cost all-gather units: about 8 KiB each, at most 64 per warp (a sweep
+  // of 4-32 KiB and 2-4 CTAs per SM on the four full-size workloads put the
+  // best here).
   try {
-    const std::vector<UnitStart> au = ag_unit_starts(pl, (int64_t)pl->ag_grid * (kAgThreads / 32), 16 << 10, 32);
+    const std::vector<UnitStart> au = ag_unit_starts(pl, (int64_t)pl->ag_grid * (kAgThreads / 32), 8 << 10, 64);
     pl->ag_units = (int64_t)au.size() - 1;
     // Unpadded all-gather and Slot-Reuse packing lists.
     auto upload = [&](const std::vector<AgItem>& v, AgItem** d_items, UnitStart** d_units,
                       int64_t* n_units) -> cudaError_t {
       if (v.empty()) return cudaSuccess;
-      const std::vector<UnitStart> u = ag_unit_starts_of(v, (int64_t)pl->ag_grid * (kAgThreads / 32), 16 << 10, 32);
+      const std::vector<UnitStart> u = ag_unit_starts_of(v, (int64_t)pl->ag_grid * (kAgThreads / 32), 8 << 10, 64);
       *n_units = (int64_t)u.size() - 1;
       cudaError_t e2 = cudaMalloc(d_items, v.size() * sizeof(AgItem));
       if (e2 == cudaSuccess) e2 = cudaMemcpy(*d_items, v.data(), v.size() * sizeof(AgItem), cudaMemcpyHostToDevice);
@@ -181,7 +183,7 @@ tide_status ensure_device(tide_plan* pl) {
         if (it.r % pl->L == l) ri.push_back(it);
       pl->rail_n_items[l] = (int64_t)ri.size();
       if (ri.empty()) continue;
-      const std::vector<UnitStart> ru = ag_unit_starts_of(ri, (int64_t)pl->ag_grid * (kAgThreads / 32), 16 << 10, 32);
+      const std::vector<UnitStart> ru = ag_unit_starts_of(ri, (int64_t)pl->ag_grid * (kAgThreads / 32), 8 << 10, 64);
       pl->rail_n_units[l] = (int64_t)ru.size() - 1;
       if ((err = cudaMalloc(&pl->d_rail_items[l], ri.size() * sizeof(AgItem))) != cudaSuccess)
         return bail(err, "cudaMalloc(rail items)");
