@@ -152,8 +152,11 @@ tide_status ensure_device(tide_plan* pl) {
     return fail(TIDE_ERR_CUDA, "occupancy query failed (is this an sm_103 device?)");
   }
   pl->rs_grid = (int)std::min<int64_t>((int64_t)pl->num_sms * rs_occ, std::max<int64_t>(1, pl->rs_items.size()));
-  pl->ag_grid = (int)std::min<int64_t>((int64_t)pl->num_sms * ag_occ,
-                                       std::max<int64_t>(1, ((int64_t)pl->ag_items.size() + 7) / 8));
+  // The all-gather's units are dealt to warps statically, so every SM gets
+  // the same number of CTAs: with fewer CTAs than SMs x occupancy, SMs with
+  // more CTAs give each warp less bandwidth and set the tail.  Warps left
+  // without units exit at once.
+  pl->ag_grid = pl->num_sms * ag_occ;
   // Equal-cost all-gather units: about 8 KiB each, at most 64 per warp (a sweep
   // of 4-32 KiB and 2-4 CTAs per SM on the four full-size workloads put the
   // best here).
