@@ -74,6 +74,7 @@ namespace {
 
 void build_rs_items(tide_plan* pl) {
   const int64_t S = pl->S;
+  const int64_t chunk = rs_chunk_elems(pl->N);
   const int64_t slice_len = S > 0 ? (S + pl->L - 1) / pl->L : 1;
   for (int32_t p = 0; p < pl->P; ++p) {
     const int64_t e_p = pl->e[p], o_p = pl->o[p];
@@ -85,7 +86,7 @@ void build_rs_items(tide_plan* pl) {
       for (int64_t e = 0; e < v;) {
         const int64_t s = (o_p + e) / slice_len;
         const int64_t slice_end = (s + 1) * slice_len - o_p;
-        const int64_t chunk_end = ((src0 + e) / kRsChunk + 1) * kRsChunk - src0;
+        const int64_t chunk_end = ((src0 + e) / chunk + 1) * chunk - src0;
         const int64_t end = std::min(v, std::min(slice_end, chunk_end));
         pl->rs_items.push_back(RsItem{src0 + e, o_p + e, (int32_t)(end - e), p, r, (int16_t)s, RS_VALID});
         e = end;

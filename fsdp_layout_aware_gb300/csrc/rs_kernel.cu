@@ -13,8 +13,9 @@
 // the fp32 additions is exactly that one, so the result is bit-reproducible.
 //
 // Work decomposition: a persistent grid of CTAs walks the plan's item list
-// round-robin; an item is one contiguous range (<= 8192 elements) of one
-// (parameter, destination rank) piece inside one level-2 slice.  Each thread
+// from a shared counter; an item is one contiguous range (2048-8192 elements,
+// fewer the more ranks read it) of one (parameter, destination rank) piece
+// inside one level-2 slice.  Each thread
 // owns 8 consecutive outputs, so each contributor is read with one 16-byte
 // load per thread and a warp reads 512 contiguous bytes of each contributor.
 

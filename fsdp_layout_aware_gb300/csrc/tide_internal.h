@@ -44,12 +44,22 @@ struct AgItem {
 };
 static_assert(sizeof(AgItem) == 32, "AgItem layout");
 
-// Work-list chunking.  A valid RS chunk covers at most kRsChunk elements and
-// starts on a multiple of kRsChunk in contributor-index space, so interior
-// chunks are whole, 16-byte aligned runs of every contributor; padding chunks
-// only write, so they are larger.  AG chunks are kAgChunkBytes of payload.
+// Work-list chunking.  A valid RS chunk covers at most rs_chunk_elems(N)
+// elements and starts on a multiple of it in contributor-index space, so
+// interior chunks are whole, 16-byte aligned runs of every contributor; padding
+// chunks only write, so they are larger.  AG chunks are kAgChunkBytes of
+// payload.
 constexpr int kRsThreads = 256;
-constexpr int64_t kRsChunk = 8192;
+// An RS item reads 2*N bytes per element.  Items of about 128-256 KB of reads
+// were fastest in a sweep of 1024-32768 elements on the four full-size
+// workloads: larger ones leave a long tail when the last items finish, smaller
+// ones pay the per-item set-up more often.  So the chunk is the power of two
+// nearest below 128 Ki / N elements, kept within [2048, 8192].
+inline int64_t rs_chunk_elems(int32_t N) {
+  int64_t c = 8192;
+  while (c > 2048 && c * N > (int64_t)1 << 17) c >>= 1;
+  return c;
+}
 constexpr int64_t kRsPadChunk = 32768;
 constexpr int kAgThreads = 256;
 constexpr int64_t kAgChunkBytes = 65536;
@@ -62,8 +72,8 @@ constexpr int64_t kAgChunkBytes = 65536;
 // w, w+W, w+2W, ...: every warp gets k units of equal cost, and at any moment
 // neighbouring warps copy neighbouring parts of the item list, which keeps
 // DRAM accesses in nearly address order.  (The reduce-scatter's items are
-// already of near-equal cost -- 8192 elements -- and it takes them
-// round-robin.)
+// already of near-equal cost -- rs_chunk_elems(N) elements -- and its CTAs
+// take them from a shared counter.)
 #if defined(__CUDACC__)
 #define TIDE_HD __host__ __device__
 #else
