@@ -65,8 +65,17 @@ def _check_plan_against_oracle(shapes, M, L):
         _check_ag_items(plan, geo)
 
 
+def _rs_chunk(N):
+    """Elements per RS item: the power of two at or below 128 Ki / N, in [2048, 8192]."""
+    c = 8192
+    while c > 2048 and c * N > 1 << 17:
+        c //= 2
+    return c
+
+
 def _check_rs_items(plan, geo, M, L):
     N = geo.N
+    chunk = _rs_chunk(N)
     cover = [bytearray(geo.S) for _ in range(N)]
     for it in plan.items(0):
         p, r, n, dst = it["p"], it["r"], it["n"], it["dst_off"]
@@ -77,6 +86,8 @@ def _check_rs_items(plan, geo, M, L):
         if it["kind"] == 0:
             assert e0 + n <= v
             assert it["src_off"] == r * geo.e[p] + e0     # contributors' rows r*Rp...
+            # never across a chunk boundary of the contributors' index space
+            assert it["src_off"] // chunk == (it["src_off"] + n - 1) // chunk
         else:
             assert it["kind"] == 1 and e0 >= v
         for x in range(dst, dst + n):
@@ -114,11 +125,15 @@ def test_workload_geometry_matches_oracle(cfg):
             for s in range(w.L):
                 assert plan.level2_order(n_dest, s) == O.level2_order(s, n_dest, w.M, w.L)
         items = plan.items(0)
-        # per destination rank, item lengths add up to the shard
+        # per destination rank, item lengths add up to the shard; valid items
+        # hold at most one chunk (8192 elements for N <= 16, 2048 for N >= 48)
         per_rank = [0] * w.N
         for it in items:
             per_rank[it["r"]] += it["n"]
+            if it["kind"] == 0:
+                assert it["n"] <= _rs_chunk(w.N)
         assert per_rank == [geo.S] * w.N
+        assert _rs_chunk(w.N) == {1: 8192, 2: 8192, 3: 8192, 4: 2048, 5: 2048}[cfg]
         if cfg == 1:
             _check_rs_items(plan, geo, w.M, w.L)
             _check_ag_items(plan, geo)
