@@ -562,17 +562,21 @@ def run_rd_ag(args, local_rank):
             tide.tide_ag_rd_exchange(plan.handle, stages, 2, stream)
             tide.tide_ag_stage_place(plan.handle, stages[0], 0, rail, pp, 2, stream)
 
-    with torch.cuda.stream(stream):
-        t = _event_time(step, max(1, args.steps // 8), args.warmup, stream)
-        ta = _event_time(lambda: plan.ag_place(tide.pointer_array(ag_in), pp, 2, stream), args.steps, args.warmup,
-                         stream)
     place_bytes = 4 * w.N * S
     exch_bytes = L * M * (M - 1) * S * 2 * 2
+    res = {}
+    with torch.cuda.stream(stream):
+        for name, mode in (("copy_engines", 0), ("sm_kernel", 1)):
+            plan.set_option(tide.TIDE_OPT_RD_EXCHANGE, mode)
+            t = _event_time(step, max(1, args.steps // 8), args.warmup, stream)
+            res[name] = {"ms_per_step": round(t * 1e3, 4), "GB_s": round((place_bytes + exch_bytes) / t / 1e9, 1)}
+        ta = _event_time(lambda: plan.ag_place(tide.pointer_array(ag_in), pp, 2, stream), args.steps, args.warmup,
+                         stream)
     return {"path": "rd-ag", "metric": METRIC, "unit": "GB/s", "n_gpus": 1, "dtype": "bf16 copy", "data": "synthetic",
             "config": {"workload": f"{w.name}: {w.notes}", "N": w.N, "M": M, "L": L,
                        "rounds": tide.tide_rd_rounds(M)},
-            "ms_per_step": round(t * 1e3, 4), "placement_bytes": place_bytes, "exchange_bytes": exch_bytes,
-            "value": round((place_bytes + exch_bytes) / t / 1e9, 1),
+            "placement_bytes": place_bytes, "exchange_bytes": exch_bytes, "exchange": res,
+            "ms_per_step": res["copy_engines"]["ms_per_step"], "value": res["copy_engines"]["GB_s"],
             "direct_landing_ms": round(ta * 1e3, 4)}
 
 

@@ -62,6 +62,13 @@ void release_device_state(tide_plan* pl) {
     pl->d_rail_units[l] = nullptr;
     pl->rail_n_items[l] = pl->rail_n_units[l] = 0;
   }
+  for (int d = 0; d < tide_plan::kMaxRounds; ++d) {
+    if (pl->d_rd_items[d]) cudaFree(pl->d_rd_items[d]);
+    if (pl->d_rd_units[d]) cudaFree(pl->d_rd_units[d]);
+    pl->d_rd_items[d] = nullptr;
+    pl->d_rd_units[d] = nullptr;
+    pl->rd_n_items[d] = pl->rd_n_units[d] = 0;
+  }
   if (pl->d_status) cudaFree(pl->d_status);
   pl->d_status = nullptr;
   for (void* q : {(void*)pl->d_agu_items, (void*)pl->d_agu_units, (void*)pl->d_pack_items, (void*)pl->d_pack_units})
@@ -199,6 +206,22 @@ tide_status ensure_device(tide_plan* pl) {
           cudaSuccess)
         return bail(err, "cudaMemcpy(rail units)");
     }
+    // Recursive-doubling rounds for the SM exchange: in round d node n copies
+    // the first c = min(2^d, M - 2^d) pieces of node (n + 2^d) mod M's stage
+    // buffer to its own slots [2^d, 2^d + c), in 32768-element items.  The
+    // lists count elements, so they serve both element sizes.
+    const int32_t rounds = tide_rd_rounds(pl->M);
+    for (int32_t d = 0; d < rounds && d < tide_plan::kMaxRounds && pl->S > 0; ++d) {
+      const int64_t have = (int64_t)1 << d, c = tide_rd_send_count(pl->M, d);
+      std::vector<AgItem> v;
+      for (int32_t n = 0; n < pl->M; ++n)
+        for (int64_t e = 0; e < c * pl->S; e += 32768)
+          v.push_back(AgItem{e, have * pl->S + e, (int32_t)std::min<int64_t>(32768, c * pl->S - e), n,
+                             (int32_t)((n + have) % pl->M), 0});
+      pl->rd_n_items[d] = (int64_t)v.size();
+      if ((err = upload(v, &pl->d_rd_items[d], &pl->d_rd_units[d], &pl->rd_n_units[d])) != cudaSuccess)
+        return bail(err, "uploading the exchange rounds");
+    }
     if ((err = cudaMalloc(&pl->d_ag_units, au.size() * sizeof(UnitStart))) != cudaSuccess)
       return bail(err, "cudaMalloc(ag units)");
     if ((err = cudaMemcpy(pl->d_ag_units, au.data(), au.size() * sizeof(UnitStart), cudaMemcpyHostToDevice)) !=
@@ -223,7 +246,7 @@ tide_status acquire_slot(tide_plan* pl, tide_plan::Slot** out) {
   return TIDE_OK;
 }
 
-enum TableKind { TABLE_RS = 0, TABLE_AG = 1, TABLE_PACK = 2, TABLE_STAGE = 3 };
+enum TableKind { TABLE_RS = 0, TABLE_AG = 1, TABLE_PACK = 2, TABLE_STAGE = 3, TABLE_RD = 4 };
 
 // Puts the pointer table just built in pl->table_scratch (its first `bytes`)
 // on the device.  If the previous table of this kind is byte-for-byte the
@@ -337,6 +360,10 @@ tide_status tide_plan_set_option(tide_plan* pl, int32_t option, int64_t value) {
         return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_SUM_ORDER must be TIDE_SUM_LANDING or TIDE_SUM_RELATIVE");
       pl->sum_order = (int32_t)value;
       build_order_table(pl);  // read by every later call (passed by value at launch)
+      return TIDE_OK;
+    case TIDE_OPT_RD_EXCHANGE:
+      if (value != 0 && value != 1) return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_RD_EXCHANGE must be 0 or 1");
+      pl->rd_exchange = (int32_t)value;
       return TIDE_OK;
     case TIDE_OPT_CHECK_OVERLAP:
       if (value != 0 && value != 1) return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_CHECK_OVERLAP must be 0 or 1");
@@ -641,6 +668,32 @@ tide_status tide_ag_rd_exchange(tide_plan* pl, void* const* stages, int32_t elem
   const size_t piece = (size_t)pl->S * elem_bytes;
   cudaStream_t s = (cudaStream_t)stream;
   const int32_t rounds = tide_rd_rounds(pl->M);
+  if (pl->rd_exchange == 1) {
+    // SM kernel: one all-gather launch per round over that round's M copies
+    // (rounds stay in stream order; within a round node n reads slots below
+    // 2^d of another buffer and writes slots from 2^d up of its own).
+    tide_status st = ensure_device(pl);
+    if (st != TIDE_OK) return st;
+    if (rounds > tide_plan::kMaxRounds) return fail(TIDE_ERR_UNIMPLEMENTED, "more than 5 exchange rounds");
+    void** tab = (void**)pl->table_scratch.data();
+    for (int32_t n = 0; n < pl->M; ++n) tab[n] = stages[n];
+    tide_plan::Slot* slot = nullptr;
+    if ((st = commit_table(pl, TABLE_RD, (size_t)pl->M * 8, s, &slot)) != TIDE_OK) return st;
+    for (int32_t d = 0; d < rounds; ++d) {
+      AgArgs a;
+      a.items = pl->d_rd_items[d];
+      a.n_items = pl->rd_n_items[d];
+      a.units = pl->d_rd_units[d];
+      a.n_units = pl->rd_n_units[d];
+      a.shard_tab = (const unsigned char* const*)slot->dev;
+      a.param_tab = (unsigned char* const*)slot->dev;
+      a.elem_bytes = elem_bytes;
+      const int lerr = launch_ag(a, pl->ag_grid, stream);
+      if (d + 1 < rounds && lerr != cudaSuccess) return cuda_fail((cudaError_t)lerr, "exchange launch");
+      if (d + 1 == rounds) return finish(slot, lerr, s, "exchange launch");
+    }
+    return TIDE_OK;
+  }
   for (int32_t d = 0; d < rounds; ++d) {
     const int32_t have = 1 << d;                     // pieces every node holds before round d
     const int32_t c = tide_rd_send_count(pl->M, d);  // pieces sent this round

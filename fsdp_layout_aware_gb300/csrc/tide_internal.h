@@ -205,6 +205,15 @@ struct tide_plan {
   tide::UnitStart* d_rail_units[tide::kMaxL] = {};
   int64_t rail_n_items[tide::kMaxL] = {};
   int64_t rail_n_units[tide::kMaxL] = {};
+  // Recursive-doubling exchange on the SMs (TIDE_OPT_RD_EXCHANGE = 1): round
+  // d's copies as all-gather items whose shard and parameter tables are both
+  // the M stage buffers (r = source node, p = destination node).
+  static constexpr int kMaxRounds = 5;  // ceil(log2 32)
+  tide::AgItem* d_rd_items[kMaxRounds] = {};
+  tide::UnitStart* d_rd_units[kMaxRounds] = {};
+  int64_t rd_n_items[kMaxRounds] = {};
+  int64_t rd_n_units[kMaxRounds] = {};
+  int32_t rd_exchange = 0;                 // 0: copy engines, 1: SM kernel
   static constexpr int kRing = 8;
   struct Slot {
     unsigned char* host = nullptr;
@@ -226,9 +235,9 @@ struct tide_plan {
   size_t slot_bytes = 0;
   // Pointer tables are built in table_scratch; a call whose table equals the
   // previous one of its kind reuses that slot's device copy (no upload).
-  static constexpr int kTableKinds = 4;  // RS, AG, Slot-Reuse pack, stage placement
+  static constexpr int kTableKinds = 5;  // RS, AG, Slot-Reuse pack, stage placement, exchange
   std::vector<unsigned char> table_scratch;
-  int cached_slot[kTableKinds] = {-1, -1, -1, -1};
+  int cached_slot[kTableKinds] = {-1, -1, -1, -1, -1};
   uint64_t cached_gen[kTableKinds] = {};
   uint64_t next_gen = 0;
 };

@@ -183,11 +183,16 @@ typedef enum tide_option {
   TIDE_OPT_AG_UNPADDED = 6,    /* 1: tide_ag_place writes only the R_p real
                                   rows; params[p] then needs R_p*Kp elements */
   TIDE_OPT_SUM_ORDER = 7,      /* level-2 addition order, a tide_sum_order */
-  TIDE_OPT_CHECK_OVERLAP = 8   /* 1: every call first checks on the host that
+  TIDE_OPT_CHECK_OVERLAP = 8,  /* 1: every call first checks on the host that
                                   no output byte range overlaps an input or
                                   another output (INVALID_ARG, naming the
                                   pair); costs O(n log n) host time in the
                                   number of pointers; default 0 */
+  TIDE_OPT_RD_EXCHANGE = 9     /* tide_ag_rd_exchange's copies: 0 (default)
+                                  one copy-engine copy per node per round, as
+                                  the pages' transport; 1 one SM kernel launch
+                                  per round over all M copies (same bytes,
+                                  same result) */
 } tide_option;
 
 /* Orders for TIDE_OPT_SUM_ORDER.  The pages do not say in which order the
@@ -343,8 +348,10 @@ int32_t tide_rd_send_count(int32_t M, int32_t d);
  *               hold node n's own shard.  Slots 1..M-1 are overwritten.
  *   elem_bytes  2 or 4
  * Every round is one device-to-device copy per node (copy engines, as the
- * pages' transport), enqueued on `stream` in round order.
- * Errors: INVALID_ARG (null or aliasing buffers), CUDA. */
+ * pages' transport), enqueued on `stream` in round order; with
+ * TIDE_OPT_RD_EXCHANGE = 1 every round is one SM kernel launch instead.
+ * Errors: INVALID_ARG (null or aliasing buffers), CUDA, OUT_OF_MEMORY and
+ * DEVICE_MISMATCH (SM exchange: first call's set-up). */
 tide_status tide_ag_rd_exchange(tide_plan* plan, void* const* stages, int32_t elem_bytes, void* stream);
 
 /* Destination phase of the exchange ([Abstract] Figure 5(b)): write rail

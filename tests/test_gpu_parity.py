@@ -371,10 +371,12 @@ def test_host_buffers_through_the_c_abi():
 
 @pytest.mark.parametrize("w", [SMALL[0], SMALL[3], SMALL[4], SMALL[5]], ids=lambda w: w.name)
 @pytest.mark.parametrize("elem_bytes", [2, 4])
-def test_ag_by_recursive_doubling_matches_direct_landing(w, elem_bytes):
+@pytest.mark.parametrize("exchange", [0, 1], ids=["copy_engines", "sm_kernel"])
+def test_ag_by_recursive_doubling_matches_direct_landing(w, elem_bytes, exchange):
     """All-gather the pages' way -- per rail, recursive-doubling exchange
     between the nodes' stage buffers, then the strided stage placement --
-    must land every piece exactly where the direct all-gather does."""
+    must land every piece exactly where the direct all-gather does, with the
+    exchange on copy engines or on the SMs."""
     geo = O.geometry(w.shapes, w.N)
     M, L, S = w.M, w.L, geo.S
     dt, tdt = (np.uint16, torch.int16) if elem_bytes == 2 else (np.uint32, torch.int32)
@@ -383,6 +385,7 @@ def test_ag_by_recursive_doubling_matches_direct_landing(w, elem_bytes):
     expect = O.ag_place(geo, shards_h)
     shards = [torch.from_numpy(x.view(np.int16 if elem_bytes == 2 else np.int32)).to(DEV) for x in shards_h]
     with tide.TidePlan(w.shapes, w.N, M, L) as plan:
+        plan.set_option(tide.TIDE_OPT_RD_EXCHANGE, exchange)
         for node in sorted({0, M - 1}):
             params = [torch.full((w.N * geo.e[p],), -5, dtype=tdt, device=DEV) for p in range(w.P)]
             for rail in range(L):
