@@ -361,6 +361,10 @@ tide_status tide_plan_set_option(tide_plan* pl, int32_t option, int64_t value) {
       pl->sum_order = (int32_t)value;
       build_order_table(pl);  // read by every later call (passed by value at launch)
       return TIDE_OK;
+    case TIDE_OPT_AG_COPY_ENGINES:
+      if (value != 0 && value != 1) return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_AG_COPY_ENGINES must be 0 or 1");
+      pl->ag_copy_engines = value != 0;
+      return TIDE_OK;
     case TIDE_OPT_RD_EXCHANGE:
       if (value != 0 && value != 1) return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_RD_EXCHANGE must be 0 or 1");
       pl->rd_exchange = (int32_t)value;
@@ -571,6 +575,24 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
     tide_status st = check_overlap(in, out);
     if (st != TIDE_OK) return st;
   }
+  cudaStream_t s = (cudaStream_t)stream;
+  if (pl->ag_copy_engines) {
+    // The pages' transport: one copy-engine copy per (parameter, rank) piece,
+    // straight to its final address; no kernel, no device state.
+    for (int32_t p = 0; p < pl->P; ++p) {
+      for (int32_t r = 0; r < pl->N; ++r) {
+        const int64_t n = pl->ag_unpadded ? std::min(pl->Rp[p], std::max<int64_t>(0, pl->rows[p] - r * pl->Rp[p])) *
+                                                pl->Kp[p]
+                                          : pl->e[p];
+        if (n == 0) continue;
+        TIDE_CUDA(cudaMemcpyAsync((unsigned char*)params[p] + (size_t)r * pl->e[p] * elem_bytes,
+                                  (const unsigned char*)shards[r] + (size_t)pl->o[p] * elem_bytes,
+                                  (size_t)n * elem_bytes, cudaMemcpyDeviceToDevice, s),
+                  "all-gather piece copy");
+      }
+    }
+    return TIDE_OK;
+  }
   tide_status st = ensure_device(pl);
   if (st != TIDE_OK) return st;
   tide_plan::Slot* slot = nullptr;
@@ -578,7 +600,6 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
   void** ptab = (void**)(pl->table_scratch.data() + (size_t)pl->N * 8);
   for (int32_t r = 0; r < pl->N; ++r) stab[r] = shards[r];
   for (int32_t p = 0; p < pl->P; ++p) ptab[p] = params[p];
-  cudaStream_t s = (cudaStream_t)stream;
   if ((st = commit_table(pl, TABLE_AG, ag_table_bytes(pl), s, &slot)) != TIDE_OK) return st;
 
   AgArgs a;

@@ -214,6 +214,7 @@ struct tide_plan {
   int64_t rd_n_items[kMaxRounds] = {};
   int64_t rd_n_units[kMaxRounds] = {};
   int32_t rd_exchange = 0;                 // 0: copy engines, 1: SM kernel
+  bool ag_copy_engines = false;            // TIDE_OPT_AG_COPY_ENGINES
   static constexpr int kRing = 8;
   struct Slot {
     unsigned char* host = nullptr;

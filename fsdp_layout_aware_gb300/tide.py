@@ -34,6 +34,7 @@ TIDE_OPT_AG_UNPADDED = 6
 TIDE_OPT_SUM_ORDER = 7
 TIDE_OPT_CHECK_OVERLAP = 8
 TIDE_OPT_RD_EXCHANGE = 9
+TIDE_OPT_AG_COPY_ENGINES = 10
 TIDE_SUM_LANDING = 0
 TIDE_SUM_RELATIVE = 1
 ITEM_FIELDS = ("kind", "p", "r", "src_off", "dst_off", "n")

@@ -188,11 +188,16 @@ typedef enum tide_option {
                                   another output (INVALID_ARG, naming the
                                   pair); costs O(n log n) host time in the
                                   number of pointers; default 0 */
-  TIDE_OPT_RD_EXCHANGE = 9     /* tide_ag_rd_exchange's copies: 0 (default)
+  TIDE_OPT_RD_EXCHANGE = 9,    /* tide_ag_rd_exchange's copies: 0 (default)
                                   one copy-engine copy per node per round, as
                                   the pages' transport; 1 one SM kernel launch
                                   per round over all M copies (same bytes,
                                   same result) */
+  TIDE_OPT_AG_COPY_ENGINES = 10 /* 1: tide_ag_place issues one copy-engine
+                                  copy per (parameter, rank) piece instead of
+                                  the SM kernel -- the pages' SM-free
+                                  transport ([Richland] "What shipped"); same
+                                  result, N*P host calls per call; default 0 */
 } tide_option;
 
 /* Orders for TIDE_OPT_SUM_ORDER.  The pages do not say in which order the

@@ -219,7 +219,8 @@ def test_plan_options_validate_without_a_gpu():
         plan.check()   # never ran on a device: nothing to report
         for opt, val in [(tide.TIDE_OPT_RS_KERNEL, 2), (tide.TIDE_OPT_WAIT_LIMIT_NS, 0),
                          (tide.TIDE_OPT_TEST_DROP_TILE, -2), (tide.TIDE_OPT_SUM_ORDER, 2),
-                         (tide.TIDE_OPT_RD_EXCHANGE, 2), (tide.TIDE_OPT_CHECK_OVERLAP, 3), (99, 0)]:
+                         (tide.TIDE_OPT_RD_EXCHANGE, 2), (tide.TIDE_OPT_CHECK_OVERLAP, 3),
+                         (tide.TIDE_OPT_AG_COPY_ENGINES, -1), (99, 0)]:
             with pytest.raises(tide.TideError) as err:
                 plan.set_option(opt, val)
             assert err.value.status == 1

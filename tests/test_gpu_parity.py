@@ -529,3 +529,29 @@ def test_overlap_check_on_real_buffers():
             with pytest.raises(tide.TideError) as err:
                 plan.rs_reduce(flat, [inside] + outs[1:])
             assert err.value.status == 1
+
+
+@pytest.mark.parametrize("w", [SMALL[0], SMALL[1], SMALL[4], SMALL[5]], ids=lambda w: w.name)
+@pytest.mark.parametrize("unpadded", [0, 1], ids=["padded", "unpadded"])
+@pytest.mark.parametrize("elem_bytes", [2, 4])
+def test_ag_on_copy_engines(w, unpadded, elem_bytes):
+    """TIDE_OPT_AG_COPY_ENGINES: one copy-engine copy per piece lands every
+    piece exactly where the kernel does (padded and unpadded layouts)."""
+    geo = O.geometry(w.shapes, w.N)
+    rng = np.random.default_rng(29)
+    dt, tdt = (np.uint16, torch.int16) if elem_bytes == 2 else (np.uint32, torch.int32)
+    shards_h = [rng.integers(0, np.iinfo(dt).max, geo.S, dtype=dt) for _ in range(w.N)]
+    expect = O.ag_place_unpadded(geo, shards_h) if unpadded else O.ag_place(geo, shards_h)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        plan.set_option(tide.TIDE_OPT_AG_COPY_ENGINES, 1)
+        plan.set_option(tide.TIDE_OPT_AG_UNPADDED, unpadded)
+        shards = [torch.from_numpy(x.view(np.int16 if elem_bytes == 2 else np.int32)).to(DEV) for x in shards_h]
+        sizes = [e.size for e in expect]
+        backs = [torch.full((GUARD + n + GUARD,), -3, dtype=tdt, device=DEV) for n in sizes]
+        params = [b[GUARD:GUARD + n] for b, n in zip(backs, sizes)]
+        plan.ag_place(shards, params, elem_bytes)
+        torch.cuda.synchronize()
+        for p in range(w.P):
+            assert np.array_equal(params[p].cpu().numpy().view(dt), expect[p]), p
+            g = backs[p].cpu().numpy()
+            assert (g[:GUARD] == -3).all() and (g[GUARD + sizes[p]:] == -3).all()
