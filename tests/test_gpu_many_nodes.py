@@ -220,3 +220,34 @@ def test_ag_many_ranks_bit_exact(w):
             got = params[p][1].cpu().numpy().view(np.uint16)
             assert np.array_equal(got[GUARD:GUARD + w.N * geo.e[p]], expect[p]), p
             assert (got[:GUARD] == 0x1234).all() and (got[GUARD + w.N * geo.e[p]:] == 0x1234).all()
+
+
+def test_full_size_relative_order_sampled():
+    """The wan22dit group at full size (M = L = 8, where the two level-2
+    readings give different bits) under TIDE_SUM_RELATIVE: sampled outputs
+    against the oracle computed one element at a time in that order, and at
+    least one sample where the landing order would differ."""
+    from gpu_common import device_grads
+    w = configs.get(4)
+    geo = O.geometry(w.shapes, w.N)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        plan.set_option(tide.TIDE_OPT_SUM_ORDER, tide.TIDE_SUM_RELATIVE)
+        grads = device_grads(w)
+        shards = [torch.empty(geo.S, dtype=torch.float32, device=DEV) for _ in range(w.N)]
+        plan.rs_reduce(tide.pointer_array([grads[r][p] for r in range(w.N) for p in range(w.P)]),
+                       tide.pointer_array(shards))
+        torch.cuda.synchronize()
+
+        def grad_at(src, p, idx):
+            return w.grad_values(src, p, idx.astype(np.uint64))
+
+        rng = np.random.default_rng(44)
+        differs = 0
+        for r, x in zip(rng.integers(0, w.N, 800).tolist(), rng.integers(0, geo.S, 800).tolist()):
+            want = O.rs_element(geo, w.M, w.L, r, x, grad_at, O.RELATIVE)
+            got = np.float32(shards[r][x].item())
+            assert got.view(np.uint32) == np.float32(want).view(np.uint32), (r, x, got, want)
+            differs += np.float32(O.rs_element(geo, w.M, w.L, r, x, grad_at)).view(np.uint32) != got.view(np.uint32)
+        assert differs > 0
+        del grads, shards
+    torch.cuda.empty_cache()
