@@ -612,9 +612,11 @@ def run_variants(args, local_rank):
     plan.set_option(tide.TIDE_OPT_AG_UNPADDED, 1)
     timed("ag_unpadded", lambda: plan.ag_place(ap, pp, 2, stream), 4 * G)
     plan.set_option(tide.TIDE_OPT_AG_UNPADDED, 0)
-    plan.set_option(tide.TIDE_OPT_AG_COPY_ENGINES, 1)
-    timed("ag_copy_engines", lambda: plan.ag_place(ap, pp, 2, stream), nb["ag_bytes"])
-    plan.set_option(tide.TIDE_OPT_AG_COPY_ENGINES, 0)
+    for name, transport in (("ag_copy_engines", tide.TIDE_AG_COPY_ENGINES), ("ag_bulk", tide.TIDE_AG_BULK)):
+        plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, transport)
+        timed(name, lambda: plan.ag_place(ap, pp, 2, stream), nb["ag_bytes"])
+    plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, tide.TIDE_AG_SM)
+    timed("ag_sm", lambda: plan.ag_place(ap, pp, 2, stream), nb["ag_bytes"])
     del params, pp
     # Slot-Reuse: every rank's slot is its N*S-element all-gather destination
     slots = [torch.empty(N * S, dtype=torch.int16, device=dev) for _ in range(N)]

@@ -35,9 +35,10 @@ CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler",
 LIBS = {
     "tide": {
         "out": os.path.join(HERE, "libtide.so"),
-        "srcs": [os.path.join(HERE, "csrc", f) for f in ("plan.cpp", "runtime.cu", "rs_kernel.cu", "rs_bulk.cu", "rs_staged.cu", "ag_kernel.cu",
+        "srcs": [os.path.join(HERE, "csrc", f) for f in ("plan.cpp", "runtime.cu", "rs_kernel.cu", "rs_bulk.cu",
+                                                              "rs_staged.cu", "ag_kernel.cu", "ag_bulk.cu",
                                                               "rs_noalloc.cu")],
-        "deps": [os.path.join(HERE, "csrc", f) for f in ("tide_internal.h", "rs_device.cuh")] +
+        "deps": [os.path.join(HERE, "csrc", f) for f in ("tide_internal.h", "rs_device.cuh", "bulk_ptx.cuh")] +
                 [os.path.join(ROOT, "include", "tide.h")],
         "build": os.path.join(HERE, "_build"),
     },

@@ -103,6 +103,31 @@ void build_rs_items(tide_plan* pl) {
   }
 }
 
+// Split every all-gather item for the bulk-copy transport, for bf16 pieces
+// and 16-byte aligned base pointers: an item whose source and destination
+// byte offsets differ mod 16 stays whole on the SM kernel; otherwise its head
+// (up to the destination's next 16-byte boundary) and tail (below 16 bytes)
+// go to the SM kernel and the aligned middle to bulk copies, in chunks of at
+// most kAgBulkChunkElems elements.
+void build_ag_bulk_items(tide_plan* pl) {
+  for (const AgItem& it : pl->ag_items) {
+    const int64_t sb = 2 * it.src_off, db = 2 * it.dst_off;
+    if ((sb - db) % 16 != 0) {
+      pl->ag_rest_items.push_back(it);
+      continue;
+    }
+    const int64_t head = std::min<int64_t>(it.n, ((16 - db % 16) % 16) / 2);
+    const int64_t mid = (it.n - head) / 8 * 8;
+    if (head > 0) pl->ag_rest_items.push_back(AgItem{it.src_off, it.dst_off, (int32_t)head, it.p, it.r, 0});
+    for (int64_t c = 0; c < mid; c += kAgBulkChunkElems)
+      pl->ag_bulk_items.push_back(AgItem{it.src_off + head + c, it.dst_off + head + c,
+                                         (int32_t)std::min<int64_t>(kAgBulkChunkElems, mid - c), it.p, it.r, 0});
+    if (head + mid < it.n)
+      pl->ag_rest_items.push_back(AgItem{it.src_off + head + mid, it.dst_off + head + mid,
+                                         (int32_t)(it.n - head - mid), it.p, it.r, 0});
+  }
+}
+
 void build_ag_items(tide_plan* pl) {
   const int64_t chunk = kAgChunkBytes / 2;  // elements; 64 KiB of bf16
   for (int32_t p = 0; p < pl->P; ++p) {
@@ -290,6 +315,7 @@ tide_status tide_plan_create(const tide_group_desc* d, tide_plan** out_plan) {
     build_order_table(pl);
     build_rs_items(pl);
     build_ag_items(pl);
+    build_ag_bulk_items(pl);
     build_variant_items(pl);
     build_prefixes(pl);
   } catch (const std::bad_alloc&) {
@@ -340,6 +366,8 @@ int64_t tide_plan_num_items(const tide_plan* pl, int32_t which) {
   if (!pl) return -1;
   if (which == 0) return (int64_t)pl->rs_items.size();
   if (which == 1) return (int64_t)pl->ag_items.size();
+  if (which == 2) return (int64_t)pl->ag_bulk_items.size();
+  if (which == 3) return (int64_t)pl->ag_rest_items.size();
   return -1;
 }
 
@@ -355,16 +383,17 @@ tide_status tide_plan_get_items(const tide_plan* pl, int32_t which, int64_t* out
     }
     return TIDE_OK;
   }
-  if (which == 1) {
-    const int64_t n = std::min<int64_t>(cap, (int64_t)pl->ag_items.size());
+  if (which >= 1 && which <= 3) {
+    const std::vector<AgItem>& v = which == 1 ? pl->ag_items : which == 2 ? pl->ag_bulk_items : pl->ag_rest_items;
+    const int64_t n = std::min<int64_t>(cap, (int64_t)v.size());
     for (int64_t i = 0; i < n; ++i) {
-      const AgItem& it = pl->ag_items[i];
+      const AgItem& it = v[i];
       int64_t* o = out + 6 * i;
       o[0] = AG_COPY; o[1] = it.p; o[2] = it.r; o[3] = it.src_off; o[4] = it.dst_off; o[5] = it.n;
     }
     return TIDE_OK;
   }
-  return fail(TIDE_ERR_INVALID_ARG, "which must be 0 (RS) or 1 (AG)");
+  return fail(TIDE_ERR_INVALID_ARG, "which must be 0 (RS), 1 (AG), 2 or 3 (bulk AG split)");
 }
 
 }  // extern "C"

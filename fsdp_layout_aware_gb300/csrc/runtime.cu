@@ -73,6 +73,12 @@ void release_device_state(tide_plan* pl) {
   pl->d_status = nullptr;
   for (void* q : {(void*)pl->d_agu_items, (void*)pl->d_agu_units, (void*)pl->d_pack_items, (void*)pl->d_pack_units})
     if (q) cudaFree(q);
+  for (void* q : {(void*)pl->d_agb_items, (void*)pl->d_agr_items, (void*)pl->d_agr_units})
+    if (q) cudaFree(q);
+  pl->d_agb_items = pl->d_agr_items = nullptr;
+  pl->d_agr_units = nullptr;
+  pl->agb_n_items = pl->agr_n_items = pl->agr_units = 0;
+  pl->ag_bulk_ok = false;
   pl->d_agu_items = nullptr;
   pl->d_agu_units = nullptr;
   pl->d_pack_items = nullptr;
@@ -222,6 +228,29 @@ tide_status ensure_device(tide_plan* pl) {
       if ((err = upload(v, &pl->d_rd_items[d], &pl->d_rd_units[d], &pl->rd_n_units[d])) != cudaSuccess)
         return bail(err, "uploading the exchange rounds");
     }
+    // Bulk-copy all-gather lists, for bf16 and 16-byte aligned base pointers.
+    {
+      int optin = 0;
+      if ((err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+        return bail(err, "cudaDeviceGetAttribute(smem)");
+      pl->ag_bulk_ok = optin >= ag_bulk_smem_bytes();
+      if (pl->ag_bulk_ok && (err = (cudaError_t)ag_bulk_setup()) != cudaSuccess)
+        return bail(err, "cudaFuncSetAttribute(ag_bulk)");
+    }
+    if (pl->ag_bulk_ok) {
+      const std::vector<AgItem>& bulk = pl->ag_bulk_items;
+      pl->agb_n_items = (int64_t)bulk.size();
+      pl->agr_n_items = (int64_t)pl->ag_rest_items.size();
+      if (!bulk.empty()) {
+        if ((err = cudaMalloc(&pl->d_agb_items, bulk.size() * sizeof(AgItem))) != cudaSuccess)
+          return bail(err, "cudaMalloc(bulk all-gather items)");
+        if ((err = cudaMemcpy(pl->d_agb_items, bulk.data(), bulk.size() * sizeof(AgItem),
+                              cudaMemcpyHostToDevice)) != cudaSuccess)
+          return bail(err, "cudaMemcpy(bulk all-gather items)");
+      }
+      if ((err = upload(pl->ag_rest_items, &pl->d_agr_items, &pl->d_agr_units, &pl->agr_units)) != cudaSuccess)
+        return bail(err, "uploading the bulk all-gather's remainder");
+    }
     if ((err = cudaMalloc(&pl->d_ag_units, au.size() * sizeof(UnitStart))) != cudaSuccess)
       return bail(err, "cudaMalloc(ag units)");
     if ((err = cudaMemcpy(pl->d_ag_units, au.data(), au.size() * sizeof(UnitStart), cudaMemcpyHostToDevice)) !=
@@ -361,9 +390,10 @@ tide_status tide_plan_set_option(tide_plan* pl, int32_t option, int64_t value) {
       pl->sum_order = (int32_t)value;
       build_order_table(pl);  // read by every later call (passed by value at launch)
       return TIDE_OK;
-    case TIDE_OPT_AG_COPY_ENGINES:
-      if (value != 0 && value != 1) return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_AG_COPY_ENGINES must be 0 or 1");
-      pl->ag_copy_engines = value != 0;
+    case TIDE_OPT_AG_TRANSPORT:
+      if (value != TIDE_AG_SM && value != TIDE_AG_COPY_ENGINES && value != TIDE_AG_BULK)
+        return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_AG_TRANSPORT must be a tide_ag_transport");
+      pl->ag_transport = (int32_t)value;
       return TIDE_OK;
     case TIDE_OPT_RD_EXCHANGE:
       if (value != 0 && value != 1) return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_RD_EXCHANGE must be 0 or 1");
@@ -576,7 +606,7 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
     if (st != TIDE_OK) return st;
   }
   cudaStream_t s = (cudaStream_t)stream;
-  if (pl->ag_copy_engines) {
+  if (pl->ag_transport == TIDE_AG_COPY_ENGINES) {
     // The pages' transport: one copy-engine copy per (parameter, rank) piece,
     // straight to its final address; no kernel, no device state.
     for (int32_t p = 0; p < pl->P; ++p) {
@@ -601,6 +631,36 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
   for (int32_t r = 0; r < pl->N; ++r) stab[r] = shards[r];
   for (int32_t p = 0; p < pl->P; ++p) ptab[p] = params[p];
   if ((st = commit_table(pl, TABLE_AG, ag_table_bytes(pl), s, &slot)) != TIDE_OK) return st;
+
+  bool bulk = pl->ag_transport == TIDE_AG_BULK && pl->ag_bulk_ok && elem_bytes == 2 && !pl->ag_unpadded;
+  for (int32_t r = 0; bulk && r < pl->N; ++r) bulk = ((uintptr_t)shards[r] & 15) == 0;
+  for (int32_t p = 0; bulk && p < pl->P; ++p) bulk = pl->e[p] == 0 || ((uintptr_t)params[p] & 15) == 0;
+  if (bulk) {
+    // Remainder (heads, tails, phase-mismatched pieces) on the SM kernel,
+    // then the aligned middles by bulk copies; disjoint bytes, any order.
+    if (pl->agr_n_items > 0) {
+      AgArgs r;
+      r.items = pl->d_agr_items;
+      r.n_items = pl->agr_n_items;
+      r.units = pl->d_agr_units;
+      r.n_units = pl->agr_units;
+      r.shard_tab = (const unsigned char* const*)slot->dev;
+      r.param_tab = (unsigned char* const*)(slot->dev + (size_t)pl->N * 8);
+      r.elem_bytes = 2;
+      const int lerr = launch_ag(r, pl->ag_grid, stream);
+      if (lerr != cudaSuccess) return cuda_fail((cudaError_t)lerr, "ag_place (remainder) launch");
+    }
+    if (pl->agb_n_items == 0) return finish(slot, cudaSuccess, s, "bulk all-gather");
+    AgBulkArgs b;
+    b.items = pl->d_agb_items;
+    b.n_items = pl->agb_n_items;
+    b.shard_tab = (const unsigned char* const*)slot->dev;
+    b.param_tab = (unsigned char* const*)(slot->dev + (size_t)pl->N * 8);
+    b.status = pl->d_status;
+    b.wait_limit_ns = pl->wait_limit_ns;
+    const int grid = (int)std::min<int64_t>(pl->num_sms, pl->agb_n_items);
+    return finish(slot, launch_ag_bulk(b, grid, stream), s, "bulk all-gather launch");
+  }
 
   AgArgs a;
   if (pl->ag_unpadded) {

@@ -138,6 +138,18 @@ struct RsArgs {
   uint8_t order[kOrderTableSize];
 };
 
+// Bulk-copy all-gather (ag_bulk.cu): the aligned middles of the bf16 pieces
+// in chunks of at most kAgBulkChunkElems elements.
+constexpr int64_t kAgBulkChunkElems = 16384;
+struct AgBulkArgs {
+  const AgItem* items;              // chunks: 16-byte aligned at both ends
+  int64_t n_items;
+  const unsigned char* const* shard_tab;  // [N]
+  unsigned char* const* param_tab;        // [P]
+  int* status;                      // TIDE_DEVICE_TIMEOUT on a wait that ran out
+  uint64_t wait_limit_ns;
+};
+
 struct AgArgs {
   const AgItem* items;
   int64_t n_items;
@@ -151,6 +163,9 @@ struct AgArgs {
 // Launchers (rs_kernel.cu / ag_kernel.cu).  Return the cudaError_t as int.
 int launch_rs(const RsArgs& args, int grid, void* stream);
 int launch_ag(const AgArgs& args, int grid, void* stream);
+int launch_ag_bulk(const AgBulkArgs& args, int grid, void* stream);
+int ag_bulk_setup();       // raises the bulk all-gather's dynamic shared-memory limit
+int ag_bulk_smem_bytes();
 int launch_rs_bulk(const RsArgs& args, int grid, void* stream);
 int launch_rs_staged(const RsArgs& args, int sum_grid, int land_grid_x, void* stream);
 BulkLayout rs_bulk_layout(int N, int M, int L, int smem_budget);
@@ -168,7 +183,10 @@ struct tide_plan {
   int64_t S = 0;
   std::vector<tide::RsItem> rs_items;
   std::vector<tide::AgItem> ag_items;
-  std::vector<tide::AgItem> ag_items_unpadded;  // ag_items restricted to real rows
+  std::vector<tide::AgItem> ag_items_unpadded;
+  // Bulk-copy all-gather split of ag_items (bf16, 16-byte aligned bases):
+  // the aligned middles in chunks of at most kAgBulkChunkElems, and the rest.
+  std::vector<tide::AgItem> ag_bulk_items, ag_rest_items;  // ag_items restricted to real rows
   std::vector<tide::AgItem> pack_items;         // Slot-Reuse: r = grad index r*P+p, p = slot rank
   std::vector<const void*> slot_grads;          // tide_rs_reduce_slots' pointer array (host)
   std::vector<int64_t> ag_prefix;  // all-gather cost prefix sums (load balance)
@@ -214,7 +232,17 @@ struct tide_plan {
   int64_t rd_n_items[kMaxRounds] = {};
   int64_t rd_n_units[kMaxRounds] = {};
   int32_t rd_exchange = 0;                 // 0: copy engines, 1: SM kernel
-  bool ag_copy_engines = false;            // TIDE_OPT_AG_COPY_ENGINES
+  int32_t ag_transport = 0;                // TIDE_OPT_AG_TRANSPORT (tide_ag_transport)
+  // Bulk-copy all-gather lists (bf16, base pointers 16-byte aligned): chunks
+  // of the pieces' aligned middles, and the rest (heads, tails, pieces whose
+  // source and destination differ in phase) for ag_place_kernel.
+  tide::AgItem* d_agb_items = nullptr;
+  int64_t agb_n_items = 0;
+  tide::AgItem* d_agr_items = nullptr;
+  tide::UnitStart* d_agr_units = nullptr;
+  int64_t agr_n_items = 0;
+  int64_t agr_units = 0;
+  bool ag_bulk_ok = false;                 // the device has the shared memory for it
   static constexpr int kRing = 8;
   struct Slot {
     unsigned char* host = nullptr;

@@ -34,7 +34,10 @@ TIDE_OPT_AG_UNPADDED = 6
 TIDE_OPT_SUM_ORDER = 7
 TIDE_OPT_CHECK_OVERLAP = 8
 TIDE_OPT_RD_EXCHANGE = 9
-TIDE_OPT_AG_COPY_ENGINES = 10
+TIDE_OPT_AG_TRANSPORT = 10
+TIDE_AG_SM = 0
+TIDE_AG_COPY_ENGINES = 1
+TIDE_AG_BULK = 2
 TIDE_SUM_LANDING = 0
 TIDE_SUM_RELATIVE = 1
 ITEM_FIELDS = ("kind", "p", "r", "src_off", "dst_off", "n")
@@ -228,7 +231,8 @@ def tide_plan_level2_order(plan, n_dest, s, M):
 
 
 def tide_plan_items(plan, which):
-    """Work list as a list of dicts (which=0: reduce-scatter, 1: all-gather)."""
+    """Work list as a list of dicts (which=0: reduce-scatter, 1: all-gather,
+    2 / 3: the all-gather split for bulk copies: aligned middles / the rest)."""
     n = int(_lib.tide_plan_num_items(plan, which))
     if n < 0:
         raise TideError(1, "bad plan or list selector")

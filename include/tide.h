@@ -118,13 +118,16 @@ tide_status tide_plan_param_geometry(const tide_plan* plan, int32_t p, int64_t* 
                                      int64_t* Rp, int64_t* Kp, int64_t* op);
 
 /* Work-list introspection for tests.  which = 0: reduce-scatter items,
- * which = 1: all-gather items.  Each item is 6 int64 values
+ * which = 1: all-gather items, which = 2 / 3: the all-gather items as the
+ * TIDE_AG_BULK transport splits them (2: the 16-byte aligned middles it moves
+ * by bulk copies, 3: the rest, moved by the SM kernel; bf16 offsets, base
+ * pointers assumed 16-byte aligned).  Each item is 6 int64 values
  * {kind, p, r, src_off, dst_off, n}:
  *   RS: kind 0 = reduce valid rows, 1 = zero padding; src_off is the element
  *       offset inside every contributor's gradient of p, dst_off the offset
  *       inside rank r's packed shard, n the element count; one level-2 slice.
- *   AG: kind 2; src_off inside rank r's packed shard, dst_off inside
- *       parameter p's gathered block.
+ *   AG (which 1..3): kind 2; src_off inside rank r's packed shard, dst_off
+ *       inside parameter p's gathered block.
  * tide_plan_num_items returns the count (-1 for a bad plan/which);
  * tide_plan_get_items copies min(cap, count) items to out. */
 int64_t tide_plan_num_items(const tide_plan* plan, int32_t which);
@@ -153,7 +156,7 @@ tide_status tide_plan_level2_order(const tide_plan* plan, int32_t n_dest, int32_
  *                          window, so it suits groups with few ranks; it
  *                          takes at most 8 nodes (UNIMPLEMENTED beyond).
  *   TIDE_OPT_WAIT_LIMIT_NS bound, in nanoseconds, on every wait inside the
- *                          bulk-copy kernel (default 2e9).  A kernel that runs
+ *                          bulk-copy kernels (default 2e9).  A kernel that runs
  *                          out records TIDE_ERR_TIMEOUT for tide_plan_check,
  *                          drains its copies and returns; the outputs of that
  *                          call are then undefined.
@@ -193,12 +196,29 @@ typedef enum tide_option {
                                   the pages' transport; 1 one SM kernel launch
                                   per round over all M copies (same bytes,
                                   same result) */
-  TIDE_OPT_AG_COPY_ENGINES = 10 /* 1: tide_ag_place issues one copy-engine
-                                  copy per (parameter, rank) piece instead of
-                                  the SM kernel -- the pages' SM-free
-                                  transport ([Richland] "What shipped"); same
-                                  result, N*P host calls per call; default 0 */
+  TIDE_OPT_AG_TRANSPORT = 10   /* how tide_ag_place moves the pieces, a
+                                  tide_ag_transport (default TIDE_AG_SM) */
 } tide_option;
+
+/* Transports for TIDE_OPT_AG_TRANSPORT; all give the same result.  The pages'
+ * all-gather uses no SM threads ([Richland] "What shipped").
+ *   TIDE_AG_SM            (default) one kernel over the work list, every
+ *                         thread copying 16-byte words;
+ *   TIDE_AG_COPY_ENGINES  one copy-engine copy per (parameter, rank) piece:
+ *                         no kernel, N*P host calls per call;
+ *   TIDE_AG_BULK          bf16 only: one thread per SM moves each piece's
+ *                         16-byte aligned middle global -> shared -> global
+ *                         with bulk copies (TMA), the SM kernel the rest.
+ *                         Needs every shard and parameter pointer 16-byte
+ *                         aligned and the padded layout; otherwise, and for
+ *                         4-byte elements, the call uses TIDE_AG_SM.  Its
+ *                         waits are bounded by TIDE_OPT_WAIT_LIMIT_NS
+ *                         (TIDE_ERR_TIMEOUT from tide_plan_check). */
+typedef enum tide_ag_transport {
+  TIDE_AG_SM = 0,
+  TIDE_AG_COPY_ENGINES = 1,
+  TIDE_AG_BULK = 2
+} tide_ag_transport;
 
 /* Orders for TIDE_OPT_SUM_ORDER.  The pages do not say in which order the
  * NVSwitch read-and-add combines the partials ([Endgame] "Reduce-scatter:

@@ -220,7 +220,7 @@ def test_plan_options_validate_without_a_gpu():
         for opt, val in [(tide.TIDE_OPT_RS_KERNEL, 2), (tide.TIDE_OPT_WAIT_LIMIT_NS, 0),
                          (tide.TIDE_OPT_TEST_DROP_TILE, -2), (tide.TIDE_OPT_SUM_ORDER, 2),
                          (tide.TIDE_OPT_RD_EXCHANGE, 2), (tide.TIDE_OPT_CHECK_OVERLAP, 3),
-                         (tide.TIDE_OPT_AG_COPY_ENGINES, -1), (99, 0)]:
+                         (tide.TIDE_OPT_AG_TRANSPORT, 3), (99, 0)]:
             with pytest.raises(tide.TideError) as err:
                 plan.set_option(opt, val)
             assert err.value.status == 1
@@ -341,3 +341,51 @@ def test_overlap_check_lets_disjoint_and_shared_inputs_through():
         params = [ag_in[0] - 10 * 64 * 2, 0x9000000, 0x9100000]
         st, _ = _overlap_status(lambda: plan.ag_place(ag_in, params, 2, stream=0))
         assert st == 5
+
+
+def _check_ag_bulk_split(plan, geo, N):
+    """The bulk-copy transport's split of the all-gather work: every chunk is
+    16-byte aligned at both ends (with 16-byte aligned bases), a multiple of
+    16 bytes, at most 32 KiB and inside its shard and block; chunks and the
+    rest tile every all-gather item exactly once."""
+    hits = {}
+    for which in (2, 3):
+        for it in plan.items(which):
+            p, r, n, so, do = it["p"], it["r"], it["n"], it["src_off"], it["dst_off"]
+            assert n > 0 and 0 <= so and so + n <= geo.S and 0 <= do and do + n <= N * geo.e[p]
+            assert do - r * geo.e[p] == so - geo.o[p]          # the direct-landing map
+            if which == 2:
+                assert (2 * so) % 16 == 0 and (2 * do) % 16 == 0 and (2 * n) % 16 == 0 and 2 * n <= 32768
+            for y in range(do, do + n):
+                hits[(p, y)] = hits.get((p, y), 0) + 1
+    assert all(h == 1 for h in hits.values())
+    assert sum(hits.values()) == N * geo.S
+
+
+@pytest.mark.parametrize("shapes,M,L", GROUPS)
+def test_ag_bulk_split_small_groups(shapes, M, L):
+    N = M * L
+    geo = O.geometry(shapes, N)
+    with tide.TidePlan(shapes, N, M, L) as plan:
+        _check_ag_bulk_split(plan, geo, N)
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+def test_ag_bulk_split_workloads(cfg):
+    """Full-size groups, checked by counting instead of element by element."""
+    w = configs.get(cfg)
+    geo = O.geometry(w.shapes, w.N)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        bulk, rest = plan.items(2), plan.items(3)
+        total = 0
+        for it in bulk:
+            assert (2 * it["src_off"]) % 16 == 0 and (2 * it["dst_off"]) % 16 == 0
+            assert (2 * it["n"]) % 16 == 0 and 0 < 2 * it["n"] <= 32768
+            assert it["src_off"] + it["n"] <= geo.S and it["dst_off"] + it["n"] <= w.N * geo.e[it["p"]]
+            total += it["n"]
+        for it in rest:
+            assert it["n"] > 0 and it["src_off"] + it["n"] <= geo.S
+            total += it["n"]
+        assert total == w.N * geo.S
+        if cfg in (2, 3, 4):          # even row lengths throughout: nearly everything goes by bulk copy
+            assert sum(it["n"] for it in rest) < 0.01 * total

@@ -531,27 +531,60 @@ def test_overlap_check_on_real_buffers():
             assert err.value.status == 1
 
 
-@pytest.mark.parametrize("w", [SMALL[0], SMALL[1], SMALL[4], SMALL[5]], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [SMALL[0], SMALL[1], SMALL[2], SMALL[4], SMALL[5], SMALL[6]], ids=lambda w: w.name)
 @pytest.mark.parametrize("unpadded", [0, 1], ids=["padded", "unpadded"])
 @pytest.mark.parametrize("elem_bytes", [2, 4])
-def test_ag_on_copy_engines(w, unpadded, elem_bytes):
-    """TIDE_OPT_AG_COPY_ENGINES: one copy-engine copy per piece lands every
-    piece exactly where the kernel does (padded and unpadded layouts)."""
+@pytest.mark.parametrize("transport", ["copy_engines", "bulk"])
+def test_ag_other_transports(w, unpadded, elem_bytes, transport):
+    """TIDE_OPT_AG_TRANSPORT: copy-engine copies per piece, or bulk copies of
+    the aligned middles plus the SM kernel for the rest, land every piece
+    exactly where the kernel does (combinations the bulk transport does not
+    take fall back to the kernel and must be exact too)."""
     geo = O.geometry(w.shapes, w.N)
     rng = np.random.default_rng(29)
     dt, tdt = (np.uint16, torch.int16) if elem_bytes == 2 else (np.uint32, torch.int32)
     shards_h = [rng.integers(0, np.iinfo(dt).max, geo.S, dtype=dt) for _ in range(w.N)]
     expect = O.ag_place_unpadded(geo, shards_h) if unpadded else O.ag_place(geo, shards_h)
     with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
-        plan.set_option(tide.TIDE_OPT_AG_COPY_ENGINES, 1)
+        plan.set_option(tide.TIDE_OPT_AG_TRANSPORT,
+                        tide.TIDE_AG_COPY_ENGINES if transport == "copy_engines" else tide.TIDE_AG_BULK)
         plan.set_option(tide.TIDE_OPT_AG_UNPADDED, unpadded)
         shards = [torch.from_numpy(x.view(np.int16 if elem_bytes == 2 else np.int32)).to(DEV) for x in shards_h]
         sizes = [e.size for e in expect]
-        backs = [torch.full((GUARD + n + GUARD,), -3, dtype=tdt, device=DEV) for n in sizes]
-        params = [b[GUARD:GUARD + n] for b, n in zip(backs, sizes)]
+        lead = 40  # elements before each block: 80 or 160 bytes, so the blocks stay 16-byte aligned
+        backs = [torch.full((lead + n + GUARD,), -3, dtype=tdt, device=DEV) for n in sizes]
+        params = [b[lead:lead + n] for b, n in zip(backs, sizes)]
         plan.ag_place(shards, params, elem_bytes)
-        torch.cuda.synchronize()
+        plan.check()
         for p in range(w.P):
             assert np.array_equal(params[p].cpu().numpy().view(dt), expect[p]), p
             g = backs[p].cpu().numpy()
-            assert (g[:GUARD] == -3).all() and (g[GUARD + sizes[p]:] == -3).all()
+            assert (g[:lead] == -3).all() and (g[lead + sizes[p]:] == -3).all()
+
+
+@pytest.mark.parametrize("w", [SMALL[1], SMALL[2], SMALL[4], SMALL[5]], ids=lambda w: w.name)
+@pytest.mark.parametrize("shift", [0, 4, 1], ids=["aligned", "shifted_8B", "shifted_2B"])
+def test_ag_bulk_transport_alignment(w, shift):
+    """The bulk transport with parameter blocks 16-byte aligned (bulk copies),
+    8 bytes off (the kernel takes every piece: a base is not 16-byte aligned)
+    and 2 bytes off; repeated calls reuse the table; every byte exact."""
+    geo = O.geometry(w.shapes, w.N)
+    rng = np.random.default_rng(31)
+    shards_h = [rng.integers(0, 65535, geo.S, dtype=np.uint16) for _ in range(w.N)]
+    expect = O.ag_place(geo, shards_h)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, tide.TIDE_AG_BULK)
+        shards = [to_dev_u16(x)[0] for x in shards_h]
+        lead = 40 + shift  # 40 bf16 = 80 bytes keeps the block 16-byte aligned; shift moves it off
+        outs = [to_dev_u16(np.zeros(w.N * geo.e[p], dtype=np.uint16), lead, GUARD, fill=0x5A5A)
+                for p in range(w.P)]
+        for _ in range(3):
+            for o in outs:
+                o[0].fill_(0x1111)
+            plan.ag_place(shards, [o[0] for o in outs], 2)
+            plan.check()
+            for p in range(w.P):
+                got = outs[p][1].cpu().numpy().view(np.uint16)
+                n = w.N * geo.e[p]
+                assert np.array_equal(got[lead:lead + n], expect[p]), p
+                assert (got[:lead] == 0x5A5A).all() and (got[lead + n:] == 0x5A5A).all()
