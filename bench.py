@@ -257,12 +257,15 @@ def run_ours(args, rank, world, local_rank):
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.time()
+    launches = [0, 0]  # kernels launched by the RS and AG calls (the library's own count)
     start.record(stream)
     for k in range(K):
         ev[k][0].record(stream)
         plan.rs_reduce(grads_p, rs_out_p, stream)
+        launches[0] += plan.last_launches()
         ev[k][1].record(stream)
         plan.ag_place(ag_in_p, ag_out_p, 2, stream)
+        launches[1] += plan.last_launches()
         ev[k][2].record(stream)
     stop.record(stream)
     torch.cuda.synchronize()
@@ -316,7 +319,8 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"kernel": "rs_fused", "bound": "hbm", "achieved": round(rs_gbs, 2), "peak": peak,
                      "peak_source": peak_kind, "unit": "GB/s", "frac": round(rs_gbs / peak, 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": nbytes["rs_bytes"]},
-        "gpu_launches": 2 * K,
+        "gpu_launches": launches[0] + launches[1],
+        "kernels_per_step": {"rs": launches[0] / K, "ag": launches[1] / K},
         "clocks": clocks,
         "e2e": e2e,
     }
@@ -612,11 +616,11 @@ def run_variants(args, local_rank):
     plan.set_option(tide.TIDE_OPT_AG_UNPADDED, 1)
     timed("ag_unpadded", lambda: plan.ag_place(ap, pp, 2, stream), 4 * G)
     plan.set_option(tide.TIDE_OPT_AG_UNPADDED, 0)
-    for name, transport in (("ag_copy_engines", tide.TIDE_AG_COPY_ENGINES), ("ag_bulk", tide.TIDE_AG_BULK)):
+    for name, transport in (("ag_copy_engines", tide.TIDE_AG_COPY_ENGINES), ("ag_bulk", tide.TIDE_AG_BULK),
+                            ("ag_sm", tide.TIDE_AG_SM)):
         plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, transport)
         timed(name, lambda: plan.ag_place(ap, pp, 2, stream), nb["ag_bytes"])
-    plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, tide.TIDE_AG_SM)
-    timed("ag_sm", lambda: plan.ag_place(ap, pp, 2, stream), nb["ag_bytes"])
+    plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, tide.TIDE_AG_AUTO)
     del params, pp
     # Slot-Reuse: every rank's slot is its N*S-element all-gather destination
     slots = [torch.empty(N * S, dtype=torch.int16, device=dev) for _ in range(N)]

@@ -78,6 +78,7 @@ extern "C" tide_status tide_rs_reduce_noalloc(const tide_plan* pl, const void* c
                                               void* stream) {
   clear_error();
   if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  pl->last_launches = 0;
   if (pl->rs_items.empty()) return TIDE_OK;
   const tide_status st = check_rs_call(pl, grads, shards, nullptr);
   if (st != TIDE_OK) return st;
@@ -151,5 +152,6 @@ extern "C" tide_status tide_rs_reduce_noalloc(const tide_plan* pl, const void* c
   const int grid = (int)std::min<int64_t>((int64_t)sms * occ, a.n_items);
   const int lerr = launch_rs(a, grid, stream);
   if (lerr != cudaSuccess) return cuda_status((cudaError_t)lerr, "rs_fused launch");
+  pl->last_launches = 2;  // the table kernel and rs_fused
   return TIDE_OK;
 }

@@ -391,7 +391,7 @@ tide_status tide_plan_set_option(tide_plan* pl, int32_t option, int64_t value) {
       build_order_table(pl);  // read by every later call (passed by value at launch)
       return TIDE_OK;
     case TIDE_OPT_AG_TRANSPORT:
-      if (value != TIDE_AG_SM && value != TIDE_AG_COPY_ENGINES && value != TIDE_AG_BULK)
+      if (value < TIDE_AG_AUTO || value > TIDE_AG_BULK)
         return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_AG_TRANSPORT must be a tide_ag_transport");
       pl->ag_transport = (int32_t)value;
       return TIDE_OK;
@@ -410,6 +410,8 @@ tide_status tide_plan_set_option(tide_plan* pl, int32_t option, int64_t value) {
   }
   return fail(TIDE_ERR_INVALID_ARG, "unknown option " + std::to_string(option));
 }
+
+int32_t tide_plan_last_launches(const tide_plan* pl) { return pl ? pl->last_launches : -1; }
 
 tide_status tide_plan_check(tide_plan* pl) {
   clear_error();
@@ -542,6 +544,7 @@ extern "C" {
 tide_status tide_rs_reduce(tide_plan* pl, const void* const* grads, float* const* shards, void* stream) {
   clear_error();
   if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  pl->last_launches = 0;
   if (pl->rs_items.empty()) return TIDE_OK;  // S == 0: nothing to write
   if (pl->rs_kernel == 1 && pl->M > 8)
     return fail(TIDE_ERR_UNIMPLEMENTED, "the bulk-copy kernel handles at most 8 nodes (TIDE_OPT_RS_KERNEL = 0 does)");
@@ -550,6 +553,7 @@ tide_status tide_rs_reduce(tide_plan* pl, const void* const* grads, float* const
   tide_status st = prepare_rs(pl, grads, shards, stream, &a, &slot);
   if (st != TIDE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
+  pl->last_launches = 1;
   if (pl->rs_kernel == 1) return finish(slot, launch_rs_bulk(a, pl->bulk_grid, stream), s, "rs_bulk launch");
   return finish(slot, launch_rs(a, pl->rs_grid, stream), s, "rs_fused launch");
 }
@@ -565,6 +569,7 @@ tide_status tide_rs_staged(tide_plan* pl, const void* const* grads, float* const
                            int32_t sum_ctas_per_rank, int32_t landing_ctas_per_rank, void* stream) {
   clear_error();
   if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  pl->last_launches = 0;
   if (sum_ctas_per_rank < 0 || landing_ctas_per_rank < 0) return fail(TIDE_ERR_INVALID_ARG, "negative CTA count");
   if (pl->rs_items.empty()) return TIDE_OK;
   if (!inbox) return fail(TIDE_ERR_INVALID_ARG, "inbox is NULL");
@@ -579,6 +584,7 @@ tide_status tide_rs_staged(tide_plan* pl, const void* const* grads, float* const
   const int land_per_sm = pl->M > pl->L ? 5 : 8;  // resident landing CTAs per SM (48 / 32 registers)
   const int land_x =
       landing_ctas_per_rank > 0 ? landing_ctas_per_rank : std::max(1, pl->num_sms * land_per_sm / pl->N);
+  pl->last_launches = 2;
   return finish(slot, launch_rs_staged(a, (int)sum_grid, land_x, stream), (cudaStream_t)stream, "rs_staged launch");
 }
 
@@ -586,6 +592,7 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
                           void* stream) {
   clear_error();
   if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  pl->last_launches = 0;
   if (elem_bytes != 2 && elem_bytes != 4) return fail(TIDE_ERR_INVALID_ARG, "elem_bytes must be 2 or 4");
   if (pl->ag_items.empty()) return TIDE_OK;
   if (!shards || !params) return fail(TIDE_ERR_INVALID_ARG, "shards or params array is NULL");
@@ -632,7 +639,12 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
   for (int32_t p = 0; p < pl->P; ++p) ptab[p] = params[p];
   if ((st = commit_table(pl, TABLE_AG, ag_table_bytes(pl), s, &slot)) != TIDE_OK) return st;
 
-  bool bulk = pl->ag_transport == TIDE_AG_BULK && pl->ag_bulk_ok && elem_bytes == 2 && !pl->ag_unpadded;
+  // Bulk copies when asked for, or (auto) when the SM kernel would be left at
+  // most 1/16 of the elements; the bases must allow 16-byte aligned copies.
+  const int64_t all_elems = (int64_t)pl->N * pl->S;
+  bool bulk = (pl->ag_transport == TIDE_AG_BULK ||
+               (pl->ag_transport == TIDE_AG_AUTO && pl->ag_rest_elems * 16 <= all_elems)) &&
+              pl->ag_bulk_ok && elem_bytes == 2 && !pl->ag_unpadded;
   for (int32_t r = 0; bulk && r < pl->N; ++r) bulk = ((uintptr_t)shards[r] & 15) == 0;
   for (int32_t p = 0; bulk && p < pl->P; ++p) bulk = pl->e[p] == 0 || ((uintptr_t)params[p] & 15) == 0;
   if (bulk) {
@@ -649,6 +661,7 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
       r.elem_bytes = 2;
       const int lerr = launch_ag(r, pl->ag_grid, stream);
       if (lerr != cudaSuccess) return cuda_fail((cudaError_t)lerr, "ag_place (remainder) launch");
+      pl->last_launches = 1;
     }
     if (pl->agb_n_items == 0) return finish(slot, cudaSuccess, s, "bulk all-gather");
     AgBulkArgs b;
@@ -659,6 +672,7 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
     b.status = pl->d_status;
     b.wait_limit_ns = pl->wait_limit_ns;
     const int grid = (int)std::min<int64_t>(pl->num_sms, pl->agb_n_items);
+    ++pl->last_launches;
     return finish(slot, launch_ag_bulk(b, grid, stream), s, "bulk all-gather launch");
   }
 
@@ -677,12 +691,14 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
   a.shard_tab = (const unsigned char* const*)slot->dev;
   a.param_tab = (unsigned char* const*)(slot->dev + (size_t)pl->N * 8);
   a.elem_bytes = elem_bytes;
+  pl->last_launches = 1;
   return finish(slot, launch_ag(a, pl->ag_grid, stream), s, "ag_place launch");
 }
 
 tide_status tide_slot_pack(tide_plan* pl, const void* const* grads, void* const* slots, void* stream) {
   clear_error();
   if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  pl->last_launches = 0;
   if (pl->pack_items.empty()) return TIDE_OK;
   if (!grads || !slots) return fail(TIDE_ERR_INVALID_ARG, "grads or slots array is NULL");
   for (int32_t r = 0; r < pl->N; ++r) {
@@ -720,6 +736,7 @@ tide_status tide_slot_pack(tide_plan* pl, const void* const* grads, void* const*
   a.shard_tab = (const unsigned char* const*)slot->dev;
   a.param_tab = (unsigned char* const*)(slot->dev + n_grad * 8);
   a.elem_bytes = 2;
+  pl->last_launches = 1;
   return finish(slot, launch_ag(a, pl->ag_grid, stream), s, "slot pack launch");
 }
 
@@ -738,6 +755,7 @@ tide_status tide_rs_reduce_slots(tide_plan* pl, const void* const* slots, float*
 tide_status tide_ag_rd_exchange(tide_plan* pl, void* const* stages, int32_t elem_bytes, void* stream) {
   clear_error();
   if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  pl->last_launches = 0;
   if (elem_bytes != 2 && elem_bytes != 4) return fail(TIDE_ERR_INVALID_ARG, "elem_bytes must be 2 or 4");
   if (pl->S == 0 || pl->M == 1) return TIDE_OK;
   if (!stages) return fail(TIDE_ERR_INVALID_ARG, "stages array is NULL");
@@ -770,6 +788,7 @@ tide_status tide_ag_rd_exchange(tide_plan* pl, void* const* stages, int32_t elem
       a.param_tab = (unsigned char* const*)slot->dev;
       a.elem_bytes = elem_bytes;
       const int lerr = launch_ag(a, pl->ag_grid, stream);
+      ++pl->last_launches;
       if (d + 1 < rounds && lerr != cudaSuccess) return cuda_fail((cudaError_t)lerr, "exchange launch");
       if (d + 1 == rounds) return finish(slot, lerr, s, "exchange launch");
     }
@@ -791,6 +810,7 @@ tide_status tide_ag_stage_place(tide_plan* pl, const void* stage, int32_t node, 
                                 int32_t elem_bytes, void* stream) {
   clear_error();
   if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  pl->last_launches = 0;
   if (elem_bytes != 2 && elem_bytes != 4) return fail(TIDE_ERR_INVALID_ARG, "elem_bytes must be 2 or 4");
   if (node < 0 || node >= pl->M || rail < 0 || rail >= pl->L) return fail(TIDE_ERR_INVALID_ARG, "node or rail out of range");
   if (pl->ag_items.empty()) return TIDE_OK;
@@ -831,6 +851,7 @@ tide_status tide_ag_stage_place(tide_plan* pl, const void* stage, int32_t node, 
   a.shard_tab = (const unsigned char* const*)slot->dev;
   a.param_tab = (unsigned char* const*)(slot->dev + (size_t)pl->N * 8);
   a.elem_bytes = elem_bytes;
+  pl->last_launches = 1;
   return finish(slot, launch_ag(a, pl->ag_grid, stream), s, "ag_place (stage) launch");
 }
 

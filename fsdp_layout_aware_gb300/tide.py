@@ -35,9 +35,10 @@ TIDE_OPT_SUM_ORDER = 7
 TIDE_OPT_CHECK_OVERLAP = 8
 TIDE_OPT_RD_EXCHANGE = 9
 TIDE_OPT_AG_TRANSPORT = 10
-TIDE_AG_SM = 0
-TIDE_AG_COPY_ENGINES = 1
-TIDE_AG_BULK = 2
+TIDE_AG_AUTO = 0
+TIDE_AG_SM = 1
+TIDE_AG_COPY_ENGINES = 2
+TIDE_AG_BULK = 3
 TIDE_SUM_LANDING = 0
 TIDE_SUM_RELATIVE = 1
 ITEM_FIELDS = ("kind", "p", "r", "src_off", "dst_off", "n")
@@ -74,6 +75,7 @@ def _load():
         "tide_rs_reduce_noalloc": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
         "tide_plan_set_option": (i32, [vp, i32, i64]),
         "tide_plan_check": (i32, [vp]),
+        "tide_plan_last_launches": (i32, [vp]),
         "tide_slot_pack": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
         "tide_rs_reduce_slots": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
         "tide_plan_inbox_elems": (i64, [vp]),
@@ -286,6 +288,10 @@ class TidePlan:
 
     def check(self):
         tide_plan_check(self.handle)
+
+    def last_launches(self):
+        """Kernels launched by the plan's most recent compute call."""
+        return int(_lib.tide_plan_last_launches(self.handle))
 
     def level2_order(self, n_dest, s):
         return tide_plan_level2_order(self.handle, n_dest, s, self.M)

@@ -197,13 +197,16 @@ typedef enum tide_option {
                                   per round over all M copies (same bytes,
                                   same result) */
   TIDE_OPT_AG_TRANSPORT = 10   /* how tide_ag_place moves the pieces, a
-                                  tide_ag_transport (default TIDE_AG_SM) */
+                                  tide_ag_transport (default TIDE_AG_AUTO) */
 } tide_option;
 
 /* Transports for TIDE_OPT_AG_TRANSPORT; all give the same result.  The pages'
  * all-gather uses no SM threads ([Richland] "What shipped").
- *   TIDE_AG_SM            (default) one kernel over the work list, every
- *                         thread copying 16-byte words;
+ *   TIDE_AG_AUTO          (default) TIDE_AG_BULK when the call qualifies for
+ *                         it and at most 1/16 of the group's elements are
+ *                         left to the SM kernel, else TIDE_AG_SM;
+ *   TIDE_AG_SM            one kernel over the work list, every thread
+ *                         copying 16-byte words;
  *   TIDE_AG_COPY_ENGINES  one copy-engine copy per (parameter, rank) piece:
  *                         no kernel, N*P host calls per call;
  *   TIDE_AG_BULK          bf16 only: one thread per SM moves each piece's
@@ -215,9 +218,10 @@ typedef enum tide_option {
  *                         waits are bounded by TIDE_OPT_WAIT_LIMIT_NS
  *                         (TIDE_ERR_TIMEOUT from tide_plan_check). */
 typedef enum tide_ag_transport {
-  TIDE_AG_SM = 0,
-  TIDE_AG_COPY_ENGINES = 1,
-  TIDE_AG_BULK = 2
+  TIDE_AG_AUTO = 0,
+  TIDE_AG_SM = 1,
+  TIDE_AG_COPY_ENGINES = 2,
+  TIDE_AG_BULK = 3
 } tide_ag_transport;
 
 /* Orders for TIDE_OPT_SUM_ORDER.  The pages do not say in which order the
@@ -238,6 +242,12 @@ tide_status tide_plan_set_option(tide_plan* plan, int32_t option, int64_t value)
  * (TIDE_ERR_TIMEOUT; the flag is then cleared).  TIDE_OK for a plan that has
  * not run yet.  Errors: INVALID_ARG, CUDA. */
 tide_status tide_plan_check(tide_plan* plan);
+
+/* Kernels the plan's most recent compute call launched (0 for a call that
+ * only enqueued copies or had nothing to do; tide_rs_reduce_noalloc counts
+ * its table kernel too); -1 for a NULL plan.  Host-side bookkeeping, no
+ * synchronisation. */
+int32_t tide_plan_last_launches(const tide_plan* plan);
 
 /* TIDE-RS: per-parameter bf16 gradients read in place, reduced in fp32
  * straight into every rank's packed fp32 shard at its final offset
