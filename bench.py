@@ -51,6 +51,8 @@ def parse_args(argv=None):
                          "through an inbox; rd-ag: the all-gather by recursive-doubling exchange and stage "
                          "placement; variants: averaging / accumulating RS, Slot-Reuse pack + RS from "
                          "slots, unpadded AG")
+    ap.add_argument("--ag-transport", choices=["sm", "bulk", "copy-engines"], default="sm",
+                    help="how tide_ag_place moves the pieces (default: the SM kernel)")
     ap.add_argument("--nodes", type=int, default=0,
                     help="regroup the workload's N ranks as this many nodes of N / nodes GPUs (e.g. 16 for "
                          "wan22dit as 16 x 4: more nodes than GPUs per node)")
@@ -213,6 +215,8 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     w = get_workload(args)
     plan = tide.TidePlan(w.shapes, w.N, w.M, w.L)
+    plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, {"sm": tide.TIDE_AG_SM, "bulk": tide.TIDE_AG_BULK,
+                                                 "copy-engines": tide.TIDE_AG_COPY_ENGINES}[args.ag_transport])
     geo = plan
     nbytes = algorithmic_bytes(w, geo)
     S = plan.S
@@ -321,6 +325,7 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": traffic, "algorithmic_bytes_per_launch": nbytes["rs_bytes"]},
         "gpu_launches": launches[0] + launches[1],
         "kernels_per_step": {"rs": launches[0] / K, "ag": launches[1] / K},
+        "ag_transport": args.ag_transport,
         "clocks": clocks,
         "e2e": e2e,
     }
@@ -620,7 +625,7 @@ def run_variants(args, local_rank):
                             ("ag_sm", tide.TIDE_AG_SM)):
         plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, transport)
         timed(name, lambda: plan.ag_place(ap, pp, 2, stream), nb["ag_bytes"])
-    plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, tide.TIDE_AG_AUTO)
+    plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, tide.TIDE_AG_SM)
     del params, pp
     # Slot-Reuse: every rank's slot is its N*S-element all-gather destination
     slots = [torch.empty(N * S, dtype=torch.int16, device=dev) for _ in range(N)]

@@ -19,6 +19,13 @@
 // "at most kStages - kLookahead newer groups pending".  So kLookahead loads
 // and kStages - kLookahead stores are in flight per SM.
 //
+// Loads and stores carry an evict-first L2 policy.  Without it the stores
+// leave L2 full of dirty lines that the next kernel (the reduce-scatter in a
+// training step) has to write back: measured on llama70b, this kernel took
+// 0.496 ms against the SM kernel's 0.520 ms, but the reduce-scatter after it
+// slowed from 2.365 to 2.418 ms; with the policy the two take 0.516 and
+// 2.374 ms and the step is level with the SM kernel's.
+//
 // Every wait is bounded by %globaltimer.  On timeout the thread records
 // TIDE_DEVICE_TIMEOUT in the plan's status word, stops issuing, waits
 // (bounded again) for the loads it issued, waits for its stores, and returns.
@@ -52,6 +59,7 @@ __global__ void __launch_bounds__(32, 1) ag_bulk_kernel(const __grid_constant__ 
   for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 
+  const uint64_t pol = policy_evict_first();  // every byte is read once and written once
   unsigned char* pend_dst[kStages];
   uint32_t pend_bytes[kStages];
   int64_t issued = 0, retired = 0;
@@ -65,7 +73,7 @@ __global__ void __launch_bounds__(32, 1) ag_bulk_kernel(const __grid_constant__ 
         break;
       }
       fence_proxy_async_smem();
-      bulk_store(pend_dst[s], smem + s * kChunkBytes, pend_bytes[s]);
+      bulk_store_policy(pend_dst[s], smem + s * kChunkBytes, pend_bytes[s], pol);
       bulk_commit();
       ++retired;
     }
@@ -76,7 +84,7 @@ __global__ void __launch_bounds__(32, 1) ag_bulk_kernel(const __grid_constant__ 
     const int s = (int)(issued % kStages);
     const uint32_t bytes = 2u * (uint32_t)it.n;
     mbar_arrive_expect_tx(&bar[s], bytes);
-    bulk_load(smem + s * kChunkBytes, a.shard_tab[it.r] + 2 * it.src_off, bytes, &bar[s]);
+    bulk_load_policy(smem + s * kChunkBytes, a.shard_tab[it.r] + 2 * it.src_off, bytes, &bar[s], pol);
     pend_dst[s] = a.param_tab[it.p] + 2 * it.dst_off;
     pend_bytes[s] = bytes;
     ++issued;
@@ -88,7 +96,7 @@ __global__ void __launch_bounds__(32, 1) ag_bulk_kernel(const __grid_constant__ 
       break;
     }
     fence_proxy_async_smem();
-    bulk_store(pend_dst[s], smem + s * kChunkBytes, pend_bytes[s]);
+    bulk_store_policy(pend_dst[s], smem + s * kChunkBytes, pend_bytes[s], pol);
     bulk_commit();
     ++retired;
   }

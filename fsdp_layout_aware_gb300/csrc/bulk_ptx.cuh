@@ -46,10 +46,30 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, 
                : "memory");
 }
 
-// shared -> global, tracked by this thread's bulk async-groups.
-__device__ __forceinline__ void bulk_store(void* gmem_dst, const void* smem_src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst), "r"(smem_addr(smem_src)),
-               "r"(bytes)
+// An L2 policy that marks lines first in line for eviction: for data read
+// or written once, so that it does not crowd L2 (or leave it full of dirty
+// lines for the next kernel to write back).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// bulk_load with an L2 cache policy.
+__device__ __forceinline__ void bulk_load_policy(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar,
+                                                 uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_addr(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+
+// shared -> global with an L2 cache policy, tracked by this thread's bulk
+// async-groups.
+__device__ __forceinline__ void bulk_store_policy(void* gmem_dst, const void* smem_src, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(gmem_dst),
+               "r"(smem_addr(smem_src)), "r"(bytes), "l"(pol)
                : "memory");
 }
 

@@ -316,7 +316,6 @@ tide_status tide_plan_create(const tide_group_desc* d, tide_plan** out_plan) {
     build_rs_items(pl);
     build_ag_items(pl);
     build_ag_bulk_items(pl);
-    for (const AgItem& it : pl->ag_rest_items) pl->ag_rest_elems += it.n;
     build_variant_items(pl);
     build_prefixes(pl);
   } catch (const std::bad_alloc&) {

@@ -391,7 +391,7 @@ tide_status tide_plan_set_option(tide_plan* pl, int32_t option, int64_t value) {
       build_order_table(pl);  // read by every later call (passed by value at launch)
       return TIDE_OK;
     case TIDE_OPT_AG_TRANSPORT:
-      if (value < TIDE_AG_AUTO || value > TIDE_AG_BULK)
+      if (value < TIDE_AG_SM || value > TIDE_AG_BULK)
         return fail(TIDE_ERR_INVALID_ARG, "TIDE_OPT_AG_TRANSPORT must be a tide_ag_transport");
       pl->ag_transport = (int32_t)value;
       return TIDE_OK;
@@ -639,12 +639,8 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
   for (int32_t p = 0; p < pl->P; ++p) ptab[p] = params[p];
   if ((st = commit_table(pl, TABLE_AG, ag_table_bytes(pl), s, &slot)) != TIDE_OK) return st;
 
-  // Bulk copies when asked for, or (auto) when the SM kernel would be left at
-  // most 1/16 of the elements; the bases must allow 16-byte aligned copies.
-  const int64_t all_elems = (int64_t)pl->N * pl->S;
-  bool bulk = (pl->ag_transport == TIDE_AG_BULK ||
-               (pl->ag_transport == TIDE_AG_AUTO && pl->ag_rest_elems * 16 <= all_elems)) &&
-              pl->ag_bulk_ok && elem_bytes == 2 && !pl->ag_unpadded;
+  // Bulk copies need bf16, the padded layout and 16-byte aligned bases.
+  bool bulk = pl->ag_transport == TIDE_AG_BULK && pl->ag_bulk_ok && elem_bytes == 2 && !pl->ag_unpadded;
   for (int32_t r = 0; bulk && r < pl->N; ++r) bulk = ((uintptr_t)shards[r] & 15) == 0;
   for (int32_t p = 0; bulk && p < pl->P; ++p) bulk = pl->e[p] == 0 || ((uintptr_t)params[p] & 15) == 0;
   if (bulk) {

@@ -186,8 +186,7 @@ struct tide_plan {
   std::vector<tide::AgItem> ag_items_unpadded;
   // Bulk-copy all-gather split of ag_items (bf16, 16-byte aligned bases):
   // the aligned middles in chunks of at most kAgBulkChunkElems, and the rest.
-  std::vector<tide::AgItem> ag_bulk_items, ag_rest_items;
-  int64_t ag_rest_elems = 0;               // elements in ag_rest_items  // ag_items restricted to real rows
+  std::vector<tide::AgItem> ag_bulk_items, ag_rest_items;  // ag_items restricted to real rows
   std::vector<tide::AgItem> pack_items;         // Slot-Reuse: r = grad index r*P+p, p = slot rank
   std::vector<const void*> slot_grads;          // tide_rs_reduce_slots' pointer array (host)
   std::vector<int64_t> ag_prefix;  // all-gather cost prefix sums (load balance)
@@ -233,7 +232,7 @@ struct tide_plan {
   int64_t rd_n_items[kMaxRounds] = {};
   int64_t rd_n_units[kMaxRounds] = {};
   int32_t rd_exchange = 0;                 // 0: copy engines, 1: SM kernel
-  int32_t ag_transport = TIDE_AG_AUTO;     // TIDE_OPT_AG_TRANSPORT (tide_ag_transport)
+  int32_t ag_transport = TIDE_AG_SM;       // TIDE_OPT_AG_TRANSPORT (tide_ag_transport)
   mutable int32_t last_launches = 0;       // kernels launched by the latest compute call
   // Bulk-copy all-gather lists (bf16, base pointers 16-byte aligned): chunks
   // of the pieces' aligned middles, and the rest (heads, tails, pieces whose

@@ -35,10 +35,9 @@ TIDE_OPT_SUM_ORDER = 7
 TIDE_OPT_CHECK_OVERLAP = 8
 TIDE_OPT_RD_EXCHANGE = 9
 TIDE_OPT_AG_TRANSPORT = 10
-TIDE_AG_AUTO = 0
-TIDE_AG_SM = 1
-TIDE_AG_COPY_ENGINES = 2
-TIDE_AG_BULK = 3
+TIDE_AG_SM = 0
+TIDE_AG_COPY_ENGINES = 1
+TIDE_AG_BULK = 2
 TIDE_SUM_LANDING = 0
 TIDE_SUM_RELATIVE = 1
 ITEM_FIELDS = ("kind", "p", "r", "src_off", "dst_off", "n")

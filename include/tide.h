@@ -197,31 +197,29 @@ typedef enum tide_option {
                                   per round over all M copies (same bytes,
                                   same result) */
   TIDE_OPT_AG_TRANSPORT = 10   /* how tide_ag_place moves the pieces, a
-                                  tide_ag_transport (default TIDE_AG_AUTO) */
+                                  tide_ag_transport (default TIDE_AG_SM) */
 } tide_option;
 
 /* Transports for TIDE_OPT_AG_TRANSPORT; all give the same result.  The pages'
  * all-gather uses no SM threads ([Richland] "What shipped").
- *   TIDE_AG_AUTO          (default) TIDE_AG_BULK when the call qualifies for
- *                         it and at most 1/16 of the group's elements are
- *                         left to the SM kernel, else TIDE_AG_SM;
- *   TIDE_AG_SM            one kernel over the work list, every thread
- *                         copying 16-byte words;
+ *   TIDE_AG_SM            (default) one kernel over the work list, every
+ *                         thread copying 16-byte words;
  *   TIDE_AG_COPY_ENGINES  one copy-engine copy per (parameter, rank) piece:
  *                         no kernel, N*P host calls per call;
  *   TIDE_AG_BULK          bf16 only: one thread per SM moves each piece's
  *                         16-byte aligned middle global -> shared -> global
- *                         with bulk copies (TMA), the SM kernel the rest.
+ *                         with bulk copies (TMA), the SM kernel the rest
+ *                         (two launches); a training step with it takes as
+ *                         long as with TIDE_AG_SM.
  *                         Needs every shard and parameter pointer 16-byte
  *                         aligned and the padded layout; otherwise, and for
  *                         4-byte elements, the call uses TIDE_AG_SM.  Its
  *                         waits are bounded by TIDE_OPT_WAIT_LIMIT_NS
  *                         (TIDE_ERR_TIMEOUT from tide_plan_check). */
 typedef enum tide_ag_transport {
-  TIDE_AG_AUTO = 0,
-  TIDE_AG_SM = 1,
-  TIDE_AG_COPY_ENGINES = 2,
-  TIDE_AG_BULK = 3
+  TIDE_AG_SM = 0,
+  TIDE_AG_COPY_ENGINES = 1,
+  TIDE_AG_BULK = 2
 } tide_ag_transport;
 
 /* Orders for TIDE_OPT_SUM_ORDER.  The pages do not say in which order the

@@ -220,7 +220,7 @@ def test_plan_options_validate_without_a_gpu():
         for opt, val in [(tide.TIDE_OPT_RS_KERNEL, 2), (tide.TIDE_OPT_WAIT_LIMIT_NS, 0),
                          (tide.TIDE_OPT_TEST_DROP_TILE, -2), (tide.TIDE_OPT_SUM_ORDER, 2),
                          (tide.TIDE_OPT_RD_EXCHANGE, 2), (tide.TIDE_OPT_CHECK_OVERLAP, 3),
-                         (tide.TIDE_OPT_AG_TRANSPORT, 4), (tide.TIDE_OPT_AG_TRANSPORT, -1), (99, 0)]:
+                         (tide.TIDE_OPT_AG_TRANSPORT, 3), (tide.TIDE_OPT_AG_TRANSPORT, -1), (99, 0)]:
             with pytest.raises(tide.TideError) as err:
                 plan.set_option(opt, val)
             assert err.value.status == 1
@@ -394,4 +394,4 @@ def test_ag_bulk_split_workloads(cfg):
 def test_last_launches_without_a_gpu():
     with tide.TidePlan([(8, 64)], 4, 1, 4) as plan:
         assert plan.last_launches() == 0          # nothing ran yet
-    assert tide.tide.TIDE_AG_AUTO == 0 and tide.tide.TIDE_AG_BULK == 3
+    assert tide.TIDE_AG_SM == 0 and tide.TIDE_AG_BULK == 2

@@ -590,21 +590,22 @@ def test_ag_bulk_transport_alignment(w, shift):
                 assert (got[:lead] == 0x5A5A).all() and (got[lead + n:] == 0x5A5A).all()
 
 
-def test_ag_auto_transport_choice():
-    """TIDE_AG_AUTO (the default) takes bulk copies when the SM kernel would be
-    left at most 1/16 of the elements (llama70b rows/512: the bulk kernel plus
-    one remainder launch) and the SM kernel otherwise (uneven subset: one
-    launch); both exact."""
-    for w, want in [(SMALL[1], 2), (SMALL[4], 1)]:
-        geo = O.geometry(w.shapes, w.N)
-        rng = np.random.default_rng(37)
-        shards_h = [rng.integers(0, 65535, geo.S, dtype=np.uint16) for _ in range(w.N)]
-        expect = O.ag_place(geo, shards_h)
-        with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
-            shards = [to_dev_u16(x)[0] for x in shards_h]
+def test_ag_bulk_launch_count():
+    """The bulk transport launches its kernel plus one remainder launch when
+    the split leaves a remainder (llama70b rows/512); the default SM
+    transport one kernel; both exact."""
+    w = SMALL[1]
+    geo = O.geometry(w.shapes, w.N)
+    rng = np.random.default_rng(37)
+    shards_h = [rng.integers(0, 65535, geo.S, dtype=np.uint16) for _ in range(w.N)]
+    expect = O.ag_place(geo, shards_h)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        shards = [to_dev_u16(x)[0] for x in shards_h]
+        for transport, want in [(tide.TIDE_AG_SM, 1), (tide.TIDE_AG_BULK, 2)]:
+            plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, transport)
             params = [torch.full((w.N * geo.e[p],), -1, dtype=torch.int16, device=DEV) for p in range(w.P)]
             plan.ag_place(shards, params, 2)
-            assert plan.last_launches() == want, w.name
+            assert plan.last_launches() == want
             plan.check()
             for p in range(w.P):
-                assert np.array_equal(params[p].cpu().numpy().view(np.uint16), expect[p]), (w.name, p)
+                assert np.array_equal(params[p].cpu().numpy().view(np.uint16), expect[p]), (transport, p)
