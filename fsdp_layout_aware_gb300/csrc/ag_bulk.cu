@@ -29,6 +29,8 @@
 // Every wait is bounded by %globaltimer.  On timeout the thread records
 // TIDE_DEVICE_TIMEOUT in the plan's status word, stops issuing, waits
 // (bounded again) for the loads it issued, waits for its stores, and returns.
+// A test hook (TIDE_OPT_TEST_DROP_TILE) arms one stage without issuing its
+// load, so that path runs without any fault.
 
 #include <cuda_runtime.h>
 
@@ -84,7 +86,8 @@ __global__ void __launch_bounds__(32, 1) ag_bulk_kernel(const __grid_constant__ 
     const int s = (int)(issued % kStages);
     const uint32_t bytes = 2u * (uint32_t)it.n;
     mbar_arrive_expect_tx(&bar[s], bytes);
-    bulk_load_policy(smem + s * kChunkBytes, a.shard_tab[it.r] + 2 * it.src_off, bytes, &bar[s], pol);
+    if (issued != a.test_drop_chunk)  // test hook: an armed stage whose data never comes
+      bulk_load_policy(smem + s * kChunkBytes, a.shard_tab[it.r] + 2 * it.src_off, bytes, &bar[s], pol);
     pend_dst[s] = a.param_tab[it.p] + 2 * it.dst_off;
     pend_bytes[s] = bytes;
     ++issued;

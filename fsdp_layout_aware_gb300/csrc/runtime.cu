@@ -667,6 +667,7 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
     b.param_tab = (unsigned char* const*)(slot->dev + (size_t)pl->N * 8);
     b.status = pl->d_status;
     b.wait_limit_ns = pl->wait_limit_ns;
+    b.test_drop_chunk = pl->test_drop_tile;
     const int grid = (int)std::min<int64_t>(pl->num_sms, pl->agb_n_items);
     ++pl->last_launches;
     return finish(slot, launch_ag_bulk(b, grid, stream), s, "bulk all-gather launch");

@@ -148,6 +148,7 @@ struct AgBulkArgs {
   unsigned char* const* param_tab;        // [P]
   int* status;                      // TIDE_DEVICE_TIMEOUT on a wait that ran out
   uint64_t wait_limit_ns;
+  int64_t test_drop_chunk;          // chunk (counted per CTA) whose load is never issued (tests); -1: none
 };
 
 struct AgArgs {

@@ -170,9 +170,11 @@ tide_status tide_plan_level2_order(const tide_plan* plan, int32_t n_dest, int32_
  *                          ([Endgame] "Reduce-scatter...").
  *   TIDE_OPT_SUM_ORDER     the level-2 addition order (tide_sum_order,
  *                          below); default TIDE_SUM_LANDING.
- *   TIDE_OPT_TEST_DROP_TILE  test hook: the bulk kernel's producer withholds
- *                          the given tile (counted per CTA from 0), so the
- *                          consumers' wait runs out; -1 (default) disables.
+ *   TIDE_OPT_TEST_DROP_TILE  test hook: the bulk reduce-scatter's producer
+ *                          withholds the given tile, and the bulk
+ *                          all-gather skips the given chunk's load (both
+ *                          counted per CTA from 0), so a bounded wait runs
+ *                          out; -1 (default) disables.
  * Errors: INVALID_ARG for an unknown option or value. */
 typedef enum tide_option {
   TIDE_OPT_RS_KERNEL = 1,

@@ -349,6 +349,34 @@ def test_bulk_kernel_wait_runs_out_and_context_survives():
             assert np.array_equal(f32_bits(outs[r]), expect[r].view(np.uint32)), r
 
 
+def test_bulk_all_gather_wait_runs_out_and_context_survives():
+    """The bulk all-gather with one chunk's load withheld: its bounded wait
+    runs out (TIDE_ERR_TIMEOUT), and the next call on the same context is
+    exact."""
+    w = SMALL[1]
+    geo = O.geometry(w.shapes, w.N)
+    rng = np.random.default_rng(41)
+    shards_h = [rng.integers(0, 65535, geo.S, dtype=np.uint16) for _ in range(w.N)]
+    expect = O.ag_place(geo, shards_h)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, tide.TIDE_AG_BULK)
+        shards = [to_dev_u16(x)[0] for x in shards_h]
+        params = [torch.full((w.N * geo.e[p],), -1, dtype=torch.int16, device=DEV) for p in range(w.P)]
+        assert len(plan.items(2)) > 0
+        plan.set_option(tide.TIDE_OPT_WAIT_LIMIT_NS, 20_000_000)
+        plan.set_option(tide.TIDE_OPT_TEST_DROP_TILE, 0)
+        plan.ag_place(shards, params, 2)
+        with pytest.raises(tide.TideError) as err:
+            plan.check()
+        assert err.value.status == 8
+        plan.set_option(tide.TIDE_OPT_TEST_DROP_TILE, -1)
+        plan.set_option(tide.TIDE_OPT_WAIT_LIMIT_NS, 2_000_000_000)
+        plan.ag_place(shards, params, 2)
+        plan.check()
+        for p in range(w.P):
+            assert np.array_equal(params[p].cpu().numpy().view(np.uint16), expect[p]), p
+
+
 def test_host_buffers_through_the_c_abi():
     """Pinned host memory passed straight to the C ABI (the kernels read and
     write it over the host link): same bits as the oracle."""
