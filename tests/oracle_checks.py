@@ -473,4 +473,29 @@ def check_stage_place_equals_direct_landing():
             assert all(np.array_equal(a, b) for a, b in zip(params, direct))
 
 
+def check_rs_buffer_accounting():
+    """Table 8's stock-FSDP2 buffers are N x the output plus a small constant,
+    as the N*S packed layout implies; and the staged reduce-scatter's inbox
+    carries one fp32 partial per node where the raw cross-node data would be
+    L bf16 copies, a quarter of the bytes at L = 8."""
+    g = _golden("rs_buffer_accounting.json")
+    for mib, extra in ((32, 0.03), (128, 0.12)):
+        for row in (r for r in g["rows"] if r["output_mib"] == mib):
+            N = row["gpus"]
+            # P = 16 equal bf16 parameters whose per-rank fp32 shard is `mib` MiB
+            S = mib * 2 ** 20 // 4
+            geo = O.geometry([(N * (S // 16 // 1024), 1024)] * 16, N)
+            assert 4 * geo.S == mib * 2 ** 20
+            packed_gib = 4 * N * geo.S / 2 ** 30           # the packed fp32 reduce-scatter input
+            assert abs(row["stock_buffer_gib"] - packed_gib - extra) < 0.006, (row, packed_gib)
+    ratio = g["cross_node_ratio"]
+    M, L = 2, ratio["L"]
+    geo = O.geometry([(M * L * 4, 16)], M * L)
+    grads = [[np.zeros(M * L * 4 * 16, dtype=np.uint16)] for _ in range(M * L)]
+    inbox = O.rs_inbox(geo, grads, M, L)
+    partial_bytes = 4 * inbox.size                     # fp32 partials the landing side reads
+    raw_bytes = 2 * (M * L) * (M * L) * geo.S          # every contributor's bf16 slice, for every destination
+    assert abs(partial_bytes / raw_bytes - ratio["ratio"]) < 1e-12
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

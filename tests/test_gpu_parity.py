@@ -70,6 +70,10 @@ def test_rs_small_bit_exact(w):
             assert bad.size == 0, f"rank {r}: {bad.size} mismatches, first at {bad[:5]}"
             guards = f32_bits(outs[r][1])
             assert (guards[:GUARD] == 0x7FC00000).all() and (guards[GUARD + geo.S:] == 0x7FC00000).all()
+        # the inputs are read only: every gradient still holds what was uploaded
+        for r in range(w.N):
+            for p in range(w.P):
+                assert np.array_equal(u16_of(dev[r][p]), grads[r][p]), (r, p)
 
 
 @pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
@@ -92,6 +96,9 @@ def test_ag_small_bit_exact(w, elem_bytes):
             assert np.array_equal(got, expect[p]), f"param {p}"
             g = backs[p].cpu().numpy()
             assert (g[:GUARD] == -7).all() and (g[GUARD + w.N * geo.e[p]:] == -7).all()
+        # the shards are read only
+        for r in range(w.N):
+            assert np.array_equal(shards[r].cpu().numpy().view(dt), shards_h[r]), r
 
 
 def test_rs_then_ag_round_trip_fp32():
