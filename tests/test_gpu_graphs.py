@@ -30,7 +30,8 @@ def _load(dev, grads, w):
 
 
 @pytest.mark.parametrize("staged", [False, True], ids=["fused", "staged"])
-def test_capture_and_replay(staged):
+@pytest.mark.parametrize("transport", ["sm", "bulk", "copy_engines"])
+def test_capture_and_replay(staged, transport):
     w = W
     geo = O.geometry(w.shapes, w.N)
     datasets = [host_grads(_variant(w, k)) for k in range(3)]
@@ -39,6 +40,8 @@ def test_capture_and_replay(staged):
     ag_sets = [[rng.integers(0, 65535, geo.S, dtype=np.uint16) for _ in range(w.N)] for _ in range(3)]
     ag_expects = [O.ag_place(geo, s) for s in ag_sets]
     with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, {"sm": tide.TIDE_AG_SM, "bulk": tide.TIDE_AG_BULK,
+                                                     "copy_engines": tide.TIDE_AG_COPY_ENGINES}[transport])
         dev = [[to_dev_u16(datasets[0][r][p])[0] for p in range(w.P)] for r in range(w.N)]
         flat = tide.pointer_array([dev[r][p] for r in range(w.N) for p in range(w.P)])
         outs = [torch.empty(geo.S, dtype=torch.float32, device=DEV) for _ in range(w.N)]
