@@ -2,7 +2,8 @@
 
 Each case draws M, L (M > L included), parameter shapes (0-D, 1-D, 3-D, empty,
 fewer rows than ranks, odd row lengths), value distributions, the level-2
-order and the averaging / accumulate variants, then runs the reduce-scatter on
+order and the averaging / accumulate variants (every fourth case with pieces
+of several work items), then runs the reduce-scatter on
 the direct, staged, bulk (M <= 8) and no-allocation paths and the all-gather
 on the SM and bulk transports.  Sizes stay small so the oracle is quick.
 """
@@ -19,22 +20,23 @@ from gpu_common import DEV, f32_bits, host_grads, to_dev_u16
 
 pytestmark = pytest.mark.gpu
 
-SEEDS = list(range(16))
+SEEDS = list(range(48))
 
 
 def _case(seed):
     rng = np.random.default_rng(1000 + seed)
     L = int(rng.integers(1, 9))
     if seed % 3 == 0:   # more nodes than GPUs per node
-        M = int(rng.integers(L + 1, 13)) if L <= 4 else int(rng.integers(L, 7 + L // 8))
+        M = int(rng.integers(L + 1, 13)) if L <= 4 else int(rng.integers(L, L + 2))
     else:
         M = int(rng.integers(1, L + 1))
     N = M * L
+    big = seed % 4 == 1   # pieces of several work items each
     shapes = []
-    for _ in range(int(rng.integers(1, 10))):
+    for _ in range(int(rng.integers(1, 4 if big else 10))):
         kind = int(rng.integers(0, 6))
-        rows = int(rng.integers(0, 2 * N + 2))
-        cols = int(rng.integers(1, 90))
+        rows = int(rng.integers(0, (40 if big else 2) * N + 2))
+        cols = int(rng.integers(1, 600 if big else 90))
         if kind == 0:
             shapes.append(())
         elif kind == 1:
