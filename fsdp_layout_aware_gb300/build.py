@@ -4,6 +4,11 @@
   * ``fsdp_layout_aware_gb300/libtide.so``  -- the C-ABI library (include/tide.h)
   * ``synth/libtide_synth.so``              -- the seeded input generator's
                                                device twin (tests and bench only)
+and, on request (``build_lib("tide_checked")``, ``--checked``):
+  * ``fsdp_layout_aware_gb300/libtide_checked.so`` -- the same library compiled
+                                               with TIDE_CHECKED: every kernel
+                                               store checked against its work
+                                               item (check.cuh; tests only)
 A library is rebuilt only when its sources, headers or flags changed (a
 content hash is kept next to the objects in ``_build/``).
 """
@@ -32,15 +37,25 @@ def _cuda_lib_dir(nvcc):
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 
+TIDE_SRCS = [os.path.join(HERE, "csrc", f) for f in ("plan.cpp", "runtime.cu", "rs_kernel.cu", "rs_bulk.cu",
+                                                     "rs_staged.cu", "ag_kernel.cu", "ag_bulk.cu", "rs_noalloc.cu")]
+TIDE_DEPS = [os.path.join(HERE, "csrc", f) for f in ("tide_internal.h", "rs_device.cuh", "bulk_ptx.cuh",
+                                                     "check.cuh")] + [os.path.join(ROOT, "include", "tide.h")]
+
 LIBS = {
     "tide": {
         "out": os.path.join(HERE, "libtide.so"),
-        "srcs": [os.path.join(HERE, "csrc", f) for f in ("plan.cpp", "runtime.cu", "rs_kernel.cu", "rs_bulk.cu",
-                                                              "rs_staged.cu", "ag_kernel.cu", "ag_bulk.cu",
-                                                              "rs_noalloc.cu")],
-        "deps": [os.path.join(HERE, "csrc", f) for f in ("tide_internal.h", "rs_device.cuh", "bulk_ptx.cuh")] +
-                [os.path.join(ROOT, "include", "tide.h")],
+        "srcs": TIDE_SRCS,
+        "deps": TIDE_DEPS,
         "build": os.path.join(HERE, "_build"),
+    },
+    "tide_checked": {
+        "out": os.path.join(HERE, "libtide_checked.so"),
+        "srcs": TIDE_SRCS,
+        "deps": TIDE_DEPS,
+        "build": os.path.join(HERE, "_build_checked"),
+        "flags": ["-DTIDE_CHECKED"],
+        "on_request": True,
     },
     "synth": {
         "out": os.path.join(ROOT, "synth", "libtide_synth.so"),
@@ -69,7 +84,7 @@ def _run(cmd):
 def build_lib(name, force=False, verbose=False, extra_flags=()):
     spec = LIBS[name]
     nvcc = _nvcc()
-    flags = ARCH + CFLAGS + list(extra_flags)
+    flags = ARCH + CFLAGS + spec.get("flags", []) + list(extra_flags)
     os.makedirs(spec["build"], exist_ok=True)
     stamp = os.path.join(spec["build"], "stamp")
     digest = _digest(spec, flags)
@@ -94,11 +109,13 @@ def build_lib(name, force=False, verbose=False, extra_flags=()):
     return spec["out"]
 
 
-def build_all(force=False, verbose=False):
-    return [build_lib(n, force=force, verbose=verbose) for n in LIBS]
+def build_all(force=False, verbose=False, checked=False):
+    """The libraries the package needs; the checked variant only if asked."""
+    return [build_lib(n, force=force, verbose=verbose) for n, spec in LIBS.items()
+            if checked or not spec.get("on_request")]
 
 
 if __name__ == "__main__":
     import sys
-    for path in build_all(force="--force" in sys.argv, verbose=True):
+    for path in build_all(force="--force" in sys.argv, verbose=True, checked="--checked" in sys.argv):
         print(path)

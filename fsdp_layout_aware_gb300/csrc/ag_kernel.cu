@@ -17,6 +17,7 @@
 
 #include <cstdint>
 
+#include "check.cuh"
 #include "tide_internal.h"
 
 namespace tide {
@@ -28,7 +29,9 @@ union Vec16 {
   uint16_t h[8];
 };
 
-__device__ __forceinline__ void copy_elem(unsigned char* d, const unsigned char* s, int eb) {
+__device__ __forceinline__ void copy_elem(unsigned char* d, const unsigned char* s, int eb, const void* lo,
+                                          const void* hi) {
+  if (!store_ok(d, eb, lo, hi)) return;
   if (eb == 4)
     *reinterpret_cast<uint32_t*>(d) = *reinterpret_cast<const uint32_t*>(s);
   else
@@ -41,20 +44,23 @@ __device__ __forceinline__ void copy_elem(unsigned char* d, const unsigned char*
 __device__ __forceinline__ void warp_copy_same_phase(unsigned char* dst, const unsigned char* src, int64_t nbytes,
                                                      int eb, int lane) {
   const int64_t head = min(nbytes, (int64_t)((16 - ((uintptr_t)dst & 15)) & 15));
-  for (int64_t i = (int64_t)lane * eb; i < head; i += 32 * eb) copy_elem(dst + i, src + i, eb);
+  const unsigned char* const end = dst + nbytes;
+  for (int64_t i = (int64_t)lane * eb; i < head; i += 32 * eb) copy_elem(dst + i, src + i, eb, dst, end);
   const int64_t nv = (nbytes - head) >> 4;
   const uint4* s4 = reinterpret_cast<const uint4*>(src + head);
   uint4* d4 = reinterpret_cast<uint4*>(dst + head);
   int64_t i = lane;
   for (; i + 96 < nv; i += 128) {
     const uint4 a = __ldcs(s4 + i), b = __ldcs(s4 + i + 32), c = __ldcs(s4 + i + 64), d = __ldcs(s4 + i + 96);
-    __stcs(d4 + i, a);
-    __stcs(d4 + i + 32, b);
-    __stcs(d4 + i + 64, c);
-    __stcs(d4 + i + 96, d);
+    if (store_ok(d4 + i, 16, dst, end)) __stcs(d4 + i, a);
+    if (store_ok(d4 + i + 32, 16, dst, end)) __stcs(d4 + i + 32, b);
+    if (store_ok(d4 + i + 64, 16, dst, end)) __stcs(d4 + i + 64, c);
+    if (store_ok(d4 + i + 96, 16, dst, end)) __stcs(d4 + i + 96, d);
   }
-  for (; i < nv; i += 32) __stcs(d4 + i, __ldcs(s4 + i));
-  for (int64_t j = head + (nv << 4) + (int64_t)lane * eb; j < nbytes; j += 32 * eb) copy_elem(dst + j, src + j, eb);
+  for (; i < nv; i += 32)
+    if (store_ok(d4 + i, 16, dst, end)) __stcs(d4 + i, __ldcs(s4 + i));
+  for (int64_t j = head + (nv << 4) + (int64_t)lane * eb; j < nbytes; j += 32 * eb)
+    copy_elem(dst + j, src + j, eb, dst, end);
 }
 
 // Bytes [sh, sh + 16) of the 32-byte concatenation lo || hi (sh even).
@@ -130,19 +136,23 @@ __device__ __forceinline__ void warp_copy_shifted(unsigned char* dst, const unsi
       unsigned char* dw = dbase + 16 * w;
       Vec16 out;
       out.v = extract16(lo[j], hi, sh);
+      const void* rng_lo = (const void*)d_lo;
+      const void* rng_hi = (const void*)d_hi;
       if ((uintptr_t)dw >= d_lo && (uintptr_t)dw + 16 <= d_hi) {
-        __stcs(reinterpret_cast<uint4*>(dw), out.v);
+        if (store_ok(dw, 16, rng_lo, rng_hi)) __stcs(reinterpret_cast<uint4*>(dw), out.v);
       } else if (eb == 2) {
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
           const uintptr_t addr = (uintptr_t)dw + 2 * b;
-          if (addr >= d_lo && addr < d_hi) *reinterpret_cast<uint16_t*>(addr) = out.h[b];
+          if (addr >= d_lo && addr < d_hi && store_ok((void*)addr, 2, rng_lo, rng_hi))
+            *reinterpret_cast<uint16_t*>(addr) = out.h[b];
         }
       } else {
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           const uintptr_t addr = (uintptr_t)dw + 4 * b;
-          if (addr >= d_lo && addr < d_hi) *reinterpret_cast<uint32_t*>(addr) = out.w[b];
+          if (addr >= d_lo && addr < d_hi && store_ok((void*)addr, 4, rng_lo, rng_hi))
+            *reinterpret_cast<uint32_t*>(addr) = out.w[b];
         }
       }
     }
@@ -178,6 +188,21 @@ __global__ void __launch_bounds__(kAgThreads, 4) ag_place_kernel(const __grid_co
 }
 
 }  // namespace
+
+TIDE_BOUNDS_COUNTER(ag_kernel_bounds)
+
+namespace {
+// Positive control of the store checks: asks about an address outside a
+// made-up range, without touching memory; a checked build counts one.
+__global__ void bounds_selftest_kernel() {
+  if (threadIdx.x == 0) (void)store_ok((const void*)64, 4, (const void*)0, (const void*)32);
+}
+}  // namespace
+
+int ag_bounds_selftest() {
+  bounds_selftest_kernel<<<1, 32>>>();
+  return (int)cudaGetLastError();
+}
 
 int launch_ag(const AgArgs& a, int grid, void* stream) {
   ag_place_kernel<<<grid, kAgThreads, 0, (cudaStream_t)stream>>>(a);

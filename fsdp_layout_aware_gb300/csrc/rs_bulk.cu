@@ -311,7 +311,8 @@ __device__ void consumers(const RsArgs& a, const Smem& m) {
               }
             }
           }
-          __stcs(d.dst + e, epilogue1(acc2, d.dst + e, a.epilogue, a.N));
+          if (store_ok(d.dst + e, 4, d.dst, d.dst + d.n))
+            __stcs(d.dst + e, epilogue1(acc2, d.dst + e, a.epilogue, a.N));
         }
         pb ^= 1;
       }
@@ -354,7 +355,8 @@ __device__ void consumers(const RsArgs& a, const Smem& m) {
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          if (i < cnt) __stcs(d.dst + e0 + i, epilogue1(acc2[i], d.dst + e0 + i, a.epilogue, a.N));
+          if (i < cnt && store_ok(d.dst + e0 + i, 4, d.dst, d.dst + d.n))
+            __stcs(d.dst + e0 + i, epilogue1(acc2[i], d.dst + e0 + i, a.epilogue, a.N));
       }
     }
     if (++stage == (uint32_t)a.bulk.stages) {
@@ -411,6 +413,8 @@ int setup_t(int smem_bytes) {
 }
 
 }  // namespace
+
+TIDE_BOUNDS_COUNTER(rs_bulk_bounds)
 
 BulkLayout rs_bulk_layout(int N, int M, int L, int smem_budget) {
   BulkLayout b{};

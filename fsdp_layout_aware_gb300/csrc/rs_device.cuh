@@ -7,6 +7,8 @@
 
 #include <cstdint>
 
+#include "check.cuh"
+
 namespace tide {
 
 // Widen the 8 bf16 values of a 16-byte vector and add them into acc (fp32,
@@ -39,12 +41,13 @@ __device__ __forceinline__ long long take_item(unsigned long long* counter, int6
 // Padding rows of a destination piece: +0.0 everywhere.
 __device__ __forceinline__ void zero_fill(float* dst, int n) {
   const int head = min(n, (int)(((16 - ((uintptr_t)dst & 15)) & 15) >> 2));
-  if ((int)threadIdx.x < head) dst[threadIdx.x] = 0.f;
+  if ((int)threadIdx.x < head && store_ok(dst + threadIdx.x, 4, dst, dst + n)) dst[threadIdx.x] = 0.f;
   const int nv = (n - head) >> 2;
   float4* d4 = reinterpret_cast<float4*>(dst + head);
-  for (int i = threadIdx.x; i < nv; i += blockDim.x) __stcs(d4 + i, make_float4(0.f, 0.f, 0.f, 0.f));
+  for (int i = threadIdx.x; i < nv; i += blockDim.x)
+    if (store_ok(d4 + i, 16, dst, dst + n)) __stcs(d4 + i, make_float4(0.f, 0.f, 0.f, 0.f));
   const int t0 = head + (nv << 2);
-  if ((int)threadIdx.x < n - t0) dst[t0 + threadIdx.x] = 0.f;
+  if ((int)threadIdx.x < n - t0 && store_ok(dst + t0 + threadIdx.x, 4, dst, dst + n)) dst[t0 + threadIdx.x] = 0.f;
 }
 
 // Store the 8 results of a vector whose lane 0 is item element e0 when the
@@ -52,25 +55,26 @@ __device__ __forceinline__ void zero_fill(float* dst, int n) {
 __device__ __forceinline__ void store8_aligned(float* dst, int e0, int n, const float (&acc)[8]) {
   if (e0 >= 0 && e0 + 8 <= n) {
     float* o = dst + e0;
-    __stcs(reinterpret_cast<float4*>(o), make_float4(acc[0], acc[1], acc[2], acc[3]));
-    __stcs(reinterpret_cast<float4*>(o + 4), make_float4(acc[4], acc[5], acc[6], acc[7]));
+    if (store_ok(o, 16, dst, dst + n)) __stcs(reinterpret_cast<float4*>(o), make_float4(acc[0], acc[1], acc[2], acc[3]));
+    if (store_ok(o + 4, 16, dst, dst + n))
+      __stcs(reinterpret_cast<float4*>(o + 4), make_float4(acc[4], acc[5], acc[6], acc[7]));
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = e0 + i;
-      if (e >= 0 && e < n) __stcs(dst + e, acc[i]);
+      if (e >= 0 && e < n && store_ok(dst + e, 4, dst, dst + n)) __stcs(dst + e, acc[i]);
     }
   }
 }
 
 __device__ __forceinline__ void store4(float* dst, int a, int n, float w0, float w1, float w2, float w3) {
   if (a >= 0 && a + 4 <= n) {
-    __stcs(reinterpret_cast<float4*>(dst + a), make_float4(w0, w1, w2, w3));
+    if (store_ok(dst + a, 16, dst, dst + n)) __stcs(reinterpret_cast<float4*>(dst + a), make_float4(w0, w1, w2, w3));
   } else {
-    if (a >= 0 && a < n) __stcs(dst + a, w0);
-    if (a + 1 >= 0 && a + 1 < n) __stcs(dst + a + 1, w1);
-    if (a + 2 >= 0 && a + 2 < n) __stcs(dst + a + 2, w2);
-    if (a + 3 >= 0 && a + 3 < n) __stcs(dst + a + 3, w3);
+    if (a >= 0 && a < n && store_ok(dst + a, 4, dst, dst + n)) __stcs(dst + a, w0);
+    if (a + 1 >= 0 && a + 1 < n && store_ok(dst + a + 1, 4, dst, dst + n)) __stcs(dst + a + 1, w1);
+    if (a + 2 >= 0 && a + 2 < n && store_ok(dst + a + 2, 4, dst, dst + n)) __stcs(dst + a + 2, w2);
+    if (a + 3 >= 0 && a + 3 < n && store_ok(dst + a + 3, 4, dst, dst + n)) __stcs(dst + a + 3, w3);
   }
 }
 
@@ -105,14 +109,14 @@ __device__ __forceinline__ void store8_shifted(float* dst, int e0, int n, int de
 #pragma unroll
     for (int i = 4; i < 8; ++i) {
       const int j = a + i;
-      if (j < e0 + 8 && j >= 0 && j < n) __stcs(dst + j, w[i]);
+      if (j < e0 + 8 && j >= 0 && j < n && store_ok(dst + j, 4, dst, dst + n)) __stcs(dst + j, w[i]);
     }
   }
   if (lane == 0) {
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
       const int j = e0 + i;
-      if (i < delta && j >= 0 && j < n) __stcs(dst + j, acc[i]);
+      if (i < delta && j >= 0 && j < n && store_ok(dst + j, 4, dst, dst + n)) __stcs(dst + j, acc[i]);
     }
   }
 }
@@ -143,14 +147,16 @@ __device__ __forceinline__ void epilogue8(float (&acc)[8], const float* dst, int
 __device__ __forceinline__ void pad_fill(float* dst, int n, int flags, int tid, int nthreads) {
   if (!(flags & EPI_ACCUMULATE)) {
     const int head = min(n, (int)(((16 - ((uintptr_t)dst & 15)) & 15) >> 2));
-    if (tid < head) dst[tid] = 0.f;
+    if (tid < head && store_ok(dst + tid, 4, dst, dst + n)) dst[tid] = 0.f;
     const int nv = (n - head) >> 2;
     float4* d4 = reinterpret_cast<float4*>(dst + head);
-    for (int i = tid; i < nv; i += nthreads) __stcs(d4 + i, make_float4(0.f, 0.f, 0.f, 0.f));
+    for (int i = tid; i < nv; i += nthreads)
+      if (store_ok(d4 + i, 16, dst, dst + n)) __stcs(d4 + i, make_float4(0.f, 0.f, 0.f, 0.f));
     const int t0 = head + (nv << 2);
-    if (tid < n - t0) dst[t0 + tid] = 0.f;
+    if (tid < n - t0 && store_ok(dst + t0 + tid, 4, dst, dst + n)) dst[t0 + tid] = 0.f;
   } else {
-    for (int i = tid; i < n; i += nthreads) dst[i] = __fadd_rn(dst[i], 0.f);
+    for (int i = tid; i < n; i += nthreads)
+      if (store_ok(dst + i, 4, dst, dst + n)) dst[i] = __fadd_rn(dst[i], 0.f);
   }
 }
 

@@ -126,7 +126,8 @@ __device__ __forceinline__ void reduce_unaligned(const uint16_t* const* src, int
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (i < cnt) __stcs(dst + e0 + i, epilogue1(acc2[i], dst + e0 + i, epi, N));
+      if (i < cnt && store_ok(dst + e0 + i, 4, dst, dst + n))
+        __stcs(dst + e0 + i, epilogue1(acc2[i], dst + e0 + i, epi, N));
   }
 }
 
@@ -203,6 +204,8 @@ int launch_rs(const RsArgs& a, int grid, void* stream) {
   }
   return (int)cudaErrorInvalidValue;
 }
+
+TIDE_BOUNDS_COUNTER(rs_kernel_bounds)
 
 int rs_blocks_per_sm(int L) {
   switch (L) {

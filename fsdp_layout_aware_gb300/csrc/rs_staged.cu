@@ -81,7 +81,8 @@ __device__ __forceinline__ void sum_unaligned(const RsArgs& a, const uint16_t* c
       float acc1 = 0.f;
 #pragma unroll
       for (int l = 0; l < L; ++l) acc1 = __fadd_rn(acc1, bf16_to_f32(__ldcs(src[n_src * L + l] + e)));
-      __stcs(inbox_block(a, n_dest, l_dest, n_src, item.slice, item.dst_off) + e, acc1);
+      float* blk = inbox_block(a, n_dest, l_dest, n_src, item.slice, item.dst_off);
+      if (store_ok(blk + e, 4, blk, blk + n)) __stcs(blk + e, acc1);
     }
   }
 }
@@ -171,7 +172,8 @@ __global__ void __launch_bounds__(256, kBatched ? 5 : 8) rs_land_kernel(const __
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int64_t x = x0 + (int64_t)u * blockDim.x;
-        if (x < hi) __stcs(out + x, epilogue1(acc[u], out + x, a.epilogue, M * L));
+        if (x < hi && store_ok(out + x, 4, out + lo, out + hi))
+          __stcs(out + x, epilogue1(acc[u], out + x, a.epilogue, M * L));
       }
     }
   }
@@ -184,6 +186,8 @@ int launch_sum_t(const RsArgs& a, int grid, cudaStream_t s) {
 }
 
 }  // namespace
+
+TIDE_BOUNDS_COUNTER(rs_staged_bounds)
 
 int launch_rs_staged(const RsArgs& a, int sum_grid, int land_grid_x, void* stream) {
   cudaStream_t s = (cudaStream_t)stream;

@@ -413,6 +413,24 @@ tide_status tide_plan_set_option(tide_plan* pl, int32_t option, int64_t value) {
 
 int32_t tide_plan_last_launches(const tide_plan* pl) { return pl ? pl->last_launches : -1; }
 
+tide_status tide_debug_bounds_selftest(void) {
+  clear_error();
+  TIDE_CUDA((cudaError_t)ag_bounds_selftest(), "bounds self-test launch");
+  TIDE_CUDA(cudaDeviceSynchronize(), "bounds self-test");
+  return TIDE_OK;
+}
+
+int64_t tide_debug_bounds_violations(int32_t reset) {
+#ifdef TIDE_CHECKED
+  if (cudaDeviceSynchronize() != cudaSuccess) return -2;
+  return (int64_t)rs_kernel_bounds(reset != 0) + rs_staged_bounds(reset != 0) + rs_bulk_bounds(reset != 0) +
+         ag_kernel_bounds(reset != 0);
+#else
+  (void)reset;
+  return -1;
+#endif
+}
+
 tide_status tide_plan_check(tide_plan* pl) {
   clear_error();
   if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");

@@ -173,6 +173,13 @@ BulkLayout rs_bulk_layout(int N, int M, int L, int smem_budget);
 int rs_bulk_setup(int L, int smem_bytes);  // raises the kernel's dynamic shared-memory limit
 // Resident CTAs per SM of each kernel (occupancy), for grid sizing.
 int rs_blocks_per_sm(int L);
+// Store-check counters of the kernels' translation units (check.cuh); 0 in
+// normal builds.
+unsigned int rs_kernel_bounds(bool reset);
+unsigned int rs_staged_bounds(bool reset);
+unsigned int rs_bulk_bounds(bool reset);
+unsigned int ag_kernel_bounds(bool reset);
+int ag_bounds_selftest();  // one deliberate out-of-range check, no memory access
 int ag_blocks_per_sm();
 
 }  // namespace tide

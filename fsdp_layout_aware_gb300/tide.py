@@ -17,7 +17,8 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libtide.so")
+# TIDE_LIBRARY=checked loads the store-checked build (tests only).
+LIB_PATH = os.path.join(HERE, "libtide_checked.so" if os.environ.get("TIDE_LIBRARY") == "checked" else "libtide.so")
 
 TIDE_OK = 0
 STATUS_NAMES = {
@@ -75,6 +76,8 @@ def _load():
         "tide_plan_set_option": (i32, [vp, i32, i64]),
         "tide_plan_check": (i32, [vp]),
         "tide_plan_last_launches": (i32, [vp]),
+        "tide_debug_bounds_violations": (i64, [i32]),
+        "tide_debug_bounds_selftest": (i32, []),
         "tide_slot_pack": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
         "tide_rs_reduce_slots": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
         "tide_plan_inbox_elems": (i64, [vp]),
@@ -229,6 +232,16 @@ def tide_plan_level2_order(plan, n_dest, s, M):
     out = (ctypes.c_int32 * M)()
     _check(_lib.tide_plan_level2_order(plan, n_dest, s, out))
     return list(out)
+
+
+def tide_debug_bounds_violations(reset=False):
+    """Stores the checked build skipped since the last reset (-1: normal build)."""
+    return int(_lib.tide_debug_bounds_violations(1 if reset else 0))
+
+
+def tide_debug_bounds_selftest():
+    """One deliberate out-of-range check with no memory access (positive control)."""
+    _check(_lib.tide_debug_bounds_selftest())
 
 
 def tide_plan_items(plan, which):

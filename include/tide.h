@@ -249,6 +249,20 @@ tide_status tide_plan_check(tide_plan* plan);
  * synchronisation. */
 int32_t tide_plan_last_launches(const tide_plan* plan);
 
+/* Checked builds only (libtide_checked.so, compiled with TIDE_CHECKED): every
+ * global store of the kernels is first compared with the range of the work
+ * item it belongs to, and a store outside it is skipped and counted.  Returns
+ * the count since the last reset, after synchronising the current device
+ * (reset != 0 clears it); -1 in normal builds, -2 if the synchronisation
+ * failed. */
+int64_t tide_debug_bounds_violations(int32_t reset);
+
+/* Positive control of the store checks: launches one thread that asks the
+ * check about an address outside a made-up range, touching no memory; a
+ * checked build's count goes up by one, a normal build's stays -1.
+ * Errors: CUDA. */
+tide_status tide_debug_bounds_selftest(void);
+
 /* TIDE-RS: per-parameter bf16 gradients read in place, reduced in fp32
  * straight into every rank's packed fp32 shard at its final offset
  * ([Richland] "What shipped"; [Abstract] abstract and Figure 6;
