@@ -644,3 +644,39 @@ def test_ag_bulk_launch_count():
             plan.check()
             for p in range(w.P):
                 assert np.array_equal(params[p].cpu().numpy().view(np.uint16), expect[p]), (transport, p)
+
+
+@pytest.mark.parametrize("cfg", [2, 4])
+@pytest.mark.parametrize("kernel", ["staged", "bulk", "noalloc"])
+def test_full_size_other_reduce_kernels_sampled(cfg, kernel):
+    """The staged, bulk-copy and no-allocation reduce-scatters on the full
+    llama70b and wan22dit groups: sampled outputs against the oracle."""
+    w = configs.get(cfg)
+    geo = O.geometry(w.shapes, w.N)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        grads = device_grads(w)
+        shards = [torch.full((geo.S,), float("nan"), dtype=torch.float32, device=DEV) for _ in range(w.N)]
+        flat = tide.pointer_array([grads[r][p] for r in range(w.N) for p in range(w.P)])
+        if kernel == "staged":
+            inbox = torch.empty(tide.tide_plan_inbox_elems(plan.handle), dtype=torch.float32, device=DEV)
+            tide.tide_rs_staged(plan.handle, flat, tide.pointer_array(shards), inbox)
+        elif kernel == "bulk":
+            plan.set_option(tide.TIDE_OPT_RS_KERNEL, 1)
+            plan.rs_reduce(flat, tide.pointer_array(shards))
+        else:
+            tide.tide_rs_reduce_noalloc(plan.handle, flat, tide.pointer_array(shards))
+        plan.check()
+
+        def grad_at(src, p, idx):
+            return w.grad_values(src, p, idx.astype(np.uint64))
+
+        rng = np.random.default_rng(100 + cfg)
+        for r, x in _sample_positions(rng, geo, w.N, 400):
+            want = O.rs_element(geo, w.M, w.L, r, x, grad_at)
+            got = shards[r][x].item()
+            assert np.float32(got).view(np.uint32) == np.float32(want).view(np.uint32), (kernel, r, x, got, want)
+        # no output left unwritten (NaN sentinel)
+        for r in range(w.N):
+            assert not torch.isnan(shards[r]).any(), (kernel, r)
+        del grads, shards
+    torch.cuda.empty_cache()
