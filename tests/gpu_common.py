@@ -5,7 +5,6 @@ the oracle's answer for the same inputs."""
 import numpy as np
 import torch
 
-import fsdp_layout_aware_gb300 as tide
 import oracle.tide_oracle as O
 from synth import configs, gen
 

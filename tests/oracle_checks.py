@@ -11,7 +11,6 @@ They are plain functions so that ``test_oracle_mutations`` can plant a
 mistake in the oracle and confirm that at least one check notices it.
 """
 
-import itertools
 import json
 import os
 
