@@ -168,6 +168,7 @@ def test_ag_misaligned_pointers(src_shift, dst_shift, elem_bytes):
             assert (got[:dst_shift] == -3).all() and (got[dst_shift + w.N * geo.e[p]:] == -3).all()
 
 
+@pytest.mark.filterwarnings("ignore:overflow encountered in add:RuntimeWarning")  # the overflow to inf is the case
 def test_rs_edge_values():
     """-0.0 everywhere (result +0.0), bf16 subnormals, and sums that overflow to inf."""
     w = configs.Workload("edges", 8, 2, 4, [(16, 24)], [gen.UNIFORM], seed=1)
