@@ -55,6 +55,12 @@ MUTATIONS = {
                                   "            for c in reversed(range(b * L, min(M, (b + 1) * L))):\n                batch +="),
     "relative landing stage reads the wrong GPU": ("g = landing_gpu(s, c, L)            # where relative index",
                                                    "g = landing_gpu(s, c + 1, L)            # where relative index"),
+    "unpadded all-gather keeps a padding row": ("return [params[p][:geo.rows[p] * geo.Kp[p]] for p in range(geo.P)]",
+                                                "return [params[p][:(geo.rows[p] + 1) * geo.Kp[p]] for p in range(geo.P)]"),
+    "inbox partial at the wrong landing GPU": ("                    g = landing_gpu(s, c, L)\n",
+                                               "                    g = landing_gpu(s + 1, c, L)\n"),
+    "accumulate drops the old value": ("x = (old[r] + x).astype(np.float32)", "x = (x + x).astype(np.float32)"),
+    "single-element form without batches": ("        acc2 = np.float32(acc2 + bsum)", "        acc2 = np.float32(bsum)"),
     "average divides by M": ("x = (x / np.float32(geo.N)).astype(np.float32)",
                              "x = (x / np.float32(geo.N - 1 or 1)).astype(np.float32)"),
     "slot pack at op": ("slot[geo.N * geo.o[p]:geo.N * geo.o[p] + n] = grads[r][p][:n]",
