@@ -49,8 +49,8 @@ def parse_args(argv=None):
     ap.add_argument("--path", choices=["fused", "staged-rs", "rd-ag", "variants"], default="fused",
                     help="fused: the hot path (RS + AG per step); staged-rs: the two-stage reduce-scatter "
                          "through an inbox; rd-ag: the all-gather by recursive-doubling exchange and stage "
-                         "placement; variants: averaging / accumulating RS, Slot-Reuse pack + RS from "
-                         "slots, unpadded AG")
+                         "placement; variants: bulk-copy RS kernel, averaging / accumulating RS, "
+                         "Slot-Reuse pack + RS from slots, unpadded AG, AG transports")
     ap.add_argument("--ag-transport", choices=["sm", "bulk", "copy-engines"], default="sm",
                     help="how tide_ag_place moves the pieces (default: the SM kernel)")
     ap.add_argument("--nodes", type=int, default=0,
@@ -591,7 +591,8 @@ def run_rd_ag(args, local_rank):
 
 def run_variants(args, local_rank):
     """The listed variants, each timed alone on the workload: the reduce-scatter
-    averaged over N and/or accumulated into the previous shard, Slot-Reuse
+    on the bulk-copy kernel (M <= 8), averaged over N and/or accumulated into
+    the previous shard, Slot-Reuse
     (pack into the vacated all-gather slot, then the reduce-scatter reading
     the slots), and the all-gather writing only the real rows."""
     import torch
@@ -612,6 +613,10 @@ def run_variants(args, local_rank):
         res[name] = {"ms": round(t * 1e3, 4), "bytes": nbytes, "GB_s": round(nbytes / t / 1e9, 1)}
 
     timed("rs_plain", lambda: plan.rs_reduce(gp, sp, stream), nb["rs_bytes"])
+    if w.M <= 8:  # the bulk-copy pipeline holds at most 8 node partials per thread
+        plan.set_option(tide.TIDE_OPT_RS_KERNEL, 1)
+        timed("rs_bulk", lambda: plan.rs_reduce(gp, sp, stream), nb["rs_bytes"])
+        plan.set_option(tide.TIDE_OPT_RS_KERNEL, 0)
     plan.set_option(tide.TIDE_OPT_RS_AVERAGE, 1)
     timed("rs_average", lambda: plan.rs_reduce(gp, sp, stream), nb["rs_bytes"])
     plan.set_option(tide.TIDE_OPT_RS_ACCUMULATE, 1)
