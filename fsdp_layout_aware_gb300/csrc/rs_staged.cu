@@ -117,10 +117,24 @@ __global__ void __launch_bounds__(kRsThreads, 4) rs_sum_kernel(const __grid_cons
 
 // Stage 2.  blockIdx.y is the destination rank.  For each slice, the first
 // M threads list where the slice's partials landed, in the plan's level-2
-// order, in shared memory; the threads then stream the slice, four outputs
-// each per round, adding the partials in that order.  Keeping the list in
-// shared memory keeps the kernel at 32 registers, so eight CTAs fit per SM
-// (five when M > L, where the batch sums take 48 registers).
+// order, in shared memory.
+__device__ __forceinline__ void list_partials(const RsArgs& a, const float** part, int n_dest, int l_dest, int s,
+                                              int64_t lo) {
+  const int M = a.M, L = a.L;
+  if ((int)threadIdx.x < M) {
+    const int k = threadIdx.x;
+    const int node = a.order[(n_dest * L + s) * M + k];
+    const int c = ((n_dest - node) % M + M) % M;  // relative index of the k-th source
+    const int g = ((s - c) % L + L) % L;            // the GPU its slice s landed on
+    part[k] = a.inbox + ((int64_t)(n_dest * L + g) * M + c) * (int64_t)L * a.slice_len +
+              (int64_t)l_dest * a.slice_len - lo;
+  }
+}
+
+// The threads then stream the slice, four outputs each per round, adding the
+// partials in that order.  Keeping the list in shared memory keeps the kernel
+// at 32 registers, so eight CTAs fit per SM (five when M > L, where the batch
+// sums take 48 registers).  Used for M = 1 and M > L.
 template <bool kBatched>
 __global__ void __launch_bounds__(256, kBatched ? 5 : 8) rs_land_kernel(const __grid_constant__ RsArgs a) {
   __shared__ const float* part[kMaxM];
@@ -129,19 +143,12 @@ __global__ void __launch_bounds__(256, kBatched ? 5 : 8) rs_land_kernel(const __
   const int r = blockIdx.y;
   const int n_dest = r / L, l_dest = r % L;
   float* out = a.shard_tab[r];
-  const int64_t slot = (int64_t)L * B;
   const int64_t step = (int64_t)gridDim.x * blockDim.x * 4;
   for (int s = 0; s < L; ++s) {
     const int64_t lo = (int64_t)s * B, hi = min(S, lo + B);
     if (lo >= hi) break;
     __syncthreads();  // the previous slice's readers of part[] are done
-    if ((int)threadIdx.x < M) {
-      const int k = threadIdx.x;
-      const int node = a.order[(n_dest * L + s) * M + k];
-      const int c = ((n_dest - node) % M + M) % M;  // relative index of the k-th source
-      const int g = ((s - c) % L + L) % L;            // the GPU its slice s landed on
-      part[k] = a.inbox + ((int64_t)(n_dest * L + g) * M + c) * slot + (int64_t)l_dest * B - lo;
-    }
+    list_partials(a, part, n_dest, l_dest, s, lo);
     __syncthreads();
     const int np = M;
     for (int64_t x0 = lo + (int64_t)blockIdx.x * blockDim.x * 4 + threadIdx.x; x0 < hi; x0 += step) {
@@ -179,6 +186,93 @@ __global__ void __launch_bounds__(256, kBatched ? 5 : 8) rs_land_kernel(const __
   }
 }
 
+// The same for 2 <= M <= L, with the partials loaded kGroup at a time into
+// registers before any of them is added: with kGroup = 2 a thread has eight
+// loads in flight instead of waiting for one partial's loads before issuing
+// the next one's.  The additions still run partial by partial in the plan's
+// order.  Still 32 registers and eight CTAs per SM.  Measured against the
+// one-partial-at-a-time loop on one box, alternating (whole staged
+// reduce-scatter, filling the GPU / with the pages' 16 + 4 CTAs): qwen3moe
+// (M = 2) 4.591 vs 4.672 ms / 12.29 vs 16.84 ms; wan22dit (M = 8) 9.871 vs
+// 9.924 / 11.89 vs 14.35 ms; uneven (M = 6) 2.324 vs 2.323 / 3.10 vs 3.53 ms.
+// With M = 1 or M > L it was slower, so those keep rs_land_kernel.  (Written as a template over the
+// batching flag and group size: the same loop as a plain kernel measured
+// slower.)
+template <bool kBatched, int kGroup>
+__global__ void __launch_bounds__(256, kBatched ? 5 : 8) rs_land_grouped_kernel(const __grid_constant__ RsArgs a) {
+  __shared__ const float* part[kMaxM];
+  const int M = a.M, L = a.L;
+  const int64_t S = a.S, B = a.slice_len;
+  const int r = blockIdx.y;
+  const int n_dest = r / L, l_dest = r % L;
+  float* out = a.shard_tab[r];
+  const int64_t slot = (int64_t)L * B;
+  const int64_t step = (int64_t)gridDim.x * blockDim.x * 4;
+  for (int s = 0; s < L; ++s) {
+    const int64_t lo = (int64_t)s * B, hi = min(S, lo + B);
+    if (lo >= hi) break;
+    __syncthreads();  // the previous slice's readers of part[] are done
+    if ((int)threadIdx.x < M) {
+      const int k = threadIdx.x;
+      const int node = a.order[(n_dest * L + s) * M + k];
+      const int c = ((n_dest - node) % M + M) % M;  // relative index of the k-th source
+      const int g = ((s - c) % L + L) % L;            // the GPU its slice s landed on
+      part[k] = a.inbox + ((int64_t)(n_dest * L + g) * M + c) * slot + (int64_t)l_dest * B - lo;
+    }
+    __syncthreads();
+    for (int64_t x0 = lo + (int64_t)blockIdx.x * blockDim.x * 4 + threadIdx.x; x0 < hi; x0 += step) {
+      // With M <= L there is one batch and acc is its sum directly.
+      float acc[4] = {0.f, 0.f, 0.f, 0.f}, bsum[kBatched ? 4 : 1] = {0.f};
+      for (int j0 = 0; j0 < M; j0 += kGroup) {
+        float v[kGroup][4];
+#pragma unroll
+        for (int q = 0; q < kGroup; ++q) {
+          const float* pj = part[min(j0 + q, M - 1)];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int64_t x = x0 + (int64_t)u * blockDim.x;
+            v[q][u] = (j0 + q < M && x < hi) ? __ldcs(pj + x) : 0.f;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kGroup; ++q) {
+          const int j = j0 + q;
+          if (j >= M) break;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if constexpr (kBatched)
+              bsum[u] = __fadd_rn(bsum[u], v[q][u]);
+            else
+              acc[u] = __fadd_rn(acc[u], v[q][u]);
+          }
+          if constexpr (kBatched) {
+            if ((j + 1) % L == 0 || j + 1 == M) {  // end of a batch
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                acc[u] = __fadd_rn(acc[u], bsum[u]);
+                bsum[u] = 0.f;
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t x = x0 + (int64_t)u * blockDim.x;
+        if (x < hi && store_ok(out + x, 4, out + lo, out + hi))
+          __stcs(out + x, epilogue1(acc[u], out + x, a.epilogue, M * L));
+      }
+    }
+  }
+}
+
+using LandKernel = void (*)(RsArgs);
+
+LandKernel land_kernel_for(int M, int L) {
+  if (M > L) return rs_land_kernel<true>;
+  return M == 1 ? rs_land_kernel<false> : rs_land_grouped_kernel<false, 2>;
+}
+
 template <int L>
 int launch_sum_t(const RsArgs& a, int grid, cudaStream_t s) {
   rs_sum_kernel<L><<<grid, kRsThreads, 0, s>>>(a);
@@ -203,11 +297,13 @@ int launch_rs_staged(const RsArgs& a, int sum_grid, int land_grid_x, void* strea
     case 8: err = launch_sum_t<8>(a, sum_grid, s); break;
   }
   if (err != cudaSuccess) return err;
-  if (a.M > a.L)
-    rs_land_kernel<true><<<dim3(land_grid_x, a.N), 256, 0, s>>>(a);
-  else
-    rs_land_kernel<false><<<dim3(land_grid_x, a.N), 256, 0, s>>>(a);
+  land_kernel_for(a.M, a.L)<<<dim3(land_grid_x, a.N), 256, 0, s>>>(a);
   return (int)cudaGetLastError();
+}
+
+int rs_land_blocks_per_sm(int M, int L) {
+  int n = 0;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, land_kernel_for(M, L), 256, 0) == cudaSuccess ? n : 0;
 }
 
 }  // namespace tide

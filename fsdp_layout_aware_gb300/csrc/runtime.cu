@@ -599,7 +599,7 @@ tide_status tide_rs_staged(tide_plan* pl, const void* const* grads, float* const
   a.inbox = inbox;
   const int64_t sum_grid =
       sum_ctas_per_rank > 0 ? std::min<int64_t>((int64_t)sum_ctas_per_rank * pl->N, 1 << 20) : pl->rs_grid;
-  const int land_per_sm = pl->M > pl->L ? 5 : 8;  // resident landing CTAs per SM (48 / 32 registers)
+  const int land_per_sm = std::max(1, rs_land_blocks_per_sm(pl->M, pl->L));  // resident landing CTAs per SM
   const int land_x =
       landing_ctas_per_rank > 0 ? landing_ctas_per_rank : std::max(1, pl->num_sms * land_per_sm / pl->N);
   pl->last_launches = 2;
