@@ -422,6 +422,21 @@ def oracle_step(w, geo, grads, ag_in):
 SAMPLE_ROW_DIV = {"llama70b": 64, "qwen3moe": 16, "wan22dit": 64, "uneven": 8, "tiny": 1}
 
 
+def host_info():
+    """The host the CPU baseline ran on: architecture, logical cores, CPU model."""
+    import platform
+    model = platform.processor() or ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"machine": platform.machine(), "nproc": os.cpu_count(), "cpu": model}
+
+
 def cpu_baseline(w, seconds):
     """The oracle as it stands, single-threaded, over repeated passes of a row
     subset of the same workload until `seconds` of CPU time are spent."""
@@ -436,7 +451,7 @@ def cpu_baseline(w, seconds):
         if el >= seconds:
             break
     gbs = (nb["rs_bytes"] + nb["ag_bytes"]) * passes / el / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "host": host_info(),
             "sample": f"{w.name} rows/{div} (N={ws.N}, G={nb['G']}, S={nb['S']}): {passes} passes of RS+AG "
                       f"in {el:.1f} s on one host core (numpy)",
             "elements_per_s": round((nb["rs_elems"] + nb["ag_elems"]) * passes / el, 1)}
@@ -476,7 +491,8 @@ def run_reference(args, rank, world):
         "data": "synthetic (seeded SplitMix64 bf16)",
         "config": {"workload": f"{w.name}: {w.notes}", "N": w.N, "M": w.M, "L": w.L, "P": w.P,
                    "sample_row_div": div},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+                         "host": host_info()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "elements_per_s": round((nb["rs_elems"] + nb["ag_elems"]) * args.steps / el, 1),
     }
