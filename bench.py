@@ -568,9 +568,11 @@ def run_staged_rs(args, local_rank):
 
 
 def run_rd_ag(args, local_rank):
-    """The all-gather the pages' way for one destination node: per rail, the
+    """The all-gather the pages' way for one destination node: the
     recursive-doubling exchange between the M nodes' stage buffers (copy
-    engines), then the strided stage placement into the parameters."""
+    engines or SM kernel), then the strided stage placement into the
+    parameters; timed rail by rail, and for every rail at once (stage init,
+    the exchange of all rails, one placement), which is `value`."""
     import torch
 
     import fsdp_layout_aware_gb300 as tide
@@ -587,21 +589,40 @@ def run_rd_ag(args, local_rank):
             tide.tide_ag_rd_exchange(plan.handle, stages, 2, stream)
             tide.tide_ag_stage_place(plan.handle, stages[0], 0, rail, pp, 2, stream)
 
+    # Every rail at once (the rails run concurrently on the pages): one stage
+    # init launch, the rounds of all rails, one placement from the slots.
+    all_stages = [torch.empty(M * S, dtype=torch.int16, device=dev) for _ in range(L * M)]
+    sh_p, st_p = tide.pointer_array(ag_in), tide.pointer_array(all_stages)
+    slot_p = tide.pointer_array(tide.stage_shard_pointers(all_stages, 0, M, L, S, 2))
+
+    def step_rails():
+        tide.tide_ag_stage_init(plan.handle, sh_p, st_p, 2, stream)
+        tide.tide_ag_rd_exchange_rails(plan.handle, st_p, 2, stream)
+        plan.ag_place(slot_p, pp, 2, stream)
+
+    # bytes moved per step (read + write): every shard into its slot 0, the
+    # M - 1 pieces every node receives per rail, and the placement
+    init_bytes = 4 * w.N * S
     place_bytes = 4 * w.N * S
     exch_bytes = L * M * (M - 1) * S * 2 * 2
-    res = {}
+    moved = init_bytes + place_bytes + exch_bytes
+    res, res_rails = {}, {}
     with torch.cuda.stream(stream):
         for name, mode in (("copy_engines", 0), ("sm_kernel", 1)):
             plan.set_option(tide.TIDE_OPT_RD_EXCHANGE, mode)
             t = _event_time(step, max(1, args.steps // 8), args.warmup, stream)
-            res[name] = {"ms_per_step": round(t * 1e3, 4), "GB_s": round((place_bytes + exch_bytes) / t / 1e9, 1)}
+            res[name] = {"ms_per_step": round(t * 1e3, 4), "GB_s": round(moved / t / 1e9, 1)}
+            t = _event_time(step_rails, args.steps, args.warmup, stream)
+            res_rails[name] = {"ms_per_step": round(t * 1e3, 4), "GB_s": round(moved / t / 1e9, 1)}
         ta = _event_time(lambda: plan.ag_place(tide.pointer_array(ag_in), pp, 2, stream), args.steps, args.warmup,
                          stream)
+    plan.check()
     return {"path": "rd-ag", "metric": METRIC, "unit": "GB/s", "n_gpus": 1, "dtype": "bf16 copy", "data": "synthetic",
             "config": {"workload": f"{w.name}: {w.notes}", "N": w.N, "M": M, "L": L,
                        "rounds": tide.tide_rd_rounds(M)},
-            "placement_bytes": place_bytes, "exchange_bytes": exch_bytes, "exchange": res,
-            "ms_per_step": res["copy_engines"]["ms_per_step"], "value": res["copy_engines"]["GB_s"],
+            "stage_init_bytes": init_bytes, "placement_bytes": place_bytes, "exchange_bytes": exch_bytes,
+            "exchange": res, "exchange_all_rails": res_rails,
+            "ms_per_step": res_rails["copy_engines"]["ms_per_step"], "value": res_rails["copy_engines"]["GB_s"],
             "direct_landing_ms": round(ta * 1e3, 4)}
 
 

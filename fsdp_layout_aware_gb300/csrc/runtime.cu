@@ -63,12 +63,18 @@ void release_device_state(tide_plan* pl) {
     pl->rail_n_items[l] = pl->rail_n_units[l] = 0;
   }
   for (int d = 0; d < tide_plan::kMaxRounds; ++d) {
-    if (pl->d_rd_items[d]) cudaFree(pl->d_rd_items[d]);
-    if (pl->d_rd_units[d]) cudaFree(pl->d_rd_units[d]);
-    pl->d_rd_items[d] = nullptr;
-    pl->d_rd_units[d] = nullptr;
-    pl->rd_n_items[d] = pl->rd_n_units[d] = 0;
+    for (void* q : {(void*)pl->d_rd_items[d], (void*)pl->d_rd_units[d], (void*)pl->d_rdr_items[d],
+                    (void*)pl->d_rdr_units[d]})
+      if (q) cudaFree(q);
+    pl->d_rd_items[d] = pl->d_rdr_items[d] = nullptr;
+    pl->d_rd_units[d] = pl->d_rdr_units[d] = nullptr;
+    pl->rd_n_items[d] = pl->rd_n_units[d] = pl->rdr_n_items[d] = pl->rdr_n_units[d] = 0;
   }
+  for (void* q : {(void*)pl->d_init_items, (void*)pl->d_init_units})
+    if (q) cudaFree(q);
+  pl->d_init_items = nullptr;
+  pl->d_init_units = nullptr;
+  pl->init_n_items = pl->init_units = 0;
   if (pl->d_status) cudaFree(pl->d_status);
   pl->d_status = nullptr;
   for (void* q : {(void*)pl->d_agu_items, (void*)pl->d_agu_units, (void*)pl->d_pack_items, (void*)pl->d_pack_units})
@@ -227,6 +233,29 @@ tide_status ensure_device(tide_plan* pl) {
       pl->rd_n_items[d] = (int64_t)v.size();
       if ((err = upload(v, &pl->d_rd_items[d], &pl->d_rd_units[d], &pl->rd_n_units[d])) != cudaSuccess)
         return bail(err, "uploading the exchange rounds");
+      // The same round on every rail: buffer l*M + n is rail l's node n.
+      std::vector<AgItem> vr;
+      vr.reserve(v.size() * pl->L);
+      for (int32_t l = 0; l < pl->L; ++l)
+        for (const AgItem& it : v) {
+          AgItem x = it;
+          x.p = l * pl->M + it.p;
+          x.r = l * pl->M + it.r;
+          vr.push_back(x);
+        }
+      pl->rdr_n_items[d] = (int64_t)vr.size();
+      if ((err = upload(vr, &pl->d_rdr_items[d], &pl->d_rdr_units[d], &pl->rdr_n_units[d])) != cudaSuccess)
+        return bail(err, "uploading the exchange rounds of all rails");
+    }
+    // Stage init: rank r = n*L + l's shard to slot 0 of stage buffer l*M + n.
+    if (pl->S > 0) {
+      std::vector<AgItem> v;
+      for (int32_t r = 0; r < pl->N; ++r)
+        for (int64_t e = 0; e < pl->S; e += 32768)
+          v.push_back(AgItem{e, e, (int32_t)std::min<int64_t>(32768, pl->S - e), (r % pl->L) * pl->M + r / pl->L, r, 0});
+      pl->init_n_items = (int64_t)v.size();
+      if ((err = upload(v, &pl->d_init_items, &pl->d_init_units, &pl->init_units)) != cudaSuccess)
+        return bail(err, "uploading the stage-init list");
     }
     // Bulk-copy all-gather lists, for bf16 and 16-byte aligned base pointers.
     {
@@ -275,7 +304,7 @@ tide_status acquire_slot(tide_plan* pl, tide_plan::Slot** out) {
   return TIDE_OK;
 }
 
-enum TableKind { TABLE_RS = 0, TABLE_AG = 1, TABLE_PACK = 2, TABLE_STAGE = 3, TABLE_RD = 4 };
+enum TableKind { TABLE_RS = 0, TABLE_AG = 1, TABLE_PACK = 2, TABLE_STAGE = 3, TABLE_RD = 4, TABLE_RDR = 5, TABLE_INIT = 6 };
 
 // Puts the pointer table just built in pl->table_scratch (its first `bytes`)
 // on the device.  If the previous table of this kind is byte-for-byte the
@@ -819,6 +848,111 @@ tide_status tide_ag_rd_exchange(tide_plan* pl, void* const* stages, int32_t elem
     }
   }
   return TIDE_OK;
+}
+
+tide_status tide_ag_rd_exchange_rails(tide_plan* pl, void* const* stages, int32_t elem_bytes, void* stream) {
+  clear_error();
+  if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  pl->last_launches = 0;
+  if (elem_bytes != 2 && elem_bytes != 4) return fail(TIDE_ERR_INVALID_ARG, "elem_bytes must be 2 or 4");
+  if (pl->S == 0 || pl->M == 1) return TIDE_OK;
+  if (!stages) return fail(TIDE_ERR_INVALID_ARG, "stages array is NULL");
+  const int32_t nb = pl->L * pl->M;
+  const size_t piece = (size_t)pl->S * elem_bytes;
+  for (int32_t i = 0; i < nb; ++i) {
+    if (!stages[i]) return fail(TIDE_ERR_INVALID_ARG, "stages[" + std::to_string(i) + "] is NULL");
+    if ((uintptr_t)stages[i] % elem_bytes) return fail(TIDE_ERR_ALIGNMENT, "stage pointer not element-aligned");
+    for (int32_t j = 0; j < i; ++j)
+      if (stages[j] == stages[i]) return fail(TIDE_ERR_INVALID_ARG, "two stage buffers are the same");
+  }
+  if (pl->check_overlap) {
+    std::vector<ByteRange> in, out;
+    add_ranges((const void* const*)stages, nb, (size_t)pl->M * piece, "stages", &out);
+    tide_status st = check_overlap(in, out);
+    if (st != TIDE_OK) return st;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  const int32_t rounds = tide_rd_rounds(pl->M);
+  if (pl->rd_exchange == 1) {
+    // SM kernel: one launch per round covers the rounds' copies of every rail.
+    tide_status st = ensure_device(pl);
+    if (st != TIDE_OK) return st;
+    if (rounds > tide_plan::kMaxRounds) return fail(TIDE_ERR_UNIMPLEMENTED, "more than 5 exchange rounds");
+    void** tab = (void**)pl->table_scratch.data();
+    for (int32_t i = 0; i < nb; ++i) tab[i] = stages[i];
+    tide_plan::Slot* slot = nullptr;
+    if ((st = commit_table(pl, TABLE_RDR, (size_t)nb * 8, s, &slot)) != TIDE_OK) return st;
+    for (int32_t d = 0; d < rounds; ++d) {
+      AgArgs a;
+      a.items = pl->d_rdr_items[d];
+      a.n_items = pl->rdr_n_items[d];
+      a.units = pl->d_rdr_units[d];
+      a.n_units = pl->rdr_n_units[d];
+      a.shard_tab = (const unsigned char* const*)slot->dev;
+      a.param_tab = (unsigned char* const*)slot->dev;
+      a.elem_bytes = elem_bytes;
+      const int lerr = launch_ag(a, pl->ag_grid, stream);
+      ++pl->last_launches;
+      if (d + 1 < rounds && lerr != cudaSuccess) return cuda_fail((cudaError_t)lerr, "exchange launch");
+      if (d + 1 == rounds) return finish(slot, lerr, s, "exchange launch");
+    }
+    return TIDE_OK;
+  }
+  for (int32_t d = 0; d < rounds; ++d) {
+    const int32_t have = 1 << d;
+    const int32_t c = tide_rd_send_count(pl->M, d);
+    for (int32_t l = 0; l < pl->L; ++l)
+      for (int32_t n = 0; n < pl->M; ++n) {
+        const unsigned char* from = (const unsigned char*)stages[l * pl->M + (n + have) % pl->M];
+        unsigned char* to = (unsigned char*)stages[l * pl->M + n] + (size_t)have * piece;
+        TIDE_CUDA(cudaMemcpyAsync(to, from, (size_t)c * piece, cudaMemcpyDeviceToDevice, s), "exchange copy");
+      }
+  }
+  return TIDE_OK;
+}
+
+tide_status tide_ag_stage_init(tide_plan* pl, const void* const* shards, void* const* stages, int32_t elem_bytes,
+                               void* stream) {
+  clear_error();
+  if (!pl) return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+  pl->last_launches = 0;
+  if (elem_bytes != 2 && elem_bytes != 4) return fail(TIDE_ERR_INVALID_ARG, "elem_bytes must be 2 or 4");
+  if (pl->S == 0) return TIDE_OK;
+  if (!shards || !stages) return fail(TIDE_ERR_INVALID_ARG, "shards or stages array is NULL");
+  for (int32_t r = 0; r < pl->N; ++r) {
+    if (!shards[r]) return fail(TIDE_ERR_INVALID_ARG, "shards[" + std::to_string(r) + "] is NULL");
+    if ((uintptr_t)shards[r] % elem_bytes) return fail(TIDE_ERR_ALIGNMENT, "shard pointer not element-aligned");
+    if (!stages[r]) return fail(TIDE_ERR_INVALID_ARG, "stages[" + std::to_string(r) + "] is NULL");
+    if ((uintptr_t)stages[r] % elem_bytes) return fail(TIDE_ERR_ALIGNMENT, "stage pointer not element-aligned");
+  }
+  if (pl->check_overlap) {
+    std::vector<ByteRange> in, out;
+    add_ranges(shards, pl->N, (size_t)pl->S * elem_bytes, "shards", &in);
+    add_ranges((const void* const*)stages, pl->N, (size_t)pl->S * elem_bytes, "stages", &out);
+    tide_status st = check_overlap(in, out);
+    if (st != TIDE_OK) return st;
+  }
+  tide_status st = ensure_device(pl);
+  if (st != TIDE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  const void** stab = (const void**)pl->table_scratch.data();
+  void** dtab = (void**)(pl->table_scratch.data() + (size_t)pl->N * 8);
+  for (int32_t r = 0; r < pl->N; ++r) {
+    stab[r] = shards[r];
+    dtab[r] = stages[r];
+  }
+  tide_plan::Slot* slot = nullptr;
+  if ((st = commit_table(pl, TABLE_INIT, (size_t)pl->N * 16, s, &slot)) != TIDE_OK) return st;
+  AgArgs a;
+  a.items = pl->d_init_items;
+  a.n_items = pl->init_n_items;
+  a.units = pl->d_init_units;
+  a.n_units = pl->init_units;
+  a.shard_tab = (const unsigned char* const*)slot->dev;
+  a.param_tab = (unsigned char* const*)(slot->dev + (size_t)pl->N * 8);
+  a.elem_bytes = elem_bytes;
+  pl->last_launches = 1;
+  return finish(slot, launch_ag(a, pl->ag_grid, stream), s, "stage init launch");
 }
 
 tide_status tide_ag_stage_place(tide_plan* pl, const void* stage, int32_t node, int32_t rail, void* const* params,

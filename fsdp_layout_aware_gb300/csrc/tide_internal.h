@@ -240,6 +240,18 @@ struct tide_plan {
   tide::UnitStart* d_rd_units[kMaxRounds] = {};
   int64_t rd_n_items[kMaxRounds] = {};
   int64_t rd_n_units[kMaxRounds] = {};
+  // The same rounds for every rail at once (tide_ag_rd_exchange_rails): the
+  // tables hold the L*M stage buffers, rail l's node n at l*M + n.
+  tide::AgItem* d_rdr_items[kMaxRounds] = {};
+  tide::UnitStart* d_rdr_units[kMaxRounds] = {};
+  int64_t rdr_n_items[kMaxRounds] = {};
+  int64_t rdr_n_units[kMaxRounds] = {};
+  // tide_ag_stage_init: rank r's shard (r = n*L + l) to slot 0 of stage
+  // buffer l*M + n.
+  tide::AgItem* d_init_items = nullptr;
+  tide::UnitStart* d_init_units = nullptr;
+  int64_t init_n_items = 0;
+  int64_t init_units = 0;
   int32_t rd_exchange = 0;                 // 0: copy engines, 1: SM kernel
   int32_t ag_transport = TIDE_AG_SM;       // TIDE_OPT_AG_TRANSPORT (tide_ag_transport)
   mutable int32_t last_launches = 0;       // kernels launched by the latest compute call
@@ -274,9 +286,10 @@ struct tide_plan {
   size_t slot_bytes = 0;
   // Pointer tables are built in table_scratch; a call whose table equals the
   // previous one of its kind reuses that slot's device copy (no upload).
-  static constexpr int kTableKinds = 5;  // RS, AG, Slot-Reuse pack, stage placement, exchange
+  static constexpr int kTableKinds = 7;  // RS, AG, Slot-Reuse pack, stage placement, exchange,
+                                         // exchange of all rails, stage init
   std::vector<unsigned char> table_scratch;
-  int cached_slot[kTableKinds] = {-1, -1, -1, -1, -1};
+  int cached_slot[kTableKinds] = {-1, -1, -1, -1, -1, -1, -1};
   uint64_t cached_gen[kTableKinds] = {};
   uint64_t next_gen = 0;
 };

@@ -86,6 +86,8 @@ def _load():
         "tide_rd_send_count": (i32, [i32, i32]),
         "tide_ag_rd_exchange": (i32, [vp, ctypes.POINTER(vp), i32, vp]),
         "tide_ag_stage_place": (i32, [vp, vp, i32, i32, ctypes.POINTER(vp), i32, vp]),
+        "tide_ag_stage_init": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp]),
+        "tide_ag_rd_exchange_rails": (i32, [vp, ctypes.POINTER(vp), i32, vp]),
         "tide_status_string": (ctypes.c_char_p, [i32]),
         "tide_last_error": (ctypes.c_char_p, []),
     }
@@ -205,6 +207,24 @@ def tide_ag_rd_exchange(plan, stages, elem_bytes, stream=None):
 def tide_ag_stage_place(plan, stage, node, rail, params, elem_bytes, stream=None):
     _check(_lib.tide_ag_stage_place(plan, _ptr(stage), node, rail, _ptr_array(params), elem_bytes,
                                     _stream(stream)))
+
+
+def tide_ag_stage_init(plan, shards, stages, elem_bytes, stream=None):
+    """shards: N device buffers; stages: L*M stage buffers (rail l's node n at l*M + n)."""
+    _check(_lib.tide_ag_stage_init(plan, _ptr_array(shards), _ptr_array(stages), elem_bytes, _stream(stream)))
+
+
+def tide_ag_rd_exchange_rails(plan, stages, elem_bytes, stream=None):
+    """stages: L*M device buffers of M*S elements, rail l's node n at l*M + n."""
+    _check(_lib.tide_ag_rd_exchange_rails(plan, _ptr_array(stages), elem_bytes, _stream(stream)))
+
+
+def stage_shard_pointers(stages, node, M, L, S, elem_bytes):
+    """Addresses that make tide_ag_place place node `node`'s pieces of every
+    rail from the stage buffers (rail l's node n at l*M + n): rank r's shard
+    is slot (r // L - node) mod M of stages[(r % L) * M + node]."""
+    base = [_ptr(x) for x in stages]
+    return [base[(r % L) * M + node] + ((r // L - node) % M) * S * elem_bytes for r in range(M * L)]
 
 
 def tide_plan_set_option(plan, option, value):

@@ -414,6 +414,43 @@ tide_status tide_ag_rd_exchange(tide_plan* plan, void* const* stages, int32_t el
 tide_status tide_ag_stage_place(tide_plan* plan, const void* stage, int32_t node, int32_t rail,
                                 void* const* params, int32_t elem_bytes, void* stream);
 
+/* ---- Every rail at once --------------------------------------------------
+ * On the pages the L rails exchange concurrently, each over its own NICs.
+ * These calls emulate all of them together, in one launch per step instead
+ * of one per rail.  Buffer l*M + n of a `stages` array is node n's stage
+ * buffer on rail l (M*S elements, slot k at k*S); all L*M are distinct,
+ * caller-owned device buffers. */
+
+/* Slot 0 of every stage buffer gets its own shard:
+ * stages[l*M + n][0 .. S) = shards[n*L + l][0 .. S).
+ *   shards      host array [N] of device pointers (S elements each), read
+ *   stages      host array [L*M] of device pointers, slot 0 written
+ *   elem_bytes  2 or 4
+ * One all-gather kernel launch on `stream`.  Errors: INVALID_ARG (null
+ * pointers; with TIDE_OPT_CHECK_OVERLAP, a slot 0 overlapping a shard or
+ * another slot 0), ALIGNMENT (pointer not element-aligned), CUDA,
+ * OUT_OF_MEMORY, DEVICE_MISMATCH. */
+tide_status tide_ag_stage_init(tide_plan* plan, const void* const* shards, void* const* stages, int32_t elem_bytes,
+                               void* stream);
+
+/* tide_ag_rd_exchange on every rail: afterwards slot k of stages[l*M + n]
+ * holds rank ((n + k) mod M)*L + l's shard, for every l and n.  With
+ * TIDE_OPT_RD_EXCHANGE = 1 each round is one SM kernel launch covering all
+ * rails; with copy engines (default) each round is L*M copies.
+ *   stages      host array [L*M] of device pointers, slot 0 already filled
+ *               (tide_ag_stage_init); slots 1..M-1 are overwritten
+ * Errors: INVALID_ARG (null or repeated buffers; with
+ * TIDE_OPT_CHECK_OVERLAP, overlapping buffers), ALIGNMENT, UNIMPLEMENTED
+ * (SM exchange with more than 5 rounds, M > 32), CUDA, OUT_OF_MEMORY,
+ * DEVICE_MISMATCH.
+ *
+ * Placement from every rail at once needs no entry point of its own: node
+ * `node`'s pieces land with tide_ag_place given
+ * shards[r] = stages[(r % L)*M + node] + ((r / L - node) mod M) * S elements,
+ * which writes params[p][r*e_p + e] from slot (r/L - node) mod M of rail
+ * r % L, as tide_ag_stage_place does rail by rail. */
+tide_status tide_ag_rd_exchange_rails(tide_plan* plan, void* const* stages, int32_t elem_bytes, void* stream);
+
 /* Static text for a status code. */
 const char* tide_status_string(tide_status status);
 

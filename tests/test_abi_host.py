@@ -395,3 +395,62 @@ def test_last_launches_without_a_gpu():
     with tide.TidePlan([(8, 64)], 4, 1, 4) as plan:
         assert plan.last_launches() == 0          # nothing ran yet
     assert tide.TIDE_AG_SM == 0 and tide.TIDE_AG_BULK == 2
+
+
+def test_all_rails_arguments_without_a_gpu():
+    """Argument errors of the every-rail calls come back before any device work."""
+    with tide.TidePlan([(8, 64), (4, 64), (12, 64)], 4, 2, 2) as plan:
+        stages = [0x1000000 * (i + 1) for i in range(4)]      # rail l's node n at l*M + n
+        shards = [0x10000000 * (r + 1) for r in range(4)]
+        cases = [
+            (lambda: tide.tide_ag_rd_exchange_rails(plan.handle, stages[:3] + [None], 2, 0), 1),
+            (lambda: tide.tide_ag_rd_exchange_rails(plan.handle, stages[:3] + [stages[1]], 2, 0), 1),
+            (lambda: tide.tide_ag_rd_exchange_rails(plan.handle, stages[:3] + [stages[3] + 1], 2, 0), 2),
+            (lambda: tide.tide_ag_rd_exchange_rails(plan.handle, stages, 3, 0), 1),
+            (lambda: tide.tide_ag_stage_init(plan.handle, shards, stages[:3] + [None], 2, 0), 1),
+            (lambda: tide.tide_ag_stage_init(plan.handle, [None] + shards[1:], stages, 2, 0), 1),
+            (lambda: tide.tide_ag_stage_init(plan.handle, shards, [stages[0] + 2] + stages[1:], 4, 0), 2),
+            (lambda: tide.tide_ag_stage_init(plan.handle, [shards[0] + 1] + shards[1:], stages, 2, 0), 2),
+            (lambda: tide.tide_ag_stage_init(plan.handle, shards, stages, 8, 0), 1),
+        ]
+        for fn, status in cases:
+            with pytest.raises(tide.TideError) as err:
+                fn()
+            assert err.value.status == status
+    with tide.TidePlan([(8, 64)], 4, 1, 4) as plan:   # one node: nothing to exchange
+        tide.tide_ag_rd_exchange_rails(plan.handle, [None] * 4, 2, 0)
+    with tide.TidePlan([], 4, 2, 2) as plan:          # empty group: nothing to copy
+        tide.tide_ag_stage_init(plan.handle, [None] * 4, [None] * 4, 2, 0)
+        tide.tide_ag_rd_exchange_rails(plan.handle, [None] * 4, 2, 0)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers must never reach a device")
+def test_all_rails_overlap_check():
+    with tide.TidePlan([(8, 64), (4, 64), (12, 64)], 4, 2, 2) as plan:
+        plan.set_option(tide.TIDE_OPT_CHECK_OVERLAP, 1)
+        S = plan.S
+        stages = [0x1000000 * (i + 1) for i in range(4)]
+        stages[2] = stages[1] + 2 * S * 2 - 2               # last element of buffer 1
+        st, msg = _overlap_status(lambda: tide.tide_ag_rd_exchange_rails(plan.handle, stages, 2, 0))
+        assert st == 1 and "stages" in msg
+        stages = [0x1000000 * (i + 1) for i in range(4)]
+        shards = [0x10000000 * (r + 1) for r in range(4)]
+        shards[3] = stages[0] + 2                            # a shard inside slot 0 of buffer 0
+        st, msg = _overlap_status(lambda: tide.tide_ag_stage_init(plan.handle, shards, stages, 2, 0))
+        assert st == 1 and "shards[3]" in msg and "stages[0]" in msg
+
+
+def test_stage_shard_pointers_follow_the_slot_rule():
+    """stage_shard_pointers(node) must hand rank r the slot k of rail r % L
+    whose content the exchange defines: slot k of node `node` holds rank
+    ((node + k) mod M) * L + rail."""
+    for M, L, S, eb in [(1, 4, 10, 2), (3, 2, 7, 2), (5, 3, 11, 4), (8, 8, 3, 2)]:
+        stages = [0x10000000 * (i + 1) for i in range(L * M)]
+        for node in range(M):
+            ptrs = tide.stage_shard_pointers(stages, node, M, L, S, eb)
+            assert len(ptrs) == M * L
+            for r, a in enumerate(ptrs):
+                i = next(j for j, b in enumerate(stages) if b <= a < b + M * S * eb)
+                k, rem = divmod(a - stages[i], S * eb)
+                assert rem == 0 and i == (r % L) * M + node
+                assert ((node + k) % M) * L + r % L == r

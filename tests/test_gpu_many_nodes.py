@@ -251,3 +251,35 @@ def test_full_size_relative_order_sampled():
         assert differs > 0
         del grads, shards
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+@pytest.mark.parametrize("exchange", [0, 1], ids=["copy_engines", "sm_kernel"])
+def test_all_rails_exchange_with_many_nodes(w, exchange):
+    """The every-rail exchange with up to 32 nodes (5 rounds, the last one
+    sending fewer pieces than it holds when M is not a power of two): every
+    stage slot holds the shard the slot rule names, and placement from the
+    slots equals the direct all-gather."""
+    geo = O.geometry(w.shapes, w.N)
+    M, L, S = w.M, w.L, geo.S
+    rng = np.random.default_rng(31)
+    shards_h = [rng.integers(0, 65535, S, dtype=np.uint16) for _ in range(w.N)]
+    expect = O.ag_place(geo, shards_h)
+    shards = [torch.from_numpy(x.view(np.int16)).to(DEV) for x in shards_h]
+    with tide.TidePlan(w.shapes, w.N, M, L) as plan:
+        plan.set_option(tide.TIDE_OPT_RD_EXCHANGE, exchange)
+        stages = [torch.full((M * S,), -9, dtype=torch.int16, device=DEV) for _ in range(L * M)]
+        tide.tide_ag_stage_init(plan.handle, shards, stages, 2)
+        tide.tide_ag_rd_exchange_rails(plan.handle, stages, 2)
+        torch.cuda.synchronize()
+        for l in range(L):
+            for n in range(M):
+                got = stages[l * M + n].view(M, S)
+                want = torch.stack([shards[((n + k) % M) * L + l] for k in range(M)])
+                assert torch.equal(got, want), (l, n)
+        node = M // 2
+        params = [torch.full((w.N * geo.e[p],), -5, dtype=torch.int16, device=DEV) for p in range(w.P)]
+        plan.ag_place(tide.stage_shard_pointers(stages, node, M, L, S, 2), params, 2)
+        torch.cuda.synchronize()
+        for p in range(w.P):
+            assert np.array_equal(params[p].cpu().numpy().view(np.uint16), expect[p]), p

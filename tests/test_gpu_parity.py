@@ -440,6 +440,42 @@ def test_ag_by_recursive_doubling_matches_direct_landing(w, elem_bytes, exchange
                 assert np.array_equal(params[p].cpu().numpy().view(dt), expect[p]), (node, p)
 
 
+@pytest.mark.parametrize("w", [SMALL[0], SMALL[3], SMALL[4], SMALL[5]], ids=lambda w: w.name)
+@pytest.mark.parametrize("elem_bytes", [2, 4])
+@pytest.mark.parametrize("exchange", [0, 1], ids=["copy_engines", "sm_kernel"])
+def test_ag_by_recursive_doubling_all_rails(w, elem_bytes, exchange):
+    """The same all-gather with every rail at once: stage init, the exchange
+    of all rails, then tide_ag_place reading the stage slots.  Every stage
+    slot must hold the shard the slot rule names, and every piece must land
+    where the direct all-gather puts it."""
+    geo = O.geometry(w.shapes, w.N)
+    M, L, S = w.M, w.L, geo.S
+    dt, tdt = (np.uint16, torch.int16) if elem_bytes == 2 else (np.uint32, torch.int32)
+    rng = np.random.default_rng(23)
+    shards_h = [rng.integers(0, np.iinfo(dt).max, S, dtype=dt) for _ in range(w.N)]
+    expect = O.ag_place(geo, shards_h)
+    shards = [torch.from_numpy(x.view(np.int16 if elem_bytes == 2 else np.int32)).to(DEV) for x in shards_h]
+    with tide.TidePlan(w.shapes, w.N, M, L) as plan:
+        plan.set_option(tide.TIDE_OPT_RD_EXCHANGE, exchange)
+        stages = [torch.full((M * S,), -9, dtype=tdt, device=DEV) for _ in range(L * M)]
+        tide.tide_ag_stage_init(plan.handle, shards, stages, elem_bytes)
+        assert plan.last_launches() == (1 if S else 0)
+        tide.tide_ag_rd_exchange_rails(plan.handle, stages, elem_bytes)
+        if exchange == 1 and M > 1 and S:
+            assert plan.last_launches() == O.rd_rounds(M)
+        torch.cuda.synchronize()
+        for l in range(L):
+            for n in range(M):
+                for k in range(M):
+                    assert torch.equal(stages[l * M + n][k * S:(k + 1) * S], shards[((n + k) % M) * L + l]), (l, n, k)
+        for node in sorted({0, M - 1}):
+            params = [torch.full((w.N * geo.e[p],), -5, dtype=tdt, device=DEV) for p in range(w.P)]
+            plan.ag_place(tide.stage_shard_pointers(stages, node, M, L, S, elem_bytes), params, elem_bytes)
+            torch.cuda.synchronize()
+            for p in range(w.P):
+                assert np.array_equal(params[p].cpu().numpy().view(dt), expect[p]), (node, p)
+
+
 @pytest.mark.parametrize("w", [SMALL[0], SMALL[2], SMALL[3], SMALL[4], SMALL[5], SMALL[6]], ids=lambda w: w.name)
 @pytest.mark.parametrize("budget", [(0, 0), (16, 4)], ids=["fill", "pages_16_4"])
 def test_rs_staged_bit_exact_and_inbox(w, budget):
