@@ -148,7 +148,10 @@ class ClockSampler:
         self.proc = None
         self.path = None
 
+    MIN_RUN_S = 1.5   # nvidia-smi needs about a second before its first sample
+
     def start(self):
+        self.t_start = time.time()
         try:
             fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
             os.close(fd)
@@ -163,6 +166,7 @@ class ClockSampler:
     def stop(self, t0, t1):
         if self.proc is None:
             return None
+        time.sleep(max(0.0, self.t_start + self.MIN_RUN_S - time.time()))
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)

@@ -1,0 +1,51 @@
+"""bench.py on the GPU at small sizes: every path exits 0 and prints one JSON
+line, and the default line carries every key of the measurement contract
+(roofline, CPU baseline, end-to-end, clocks, launch count)."""
+
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SMALL = ["--workload", "llama70b", "--row-div", "64"]
+
+
+def _run(*args):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], capture_output=True, text=True,
+                         timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1, out.stdout
+    return json.loads(lines[0])
+
+
+def test_default_line_has_every_contract_key():
+    K, W = 3, 3
+    rec = _run(*SMALL, "--steps", str(K), "--warmup", str(W), "--cpu-seconds", "1", "--e2e-steps", "1")
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e", "clocks",
+                "gpu_launches"):
+        assert key in rec, key
+    assert rec["n_gpus"] == 1 and rec["steps"] == K and rec["warmup"] == W and rec["value"] > 0
+    assert rec["higher_is_better"] is True and rec["scaling"] == "weak" and rec["vs_baseline"] is None
+    assert "workload" in rec["config"]
+    roof = rec["roofline"]
+    assert roof["bound"] == "hbm" and roof["unit"] == "GB/s" and roof["peak"] > 0
+    assert roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"], rel=1e-3)
+    cpu = rec["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] == 1 and cpu["value"] > 0 and cpu["sample"]
+    e2e = rec["e2e"]
+    assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(rec["clocks"] or {})
+    assert rec["gpu_launches"] == 2 * K   # one reduce-scatter and one all-gather kernel per step
+
+
+@pytest.mark.parametrize("path", ["staged-rs", "rd-ag", "variants"])
+def test_other_paths_print_one_line(path):
+    rec = _run("--path", path, *SMALL, "--steps", "2", "--warmup", "1")
+    assert rec["path"] == path and rec["value"] > 0
