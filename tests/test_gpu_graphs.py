@@ -106,3 +106,53 @@ def test_capture_slots_run_out_with_a_status():
         for p in range(w.P):
             assert (params[p] == 0).all()
         del g
+
+
+W3 = configs.Workload("graph_3x2", 6, 3, 2, [(7, 5), (13,), (40, 9)], [gen.UNIFORM] * 3, seed=602)
+
+
+@pytest.mark.parametrize("w", [W, W3], ids=lambda w: w.name)
+@pytest.mark.parametrize("exchange", [0, 1], ids=["copy_engines", "sm_kernel"])
+def test_capture_every_rail_all_gather(w, exchange):
+    """Stage init, the exchange of every rail and the placement from the stage
+    slots, captured once and replayed with new shards behind the same buffers:
+    every replay lands every piece where the direct all-gather puts it."""
+    geo = O.geometry(w.shapes, w.N)
+    M, L, S = w.M, w.L, geo.S
+    rng = np.random.default_rng(5)
+    sets = [[rng.integers(0, 65535, S, dtype=np.uint16) for _ in range(w.N)] for _ in range(3)]
+    expects = [O.ag_place(geo, x) for x in sets]
+    with tide.TidePlan(w.shapes, w.N, M, L) as plan:
+        plan.set_option(tide.TIDE_OPT_RD_EXCHANGE, exchange)
+        shards = [torch.empty(S, dtype=torch.int16, device=DEV) for _ in range(w.N)]
+        stages = [torch.empty(M * S, dtype=torch.int16, device=DEV) for _ in range(L * M)]
+        params = [torch.empty(w.N * geo.e[p], dtype=torch.int16, device=DEV) for p in range(w.P)]
+        sh, st = tide.pointer_array(shards), tide.pointer_array(stages)
+        slots = tide.pointer_array(tide.stage_shard_pointers(stages, M - 1, M, L, S, 2))
+        pp = tide.pointer_array(params)
+        s = torch.cuda.Stream()
+
+        def step():
+            tide.tide_ag_stage_init(plan.handle, sh, st, 2, s)
+            tide.tide_ag_rd_exchange_rails(plan.handle, st, 2, s)
+            plan.ag_place(slots, pp, 2, s)
+
+        with torch.cuda.stream(s):
+            step()                      # first calls outside capture: device state
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step()
+        torch.cuda.synchronize()
+        for k in [1, 0, 2]:
+            for r in range(w.N):
+                shards[r].copy_(torch.from_numpy(sets[k][r].view(np.int16)))
+            for x in stages:
+                x.fill_(-9)
+            for p in range(w.P):
+                params[p].fill_(-1)
+            g.replay()
+            torch.cuda.synchronize()
+            for p in range(w.P):
+                assert np.array_equal(params[p].cpu().numpy().view(np.uint16), expects[k][p]), (k, p)
+        del g
