@@ -3,9 +3,10 @@
 Each case draws M, L (M > L included), parameter shapes (0-D, 1-D, 3-D, empty,
 fewer rows than ranks, odd row lengths), value distributions, the level-2
 order and the averaging / accumulate variants (every fourth case with pieces
-of several work items), then runs the reduce-scatter on
-the direct, staged, bulk (M <= 8) and no-allocation paths and the all-gather
-on the SM and bulk transports.  Sizes stay small so the oracle is quick.
+of several work items), then runs the reduce-scatter on the direct, staged,
+bulk (M <= 8) and no-allocation paths, and the all-gather on the SM and bulk
+transports and through the every-rail exchange.  Sizes stay small so the
+oracle is quick.
 """
 
 import numpy as np
@@ -96,3 +97,17 @@ def test_fuzz_group(seed):
             for p in range(w.P):
                 got = params[p][:w.N * geo.e[p]].cpu().numpy().view(np.uint16)
                 assert np.array_equal(got, ag_expect[p]), (seed, transport, p)
+        # every rail at once: stage init, exchange (transport by seed), placement from the slots
+        plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, tide.TIDE_AG_SM)
+        plan.set_option(tide.TIDE_OPT_RD_EXCHANGE, seed % 2)
+        stages = [torch.full((w.M * geo.S,), -3, dtype=torch.int16, device=DEV) for _ in range(w.L * w.M)]
+        tide.tide_ag_stage_init(plan.handle, shards, stages, 2)
+        tide.tide_ag_rd_exchange_rails(plan.handle, stages, 2)
+        node = seed % w.M
+        params = [torch.full((max(1, w.N * geo.e[p]),), -1, dtype=torch.int16, device=DEV) for p in range(w.P)]
+        plan.ag_place(tide.stage_shard_pointers(stages, node, w.M, w.L, geo.S, 2),
+                      [x[:w.N * geo.e[p]] for p, x in enumerate(params)], 2)
+        plan.check()
+        for p in range(w.P):
+            got = params[p][:w.N * geo.e[p]].cpu().numpy().view(np.uint16)
+            assert np.array_equal(got, ag_expect[p]), (seed, "every rail", p)
