@@ -354,6 +354,40 @@ def _time_steps(step, K, stream, world, dev, nbytes):
     return aggregate(a.elapsed_time(b) / 1e3, float((nbytes["rs_bytes"] + nbytes["ag_bytes"]) * K), world, device=dev)
 
 
+def host_available_bytes():
+    """Host memory this process can still take: MemAvailable, capped by the
+    cgroup's limit when one is set; None if neither can be read."""
+    vals = []
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    vals.append(int(line.split()[1]) * 1024)
+    except (OSError, ValueError, IndexError):
+        pass
+    try:
+        with open("/sys/fs/cgroup/memory.max") as f:
+            lim = f.read().strip()
+        with open("/sys/fs/cgroup/memory.current") as f:
+            cur = int(f.read().strip())
+        if lim != "max":
+            vals.append(int(lim) - cur)
+    except (OSError, ValueError):
+        pass
+    return min(vals) if vals else None
+
+
+def all_ranks_ok(ok, world, dev):
+    """True only if `ok` holds on every rank (so all ranks take the same branch)."""
+    if world == 1:
+        return ok
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([1 if ok else 0], dtype=torch.int32, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MIN)
+    return bool(t.item())
+
+
 def run_e2e(args, plan, w, nbytes, grads, rs_out, ag_in, ag_out, stream, world, dev, ptrs):
     """The step through the C ABI with HOST buffers.
 
@@ -368,9 +402,24 @@ def run_e2e(args, plan, w, nbytes, grads, rs_out, ag_in, ag_out, stream, world, 
     import torch
 
     import fsdp_layout_aware_gb300 as tide
+    need = sum(t.numel() * t.element_size() for t in grads + ag_in + rs_out + ag_out)
+    local = int(os.environ.get("LOCAL_WORLD_SIZE", world))
+    avail = host_available_bytes()
+    why = None
+    if avail is not None and need * local > 0.6 * avail:
+        why = (f"needs {need / 1e9:.1f} GB of pinned host memory per rank x {local} ranks; "
+               f"{avail / 1e9:.1f} GB available")
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-    h_grads, h_ag_in = [pin(t) for t in grads], [pin(t) for t in ag_in]
-    h_rs_out, h_ag_out = [pin(t) for t in rs_out], [pin(t) for t in ag_out]
+    h_grads = h_ag_in = h_rs_out = h_ag_out = []
+    if why is None:
+        try:
+            h_grads, h_ag_in = [pin(t) for t in grads], [pin(t) for t in ag_in]
+            h_rs_out, h_ag_out = [pin(t) for t in rs_out], [pin(t) for t in ag_out]
+        except RuntimeError as err:
+            why = f"pinned host allocation of {need / 1e9:.1f} GB failed: {str(err).splitlines()[0][:120]}"
+    if not all_ranks_ok(why is None, world, dev):
+        del h_grads, h_ag_in, h_rs_out, h_ag_out
+        return {"value": None, "unit": "GB/s", "unavailable": why or "another rank could not pin its host buffers"}
     with torch.cuda.stream(stream):
         for h, d in zip(h_grads + h_ag_in, grads + ag_in):
             h.copy_(d, non_blocking=True)

@@ -54,12 +54,15 @@ def _rank_main(rank, world, port, q):
     bench.init_dist(world, "gloo")
     secs = [1.5, 2.5][rank]
     units = [10.0, 30.0][rank]
-    q.put((rank, bench.aggregate(secs, units, world)))
+    agreed = (bench.all_ranks_ok(True, world, "cpu"), bench.all_ranks_ok(rank == 0, world, "cpu"))
+    q.put((rank, (bench.aggregate(secs, units, world), agreed)))
     import torch.distributed as dist
     dist.destroy_process_group()
 
 
-def test_aggregate_max_time_sum_units_over_gloo():
+def test_aggregate_and_agreement_over_gloo():
+    """Max time and summed units over the ranks; and a yes/no that holds only
+    if every rank says yes (the e2e leg runs on all ranks or on none)."""
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
@@ -70,7 +73,7 @@ def test_aggregate_max_time_sum_units_over_gloo():
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    assert res[0] == res[1] == (2.5, 40.0)
+    assert res[0] == res[1] == ((2.5, 40.0), (True, False))
 
 
 def test_reference_arm_only_rank0_prints(monkeypatch):
