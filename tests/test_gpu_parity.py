@@ -315,6 +315,49 @@ def test_full_size_rs_ag_sampled(cfg):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("cfg,exchange", [(3, 1), (4, 1), (4, 0), (5, 1)],
+                         ids=["qwen3moe_sm", "wan22dit_sm", "wan22dit_copy_engines", "uneven_sm"])
+def test_full_size_every_rail_all_gather(cfg, exchange):
+    """The every-rail all-gather (stage init, exchange of all rails, placement
+    from the slots) on the full groups, as bench.py --path rd-ag runs it:
+    every stage slot equals the shard the slot rule names, every placed piece
+    equals its shard slice, and sampled outputs match the oracle from the
+    host generator."""
+    w = configs.get(cfg)
+    geo = O.geometry(w.shapes, w.N)
+    M, L, S = w.M, w.L, geo.S
+    with tide.TidePlan(w.shapes, w.N, M, L) as plan:
+        plan.set_option(tide.TIDE_OPT_RD_EXCHANGE, exchange)
+        ag_in = device_ag_shards(w, S)
+        stages = [torch.empty(M * S, dtype=torch.int16, device=DEV) for _ in range(L * M)]
+        params = [torch.empty(w.N * geo.e[p], dtype=torch.int16, device=DEV) for p in range(w.P)]
+        st = tide.pointer_array(stages)
+        tide.tide_ag_stage_init(plan.handle, tide.pointer_array(ag_in), st, 2)
+        tide.tide_ag_rd_exchange_rails(plan.handle, st, 2)
+        node = M - 1
+        plan.ag_place(tide.pointer_array(tide.stage_shard_pointers(stages, node, M, L, S, 2)),
+                      tide.pointer_array(params), 2)
+        plan.check()
+        for l in range(L):
+            for n in range(M):
+                for k in range(M):
+                    assert torch.equal(stages[l * M + n][k * S:(k + 1) * S], ag_in[((n + k) % M) * L + l]), (l, n, k)
+        for p in range(w.P):
+            e_p, o_p = geo.e[p], geo.o[p]
+            for r in range(w.N):
+                assert torch.equal(params[p][r * e_p:(r + 1) * e_p], ag_in[r][o_p:o_p + e_p]), (p, r)
+        rng = np.random.default_rng(100 + cfg)
+        for _ in range(1500):
+            p = int(rng.integers(0, w.P))
+            if geo.e[p] == 0:
+                continue
+            y = int(rng.integers(0, w.N * geo.e[p]))
+            want = O.ag_element(geo, p, y, lambda rr, idx: w.ag_values(rr, idx.astype(np.uint64)))
+            assert np.uint16(params[p][y].item() & 0xFFFF) == want, (p, y)
+        del ag_in, stages, params
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------- kernel choice and waits
 
 @pytest.mark.parametrize("w", [SMALL[0], SMALL[2], SMALL[4], SMALL[5], SMALL[6]], ids=lambda w: w.name)
