@@ -266,9 +266,136 @@ __global__ void __launch_bounds__(256, kBatched ? 5 : 8) rs_land_grouped_kernel(
   }
 }
 
+__device__ __forceinline__ void add4(float4& a, const float4 b) {
+  a.x = __fadd_rn(a.x, b.x);
+  a.y = __fadd_rn(a.y, b.y);
+  a.z = __fadd_rn(a.z, b.z);
+  a.w = __fadd_rn(a.w, b.w);
+}
+
+// The landing kernels again, with 16-byte loads and stores, for plans whose
+// slice length B is a multiple of 4 (llama70b, qwen3moe, uneven and wan22dit
+// as 16 x 4; not wan22dit as 8 x 8) when the inbox and every shard start on
+// a 16-byte boundary: then
+// slice s starts at element s*B of a shard and at a multiple of B in the
+// inbox, so every partial and the shard share one 16-byte phase.  Each thread
+// takes kVecs float4 outputs per round (kVecs * kGroup 16-byte loads in
+// flight); the last 1-3 elements of a slice, past its whole vectors, are
+// added element by element.  The additions are the scalar kernels',
+// component by component, in the same order.  Measured against the 4-byte
+// kernels on one box, alternating (whole staged reduce-scatter, filling the
+// GPU / with the pages' 16 + 4 CTAs): llama70b 3.374 vs 3.464 ms / 15.70 vs
+// 25.74 ms, qwen3moe 4.581 vs 4.590 / 10.21 vs 12.28, uneven 2.284 vs 2.324 /
+// 2.77 vs 3.09, wan22dit as 16 x 4 13.26 vs 13.54 / 15.93 vs 16.69.  The M = 1
+// instance takes 40 registers (6 CTAs per SM); at 32 it spilled.
+template <bool kBatched, int kGroup>
+__global__ void __launch_bounds__(256, kBatched ? 5 : (kGroup == 1 ? 6 : 8)) rs_land_vec_kernel(const __grid_constant__ RsArgs a) {
+  constexpr int kVecs = 2;
+  __shared__ const float* part[kMaxM];
+  const int M = a.M, L = a.L;
+  const int64_t S = a.S, B = a.slice_len;
+  const int r = blockIdx.y;
+  const int n_dest = r / L, l_dest = r % L;
+  float* out = a.shard_tab[r];
+  const int64_t slot = (int64_t)L * B;
+  const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < L; ++s) {
+    const int64_t lo = (int64_t)s * B, hi = min(S, lo + B);
+    if (lo >= hi) break;
+    __syncthreads();  // the previous slice's readers of part[] are done
+    if ((int)threadIdx.x < M) {
+      const int k = threadIdx.x;
+      const int node = a.order[(n_dest * L + s) * M + k];
+      const int c = ((n_dest - node) % M + M) % M;  // relative index of the k-th source
+      const int g = ((s - c) % L + L) % L;            // the GPU its slice s landed on
+      part[k] = a.inbox + ((int64_t)(n_dest * L + g) * M + c) * slot + (int64_t)l_dest * B;  // element lo
+    }
+    __syncthreads();
+    const int64_t nv = (hi - lo) >> 2;  // whole float4s of the slice
+    float* const o = out + lo;
+    for (int64_t v0 = tid; v0 < nv; v0 += kVecs * nthr) {
+      float4 acc[kVecs], bsum[kBatched ? kVecs : 1];
+#pragma unroll
+      for (int u = 0; u < kVecs; ++u) acc[u] = zero4;
+#pragma unroll
+      for (int u = 0; u < (kBatched ? kVecs : 1); ++u) bsum[u] = zero4;
+      for (int j0 = 0; j0 < M; j0 += kGroup) {
+        float4 v[kGroup][kVecs];
+#pragma unroll
+        for (int q = 0; q < kGroup; ++q) {
+          const float4* pj = reinterpret_cast<const float4*>(part[min(j0 + q, M - 1)]);
+#pragma unroll
+          for (int u = 0; u < kVecs; ++u) {
+            const int64_t vi = v0 + u * nthr;
+            v[q][u] = (j0 + q < M && vi < nv) ? __ldcs(pj + vi) : zero4;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kGroup; ++q) {
+          const int j = j0 + q;
+          if (j >= M) break;
+#pragma unroll
+          for (int u = 0; u < kVecs; ++u) {
+            if constexpr (kBatched)
+              add4(bsum[u], v[q][u]);
+            else
+              add4(acc[u], v[q][u]);
+          }
+          if constexpr (kBatched) {
+            if ((j + 1) % L == 0 || j + 1 == M) {  // end of a batch
+#pragma unroll
+              for (int u = 0; u < kVecs; ++u) {
+                add4(acc[u], bsum[u]);
+                bsum[u] = zero4;
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kVecs; ++u) {
+        const int64_t vi = v0 + u * nthr;
+        if (vi < nv) {
+          float* d = o + 4 * vi;
+          float4 res;
+          res.x = epilogue1(acc[u].x, d + 0, a.epilogue, M * L);
+          res.y = epilogue1(acc[u].y, d + 1, a.epilogue, M * L);
+          res.z = epilogue1(acc[u].z, d + 2, a.epilogue, M * L);
+          res.w = epilogue1(acc[u].w, d + 3, a.epilogue, M * L);
+          if (store_ok(d, 16, out + lo, out + hi)) __stcs(reinterpret_cast<float4*>(d), res);
+        }
+      }
+    }
+    // the 1-3 elements past the slice's whole vectors
+    const int64_t x = lo + 4 * nv + tid;
+    if (x < hi) {
+      float acc = 0.f, bsum = 0.f;
+      for (int j = 0; j < M; ++j) {
+        const float pv = __ldcs(part[j] + (x - lo));
+        if constexpr (kBatched) {
+          bsum = __fadd_rn(bsum, pv);
+          if ((j + 1) % L == 0 || j + 1 == M) {
+            acc = __fadd_rn(acc, bsum);
+            bsum = 0.f;
+          }
+        } else {
+          acc = __fadd_rn(acc, pv);
+        }
+      }
+      if (store_ok(out + x, 4, out + lo, out + hi)) __stcs(out + x, epilogue1(acc, out + x, a.epilogue, M * L));
+    }
+  }
+}
+
 using LandKernel = void (*)(RsArgs);
 
-LandKernel land_kernel_for(int M, int L) {
+LandKernel land_kernel_for(int M, int L, bool vec) {
+  if (vec) {
+    if (M > L) return rs_land_vec_kernel<true, 1>;
+    return M == 1 ? rs_land_vec_kernel<false, 1> : rs_land_vec_kernel<false, 2>;
+  }
   if (M > L) return rs_land_kernel<true>;
   return M == 1 ? rs_land_kernel<false> : rs_land_grouped_kernel<false, 2>;
 }
@@ -283,7 +410,7 @@ int launch_sum_t(const RsArgs& a, int grid, cudaStream_t s) {
 
 TIDE_BOUNDS_COUNTER(rs_staged_bounds)
 
-int launch_rs_staged(const RsArgs& a, int sum_grid, int land_grid_x, void* stream) {
+int launch_rs_staged(const RsArgs& a, int sum_grid, int land_grid_x, bool land_vec, void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
   int err = (int)cudaErrorInvalidValue;
   switch (a.L) {
@@ -297,13 +424,13 @@ int launch_rs_staged(const RsArgs& a, int sum_grid, int land_grid_x, void* strea
     case 8: err = launch_sum_t<8>(a, sum_grid, s); break;
   }
   if (err != cudaSuccess) return err;
-  land_kernel_for(a.M, a.L)<<<dim3(land_grid_x, a.N), 256, 0, s>>>(a);
+  land_kernel_for(a.M, a.L, land_vec)<<<dim3(land_grid_x, a.N), 256, 0, s>>>(a);
   return (int)cudaGetLastError();
 }
 
-int rs_land_blocks_per_sm(int M, int L) {
+int rs_land_blocks_per_sm(int M, int L, bool vec) {
   int n = 0;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, land_kernel_for(M, L), 256, 0) == cudaSuccess ? n : 0;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, land_kernel_for(M, L, vec), 256, 0) == cudaSuccess ? n : 0;
 }
 
 }  // namespace tide

@@ -551,6 +551,43 @@ def test_rs_staged_bit_exact_and_inbox(w, budget):
                         assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), (n_dest, g, c, l_dest)
 
 
+def _vec_cases():
+    """Groups whose slice length B = ceil(S / L) is a multiple of 4 (every
+    row length a multiple of 96), for M = 1, M <= L and M > L, so the 16-byte
+    landing kernels run; ragged row counts keep padding rows in every shard."""
+    shapes = [(5, 96), (100, 192), (17, 96), (1, 288), (40, 96)]
+    mixed = [gen.NORMAL if p % 2 else gen.OUTLIER for p in range(len(shapes))]
+    return [configs.Workload(f"vec_{M}x{L}", M * L, M, L, shapes, mixed, sigma=1e-3, seed=700 + M * 10 + L)
+            for M, L in [(1, 8), (2, 4), (3, 3), (4, 4), (8, 8), (6, 2), (12, 4)]]
+
+
+@pytest.mark.parametrize("w", _vec_cases(), ids=lambda w: w.name)
+@pytest.mark.parametrize("aligned", [True, False], ids=["16B", "offset"])
+@pytest.mark.parametrize("budget", [(0, 0), (16, 4)], ids=["fill", "pages_16_4"])
+def test_rs_staged_16_byte_landing(w, aligned, budget):
+    """With the inbox and every shard on a 16-byte boundary the landing runs
+    on 16-byte loads and stores (slice length a multiple of 4); one element
+    off, it runs the 4-byte kernels.  Both give the oracle's bits and leave
+    the guard bands alone."""
+    grads = host_grads(w)
+    geo, expect = oracle_rs(w, grads)
+    assert O.slice_len(geo.S, w.L) % 4 == 0
+    lead = 32 if aligned else 33     # elements before each output: 128 or 132 bytes
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        dev = [[to_dev_u16(grads[r][p])[0] for p in range(w.P)] for r in range(w.N)]
+        n_inbox = tide.tide_plan_inbox_elems(plan.handle)
+        inbox_back = torch.full((n_inbox + 8,), float("nan"), dtype=torch.float32, device=DEV)
+        inbox = inbox_back[0 if aligned else 1:][:n_inbox]
+        outs = [f32_guarded(geo.S, lead, 29) for _ in range(w.N)]
+        flat = [dev[r][p] for r in range(w.N) for p in range(w.P)]
+        tide.tide_rs_staged(plan.handle, flat, [o[0] for o in outs], inbox, *budget)
+        plan.check()
+        for r in range(w.N):
+            assert np.array_equal(f32_bits(outs[r][0]), expect[r].view(np.uint32)), r
+            back = outs[r][1]
+            assert torch.isnan(back[:lead]).all() and torch.isnan(back[lead + geo.S:]).all(), r
+
+
 # --------------------------------------------------------------- variants
 
 @pytest.mark.parametrize("w", [SMALL[0], SMALL[4], SMALL[5], SMALL[6]], ids=lambda w: w.name)
