@@ -266,30 +266,47 @@ __global__ void __launch_bounds__(256, kBatched ? 5 : 8) rs_land_grouped_kernel(
   }
 }
 
-__device__ __forceinline__ void add4(float4& a, const float4 b) {
+__device__ __forceinline__ void add_v(float4& a, const float4 b) {
   a.x = __fadd_rn(a.x, b.x);
   a.y = __fadd_rn(a.y, b.y);
   a.z = __fadd_rn(a.z, b.z);
   a.w = __fadd_rn(a.w, b.w);
 }
+__device__ __forceinline__ void add_v(float2& a, const float2 b) {
+  a.x = __fadd_rn(a.x, b.x);
+  a.y = __fadd_rn(a.y, b.y);
+}
+__device__ __forceinline__ void set_zero(float4& z) { z = make_float4(0.f, 0.f, 0.f, 0.f); }
+__device__ __forceinline__ void set_zero(float2& z) { z = make_float2(0.f, 0.f); }
+// the variants applied to each component (d: the vector's first element)
+__device__ __forceinline__ float4 epilogue_v(float4 v, const float* d, int flags, int N) {
+  return make_float4(epilogue1(v.x, d, flags, N), epilogue1(v.y, d + 1, flags, N), epilogue1(v.z, d + 2, flags, N),
+                     epilogue1(v.w, d + 3, flags, N));
+}
+__device__ __forceinline__ float2 epilogue_v(float2 v, const float* d, int flags, int N) {
+  return make_float2(epilogue1(v.x, d, flags, N), epilogue1(v.y, d + 1, flags, N));
+}
 
-// The landing kernels again, with 16-byte loads and stores, for plans whose
-// slice length B is a multiple of 4 (llama70b, qwen3moe, uneven and wan22dit
-// as 16 x 4; not wan22dit as 8 x 8) when the inbox and every shard start on
-// a 16-byte boundary: then
-// slice s starts at element s*B of a shard and at a multiple of B in the
-// inbox, so every partial and the shard share one 16-byte phase.  Each thread
-// takes kVecs float4 outputs per round (kVecs * kGroup 16-byte loads in
-// flight); the last 1-3 elements of a slice, past its whole vectors, are
-// added element by element.  The additions are the scalar kernels',
-// component by component, in the same order.  Measured against the 4-byte
-// kernels on one box, alternating (whole staged reduce-scatter, filling the
-// GPU / with the pages' 16 + 4 CTAs): llama70b 3.374 vs 3.464 ms / 15.70 vs
-// 25.74 ms, qwen3moe 4.581 vs 4.590 / 10.21 vs 12.28, uneven 2.284 vs 2.324 /
-// 2.77 vs 3.09, wan22dit as 16 x 4 13.26 vs 13.54 / 15.93 vs 16.69.  The M = 1
-// instance takes 40 registers (6 CTAs per SM); at 32 it spilled.
-template <bool kBatched, int kGroup>
-__global__ void __launch_bounds__(256, kBatched ? 5 : (kGroup == 1 ? 6 : 8)) rs_land_vec_kernel(const __grid_constant__ RsArgs a) {
+// The landing kernels again, with vector loads and stores of V (float4 or
+// float2), for plans whose slice length B is a multiple of the vector's
+// width W (4: llama70b, qwen3moe, uneven and wan22dit as 16 x 4; 2: wan22dit
+// as 8 x 8) when the inbox and every shard start on a 4*W-byte boundary:
+// then slice s starts at element s*B of a shard and at a multiple of B in the
+// inbox, so every partial of the slice and the shard share one vector phase.
+// Each thread takes kVecs vectors per round (kVecs * kGroup vector loads in
+// flight); the last W - 1 or fewer elements of a slice, past its whole
+// vectors, are added element by element.  The additions are the scalar
+// kernels', component by component, in the same order.  Measured (float4)
+// against the 4-byte kernels on one box, alternating (whole staged
+// reduce-scatter, filling the GPU / with the pages' 16 + 4 CTAs): llama70b
+// 3.374 vs 3.464 ms / 15.70 vs 25.74 ms, qwen3moe 4.581 vs 4.590 / 10.21 vs
+// 12.28, uneven 2.284 vs 2.324 / 2.77 vs 3.09, wan22dit as 16 x 4 13.26 vs
+// 13.54 / 15.93 vs 16.69; float2 on wan22dit 9.646 vs 9.770 / 10.95 vs
+// 11.94.  The M = 1 and float2 instances take 40 registers (6 CTAs per SM);
+// at 32 they spilled.
+template <bool kBatched, int kGroup, class V>
+__global__ void __launch_bounds__(256, kBatched ? 5 : ((kGroup == 1 || sizeof(V) == 8) ? 6 : 8)) rs_land_vec_kernel(const __grid_constant__ RsArgs a) {
+  constexpr int W = (int)(sizeof(V) / 4);
   constexpr int kVecs = 2;
   __shared__ const float* part[kMaxM];
   const int M = a.M, L = a.L;
@@ -300,7 +317,8 @@ __global__ void __launch_bounds__(256, kBatched ? 5 : (kGroup == 1 ? 6 : 8)) rs_
   const int64_t slot = (int64_t)L * B;
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  V zv;
+  set_zero(zv);
   for (int s = 0; s < L; ++s) {
     const int64_t lo = (int64_t)s * B, hi = min(S, lo + B);
     if (lo >= hi) break;
@@ -313,23 +331,23 @@ __global__ void __launch_bounds__(256, kBatched ? 5 : (kGroup == 1 ? 6 : 8)) rs_
       part[k] = a.inbox + ((int64_t)(n_dest * L + g) * M + c) * slot + (int64_t)l_dest * B;  // element lo
     }
     __syncthreads();
-    const int64_t nv = (hi - lo) >> 2;  // whole float4s of the slice
+    const int64_t nv = (hi - lo) / W;  // whole vectors of the slice
     float* const o = out + lo;
     for (int64_t v0 = tid; v0 < nv; v0 += kVecs * nthr) {
-      float4 acc[kVecs], bsum[kBatched ? kVecs : 1];
+      V acc[kVecs], bsum[kBatched ? kVecs : 1];
 #pragma unroll
-      for (int u = 0; u < kVecs; ++u) acc[u] = zero4;
+      for (int u = 0; u < kVecs; ++u) acc[u] = zv;
 #pragma unroll
-      for (int u = 0; u < (kBatched ? kVecs : 1); ++u) bsum[u] = zero4;
+      for (int u = 0; u < (kBatched ? kVecs : 1); ++u) bsum[u] = zv;
       for (int j0 = 0; j0 < M; j0 += kGroup) {
-        float4 v[kGroup][kVecs];
+        V v[kGroup][kVecs];
 #pragma unroll
         for (int q = 0; q < kGroup; ++q) {
-          const float4* pj = reinterpret_cast<const float4*>(part[min(j0 + q, M - 1)]);
+          const V* pj = reinterpret_cast<const V*>(part[min(j0 + q, M - 1)]);
 #pragma unroll
           for (int u = 0; u < kVecs; ++u) {
             const int64_t vi = v0 + u * nthr;
-            v[q][u] = (j0 + q < M && vi < nv) ? __ldcs(pj + vi) : zero4;
+            v[q][u] = (j0 + q < M && vi < nv) ? __ldcs(pj + vi) : zv;
           }
         }
 #pragma unroll
@@ -339,16 +357,16 @@ __global__ void __launch_bounds__(256, kBatched ? 5 : (kGroup == 1 ? 6 : 8)) rs_
 #pragma unroll
           for (int u = 0; u < kVecs; ++u) {
             if constexpr (kBatched)
-              add4(bsum[u], v[q][u]);
+              add_v(bsum[u], v[q][u]);
             else
-              add4(acc[u], v[q][u]);
+              add_v(acc[u], v[q][u]);
           }
           if constexpr (kBatched) {
             if ((j + 1) % L == 0 || j + 1 == M) {  // end of a batch
 #pragma unroll
               for (int u = 0; u < kVecs; ++u) {
-                add4(acc[u], bsum[u]);
-                bsum[u] = zero4;
+                add_v(acc[u], bsum[u]);
+                bsum[u] = zv;
               }
             }
           }
@@ -358,18 +376,14 @@ __global__ void __launch_bounds__(256, kBatched ? 5 : (kGroup == 1 ? 6 : 8)) rs_
       for (int u = 0; u < kVecs; ++u) {
         const int64_t vi = v0 + u * nthr;
         if (vi < nv) {
-          float* d = o + 4 * vi;
-          float4 res;
-          res.x = epilogue1(acc[u].x, d + 0, a.epilogue, M * L);
-          res.y = epilogue1(acc[u].y, d + 1, a.epilogue, M * L);
-          res.z = epilogue1(acc[u].z, d + 2, a.epilogue, M * L);
-          res.w = epilogue1(acc[u].w, d + 3, a.epilogue, M * L);
-          if (store_ok(d, 16, out + lo, out + hi)) __stcs(reinterpret_cast<float4*>(d), res);
+          float* d = o + W * vi;
+          const V res = epilogue_v(acc[u], d, a.epilogue, M * L);
+          if (store_ok(d, 4 * W, out + lo, out + hi)) __stcs(reinterpret_cast<V*>(d), res);
         }
       }
     }
-    // the 1-3 elements past the slice's whole vectors
-    const int64_t x = lo + 4 * nv + tid;
+    // the elements past the slice's whole vectors
+    const int64_t x = lo + W * nv + tid;
     if (x < hi) {
       float acc = 0.f, bsum = 0.f;
       for (int j = 0; j < M; ++j) {
@@ -391,11 +405,16 @@ __global__ void __launch_bounds__(256, kBatched ? 5 : (kGroup == 1 ? 6 : 8)) rs_
 
 using LandKernel = void (*)(RsArgs);
 
-LandKernel land_kernel_for(int M, int L, bool vec) {
-  if (vec) {
-    if (M > L) return rs_land_vec_kernel<true, 1>;
-    return M == 1 ? rs_land_vec_kernel<false, 1> : rs_land_vec_kernel<false, 2>;
-  }
+template <class V>
+LandKernel land_vec_kernel_for(int M, int L) {
+  if (M > L) return rs_land_vec_kernel<true, 1, V>;
+  return M == 1 ? rs_land_vec_kernel<false, 1, V> : rs_land_vec_kernel<false, 2, V>;
+}
+
+// vec: vector width of the landing (4, 2, or 0 for 4-byte accesses)
+LandKernel land_kernel_for(int M, int L, int vec) {
+  if (vec == 4) return land_vec_kernel_for<float4>(M, L);
+  if (vec == 2) return land_vec_kernel_for<float2>(M, L);
   if (M > L) return rs_land_kernel<true>;
   return M == 1 ? rs_land_kernel<false> : rs_land_grouped_kernel<false, 2>;
 }
@@ -410,7 +429,7 @@ int launch_sum_t(const RsArgs& a, int grid, cudaStream_t s) {
 
 TIDE_BOUNDS_COUNTER(rs_staged_bounds)
 
-int launch_rs_staged(const RsArgs& a, int sum_grid, int land_grid_x, bool land_vec, void* stream) {
+int launch_rs_staged(const RsArgs& a, int sum_grid, int land_grid_x, int land_vec, void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
   int err = (int)cudaErrorInvalidValue;
   switch (a.L) {
@@ -428,7 +447,7 @@ int launch_rs_staged(const RsArgs& a, int sum_grid, int land_grid_x, bool land_v
   return (int)cudaGetLastError();
 }
 
-int rs_land_blocks_per_sm(int M, int L, bool vec) {
+int rs_land_blocks_per_sm(int M, int L, int vec) {
   int n = 0;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, land_kernel_for(M, L, vec), 256, 0) == cudaSuccess ? n : 0;
 }

@@ -628,10 +628,17 @@ tide_status tide_rs_staged(tide_plan* pl, const void* const* grads, float* const
   a.inbox = inbox;
   const int64_t sum_grid =
       sum_ctas_per_rank > 0 ? std::min<int64_t>((int64_t)sum_ctas_per_rank * pl->N, 1 << 20) : pl->rs_grid;
-  // 16-byte landing when every slice starts on a 16-byte boundary of the
-  // inbox and of each shard
-  bool land_vec = a.slice_len % 4 == 0 && ((uintptr_t)inbox & 15) == 0;
-  for (int32_t r = 0; land_vec && r < pl->N; ++r) land_vec = ((uintptr_t)shards[r] & 15) == 0;
+  // Vector landing (16- or 8-byte accesses) when every slice starts on such a
+  // boundary of the inbox and of each shard.
+  int land_vec = 0;
+  for (const int w : {4, 2}) {
+    bool ok = a.slice_len % w == 0 && ((uintptr_t)inbox % (4 * w)) == 0;
+    for (int32_t r = 0; ok && r < pl->N; ++r) ok = ((uintptr_t)shards[r] % (4 * w)) == 0;
+    if (ok) {
+      land_vec = w;
+      break;
+    }
+  }
   const int land_per_sm = std::max(1, rs_land_blocks_per_sm(pl->M, pl->L, land_vec));  // resident landing CTAs per SM
   const int land_x =
       landing_ctas_per_rank > 0 ? landing_ctas_per_rank : std::max(1, pl->num_sms * land_per_sm / pl->N);

@@ -168,10 +168,10 @@ int launch_ag_bulk(const AgBulkArgs& args, int grid, void* stream);
 int ag_bulk_setup();       // raises the bulk all-gather's dynamic shared-memory limit
 int ag_bulk_smem_bytes();
 int launch_rs_bulk(const RsArgs& args, int grid, void* stream);
-// land_vec: the 16-byte landing kernels (slice length a multiple of 4, inbox
-// and shards 16-byte aligned).
-int launch_rs_staged(const RsArgs& args, int sum_grid, int land_grid_x, bool land_vec, void* stream);
-int rs_land_blocks_per_sm(int M, int L, bool vec);  // resident landing CTAs per SM (0 on error)
+// land_vec: vector width of the landing, 4 or 2 floats (slice length a
+// multiple of it, inbox and shards aligned to it), or 0 for 4-byte accesses.
+int launch_rs_staged(const RsArgs& args, int sum_grid, int land_grid_x, int land_vec, void* stream);
+int rs_land_blocks_per_sm(int M, int L, int vec);  // resident landing CTAs per SM (0 on error)
 BulkLayout rs_bulk_layout(int N, int M, int L, int smem_budget);
 int rs_bulk_setup(int L, int smem_bytes);  // raises the kernel's dynamic shared-memory limit
 // Resident CTAs per SM of each kernel (occupancy), for grid sizing.

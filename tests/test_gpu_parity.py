@@ -553,25 +553,31 @@ def test_rs_staged_bit_exact_and_inbox(w, budget):
 
 def _vec_cases():
     """Groups whose slice length B = ceil(S / L) is a multiple of 4 (every
-    row length a multiple of 96), for M = 1, M <= L and M > L, so the 16-byte
-    landing kernels run; ragged row counts keep padding rows in every shard."""
+    row length a multiple of 96) or 2 mod 4 (one more parameter of row length
+    2L), for M = 1, M <= L and M > L, so the 16- and 8-byte landing kernels
+    run; ragged row counts keep padding rows in every shard."""
     shapes = [(5, 96), (100, 192), (17, 96), (1, 288), (40, 96)]
-    mixed = [gen.NORMAL if p % 2 else gen.OUTLIER for p in range(len(shapes))]
-    return [configs.Workload(f"vec_{M}x{L}", M * L, M, L, shapes, mixed, sigma=1e-3, seed=700 + M * 10 + L)
-            for M, L in [(1, 8), (2, 4), (3, 3), (4, 4), (8, 8), (6, 2), (12, 4)]]
+    ws = []
+    for width in (4, 2):
+        for M, L in [(1, 8), (2, 4), (3, 3), (4, 4), (8, 8), (6, 2), (12, 4)]:
+            sh = shapes if width == 4 else shapes + [(3, 2 * L)]
+            mixed = [gen.NORMAL if p % 2 else gen.OUTLIER for p in range(len(sh))]
+            ws.append(configs.Workload(f"vec{width}_{M}x{L}", M * L, M, L, sh, mixed, sigma=1e-3,
+                                       seed=700 + M * 10 + L + width))
+    return ws
 
 
 @pytest.mark.parametrize("w", _vec_cases(), ids=lambda w: w.name)
 @pytest.mark.parametrize("aligned", [True, False], ids=["16B", "offset"])
 @pytest.mark.parametrize("budget", [(0, 0), (16, 4)], ids=["fill", "pages_16_4"])
-def test_rs_staged_16_byte_landing(w, aligned, budget):
+def test_rs_staged_vector_landing(w, aligned, budget):
     """With the inbox and every shard on a 16-byte boundary the landing runs
-    on 16-byte loads and stores (slice length a multiple of 4); one element
-    off, it runs the 4-byte kernels.  Both give the oracle's bits and leave
-    the guard bands alone."""
+    on 16-byte (slice length a multiple of 4) or 8-byte (slice length 2 mod 4)
+    loads and stores; one element off, it runs the 4-byte kernels.  All give
+    the oracle's bits and leave the guard bands alone."""
     grads = host_grads(w)
     geo, expect = oracle_rs(w, grads)
-    assert O.slice_len(geo.S, w.L) % 4 == 0
+    assert O.slice_len(geo.S, w.L) % 4 == (0 if w.name.startswith("vec4") else 2)
     lead = 32 if aligned else 33     # elements before each output: 128 or 132 bytes
     with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
         dev = [[to_dev_u16(grads[r][p])[0] for p in range(w.P)] for r in range(w.N)]
