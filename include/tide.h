@@ -415,9 +415,11 @@ tide_status tide_ag_stage_place(tide_plan* plan, const void* stage, int32_t node
                                 void* const* params, int32_t elem_bytes, void* stream);
 
 /* ---- Every rail at once --------------------------------------------------
- * On the pages the L rails exchange concurrently, each over its own NICs.
- * These calls emulate all of them together, in one launch per step instead
- * of one per rail.  Buffer l*M + n of a `stages` array is node n's stage
+ * On the pages every GPU forwards its own rail's data across nodes
+ * ([Richland] "What shipped"; [Abstract] Figure 5 draws one rail), so the L
+ * rails exchange independently and at the same time.  These calls emulate
+ * all of them together, in one launch per step instead of one per rail; the
+ * bytes moved and their order are those of the rail-by-rail calls.  Buffer l*M + n of a `stages` array is node n's stage
  * buffer on rail l (M*S elements, slot k at k*S); all L*M are distinct,
  * caller-owned device buffers. */
 
