@@ -681,7 +681,8 @@ def run_rd_ag(args, local_rank):
 
 def run_variants(args, local_rank):
     """The listed variants, each timed alone on the workload: the reduce-scatter
-    on the bulk-copy kernel (M <= 8), averaged over N and/or accumulated into
+    on the bulk-copy kernel (M <= 8) and through the entry point without
+    device allocation, averaged over N and/or accumulated into
     the previous shard, Slot-Reuse
     (pack into the vacated all-gather slot, then the reduce-scatter reading
     the slots), and the all-gather writing only the real rows."""
@@ -703,6 +704,8 @@ def run_variants(args, local_rank):
         res[name] = {"ms": round(t * 1e3, 4), "bytes": nbytes, "GB_s": round(nbytes / t / 1e9, 1)}
 
     timed("rs_plain", lambda: plan.rs_reduce(gp, sp, stream), nb["rs_bytes"])
+    # the entry point without device allocation: tables built per call in its static buffer
+    timed("rs_noalloc", lambda: tide.tide_rs_reduce_noalloc(plan.handle, gp, sp, stream), nb["rs_bytes"])
     if w.M <= 8:  # the bulk-copy pipeline holds at most 8 node partials per thread
         plan.set_option(tide.TIDE_OPT_RS_KERNEL, 1)
         timed("rs_bulk", lambda: plan.rs_reduce(gp, sp, stream), nb["rs_bytes"])

@@ -8,6 +8,7 @@
 // gap-free prefix sum of the per-rank pieces e_p = Rp*Kp.
 
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <iterator>
@@ -262,6 +263,8 @@ tide_status tide_plan_create(const tide_group_desc* d, tide_plan** out_plan) {
 
   tide_plan* pl = new (std::nothrow) tide_plan();
   if (!pl) return fail(TIDE_ERR_OUT_OF_MEMORY, "plan allocation failed");
+  static std::atomic<uint64_t> next_uid{1};
+  pl->uid = next_uid.fetch_add(1);
   try {
     pl->N = d->N;
     pl->M = d->M;

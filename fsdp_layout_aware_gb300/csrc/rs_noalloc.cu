@@ -15,8 +15,13 @@
 // tide_rs_reduce.
 //
 // Sharing rules: every call on a device uses the same array, and the array
-// keeps whatever the last call left in it.  Each call rewrites every byte the
-// kernel reads before the kernel runs, so nothing has to start at zero.  Two
+// keeps whatever the last call left in it.  The host remembers, per device,
+// which plan's work list the array holds and which gradient and shard
+// pointers its tables were built from; a call uploads only what differs
+// (nothing, when a plan is called again on the same buffers, as FSDP2 does
+// step after step).  The work counter of the kernel's dynamic item order
+// lives in the array too: it is zeroed (cudaMemsetAsync, no allocation) when
+// a plan's work list is uploaded, and every launch leaves it at zero.  Two
 // calls whose work overlaps on the GPU (different streams, no ordering
 // between them) race on the array; issue them on one stream or order them.
 
@@ -25,6 +30,7 @@
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "tide_internal.h"
 
@@ -39,8 +45,17 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-std::mutex g_setup_mutex;
+std::mutex g_setup_mutex;  // guards the per-device records below
 unsigned char* g_scratch_addr[kMaxDevices] = {};
+
+// What the array on a device holds: the plan whose work list and counter are
+// in place (0: unknown), and the pointer arrays its tables were built from.
+struct DeviceRecord {
+  uint64_t plan_uid = 0;
+  std::vector<const void*> grads;
+  std::vector<const void*> shards;
+};
+DeviceRecord g_record[kMaxDevices];
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -83,14 +98,15 @@ extern "C" tide_status tide_rs_reduce_noalloc(const tide_plan* pl, const void* c
   const tide_status st = check_rs_call(pl, grads, shards, nullptr);
   if (st != TIDE_OK) return st;
 
-  // Scratch layout: items | caller's [r][p] pointers | [p][r] table | shards | flags.
+  // Scratch layout: items | caller's [r][p] pointers | [p][r] table | shards | flags | work counter.
   const size_t n_ptr = (size_t)pl->N * pl->P;
   const size_t items_bytes = pl->rs_items.size() * sizeof(RsItem);
   const size_t off_grads_rp = align256(items_bytes);
   const size_t off_gtab = align256(off_grads_rp + 8 * n_ptr);
   const size_t off_shards = align256(off_gtab + 8 * n_ptr);
   const size_t off_flags = align256(off_shards + 8 * (size_t)pl->N);
-  const size_t need = off_flags + (size_t)pl->P;
+  const size_t off_counter = align256(off_flags + (size_t)pl->P);
+  const size_t need = off_counter + 8;
   if (need > kNoallocScratchBytes)
     return fail(TIDE_ERR_INVALID_ARG, "this group needs " + std::to_string(need) +
                                           " bytes of static scratch; tide_rs_reduce_noalloc is limited to " +
@@ -100,42 +116,63 @@ extern "C" tide_status tide_rs_reduce_noalloc(const tide_plan* pl, const void* c
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return cuda_status(err, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(TIDE_ERR_INVALID_ARG, "device ordinal beyond 63");
-  unsigned char* base;
-  {
-    // First call on this device: look up where the module loader put the
-    // array on this device (the address differs per device).
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[dev]) {
-      void* ptr = nullptr;
-      err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-      if (err != cudaSuccess) return cuda_status(err, "cudaGetSymbolAddress(static scratch)");
-      g_scratch_addr[dev] = (unsigned char*)ptr;
-    }
-    base = g_scratch_addr[dev];
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (!g_scratch_addr[dev]) {
+    // First call on this device: where the module loader put the array on
+    // this device (the address differs per device).
+    void* ptr = nullptr;
+    err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (err != cudaSuccess) return cuda_status(err, "cudaGetSymbolAddress(static scratch)");
+    g_scratch_addr[dev] = (unsigned char*)ptr;
   }
-
+  unsigned char* const base = g_scratch_addr[dev];
+  DeviceRecord& rec = g_record[dev];
+  const std::vector<const void*> gv(grads, grads + n_ptr);
+  const std::vector<const void*> sv((const void* const*)shards, (const void* const*)shards + pl->N);
   cudaStream_t s = (cudaStream_t)stream;
-  if ((err = cudaMemcpyAsync(base, pl->rs_items.data(), items_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
-    return cuda_status(err, "work-list upload");
-  if ((err = cudaMemcpyAsync(base + off_grads_rp, grads, 8 * n_ptr, cudaMemcpyHostToDevice, s)) != cudaSuccess)
-    return cuda_status(err, "gradient pointer upload");
-  if ((err = cudaMemcpyAsync(base + off_shards, shards, 8 * (size_t)pl->N, cudaMemcpyHostToDevice, s)) !=
-      cudaSuccess)
-    return cuda_status(err, "shard pointer upload");
-  const int tgrid = (int)std::min<int64_t>(1024, ((int64_t)n_ptr + 255) / 256);
-  noalloc_tables_kernel<<<tgrid, 256, 0, s>>>((const uint16_t* const*)(base + off_grads_rp), pl->N, pl->P,
-                                               (const uint16_t**)(base + off_gtab), base + off_flags);
-  if ((err = cudaGetLastError()) != cudaSuccess) return cuda_status(err, "pointer-table kernel launch");
+  int launches = 0;
+  // On any failure below the record is cleared, so the next call uploads everything.
+  auto cuda_fail_rec = [&](cudaError_t e, const char* what) {
+    rec = DeviceRecord();
+    return cuda_status(e, what);
+  };
+  if (rec.plan_uid != pl->uid) {
+    rec = DeviceRecord();
+    if ((err = cudaMemcpyAsync(base, pl->rs_items.data(), items_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+      return cuda_fail_rec(err, "work-list upload");
+    if ((err = cudaMemsetAsync(base + off_counter, 0, 8, s)) != cudaSuccess)
+      return cuda_fail_rec(err, "work-counter reset");
+    rec.plan_uid = pl->uid;
+  }
+  if (rec.grads != gv) {
+    if ((err = cudaMemcpyAsync(base + off_grads_rp, grads, 8 * n_ptr, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+      return cuda_fail_rec(err, "gradient pointer upload");
+    const int tgrid = (int)std::min<int64_t>(1024, ((int64_t)n_ptr + 255) / 256);
+    noalloc_tables_kernel<<<tgrid, 256, 0, s>>>((const uint16_t* const*)(base + off_grads_rp), pl->N, pl->P,
+                                                 (const uint16_t**)(base + off_gtab), base + off_flags);
+    if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail_rec(err, "pointer-table kernel launch");
+    ++launches;
+    rec.grads = gv;
+  }
+  if (rec.shards != sv) {
+    if ((err = cudaMemcpyAsync(base + off_shards, shards, 8 * (size_t)pl->N, cudaMemcpyHostToDevice, s)) !=
+        cudaSuccess)
+      return cuda_fail_rec(err, "shard pointer upload");
+    rec.shards = sv;
+  }
 
   int sms = 0;
   if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return cuda_status(err, "cudaDeviceGetAttribute");
+    return cuda_fail_rec(err, "cudaDeviceGetAttribute");
   const int occ = rs_blocks_per_sm(pl->L);
-  if (occ <= 0) return fail(TIDE_ERR_CUDA, "occupancy query failed");
+  if (occ <= 0) {
+    rec = DeviceRecord();
+    return fail(TIDE_ERR_CUDA, "occupancy query failed");
+  }
 
   RsArgs a;
   a.items = (const RsItem*)base;
-  a.counter = nullptr;  // round-robin item order: nothing in the array needs zeroing
+  a.counter = (unsigned long long*)(base + off_counter);  // zero at launch; the kernel leaves it at zero
   a.n_items = (int64_t)pl->rs_items.size();
   a.grad_tab = (const uint16_t* const*)(base + off_gtab);
   a.shard_tab = (float* const*)(base + off_shards);
@@ -151,7 +188,7 @@ extern "C" tide_status tide_rs_reduce_noalloc(const tide_plan* pl, const void* c
   std::memcpy(a.order, pl->order, sizeof(a.order));
   const int grid = (int)std::min<int64_t>((int64_t)sms * occ, a.n_items);
   const int lerr = launch_rs(a, grid, stream);
-  if (lerr != cudaSuccess) return cuda_status((cudaError_t)lerr, "rs_fused launch");
-  pl->last_launches = 2;  // the table kernel and rs_fused
+  if (lerr != cudaSuccess) return cuda_fail_rec((cudaError_t)lerr, "rs_fused launch");
+  pl->last_launches = launches + 1;  // the table kernel when the tables changed, and rs_fused
   return TIDE_OK;
 }

@@ -189,6 +189,7 @@ int ag_blocks_per_sm();
 
 // The opaque plan.
 struct tide_plan {
+  uint64_t uid = 0;  // unique per plan in this process, never reused (tide_rs_reduce_noalloc's cache key)
   int32_t N = 0, M = 0, L = 0, P = 0;
   std::vector<int64_t> rows, Kp, Rp, e, o;
   int64_t S = 0;

@@ -321,12 +321,18 @@ tide_status tide_ag_place(tide_plan* plan, const void* const* shards, void* cons
  *   plan, grads, shards, stream: as for tide_rs_reduce.  The plan's own
  *   device state is not used or created.
  * The first call on a device looks up the array's address on that device;
- * make that first call before any CUDA graph capture.  Each call copies the
- * plan's work list and the pointer arrays into the array from pageable host
- * memory, so the call may wait for earlier work on `stream`.  The array is
- * shared by all calls on a device and keeps the last call's contents; every
- * call rewrites all it reads, so nothing needs clearing, but calls whose work
- * overlaps on the GPU (different streams, no ordering) race.
+ * make that first call before any CUDA graph capture.  The array is shared by
+ * all calls on a device and keeps the last call's contents; the library
+ * remembers, per device, which plan's work list it holds and which pointer
+ * arrays its tables were built from, and a call copies into it (from
+ * pageable host memory, so the call may wait for earlier work on `stream`)
+ * only what differs: the work list when the plan changes, a pointer table
+ * when its pointers change.  Calling the same plan on the same buffers
+ * uploads nothing.  The kernel's work counter also lives in the array; it is
+ * zeroed with cudaMemsetAsync when a plan's work list is copied in, and every
+ * launch leaves it at zero.  Calls whose work overlaps on the GPU (different
+ * streams, no ordering) race on the array.  tide_plan_last_launches counts
+ * the table kernel only when the gradient pointers changed.
  * Errors: as tide_rs_reduce; INVALID_ARG also when the group's work list and
  * tables exceed the 8 MiB array (use tide_rs_reduce for such groups). */
 tide_status tide_rs_reduce_noalloc(const tide_plan* plan, const void* const* grads, float* const* shards,

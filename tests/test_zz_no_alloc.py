@@ -60,3 +60,46 @@ def test_noalloc_rejects_groups_beyond_its_scratch():
         with pytest.raises(tide.TideError) as err:
             tide.tide_rs_reduce_noalloc(plan.handle, fake_grads, fake_shards)
         assert err.value.status == 1 and "8388608" in str(err.value)
+
+
+def test_noalloc_reuses_what_the_array_holds():
+    """The array keeps the last call's work list and tables: a repeat call on
+    the same buffers uploads nothing and launches only the reduce-scatter;
+    new data behind the same pointers, new shard pointers, and two plans
+    taking turns must all still give tide_rs_reduce's bits."""
+    wa, wb = WORKLOADS[0], WORKLOADS[1]
+    with tide.TidePlan(wa.shapes, wa.N, wa.M, wa.L) as pa, tide.TidePlan(wb.shapes, wb.N, wb.M, wb.L) as pb:
+        ga, gb = _device_grads(wa, 3000), _device_grads(wb, 3001)
+        outs_a = [torch.empty(pa.S, dtype=torch.float32, device=DEV) for _ in range(wa.N)]
+        outs_a2 = [torch.empty(pa.S, dtype=torch.float32, device=DEV) for _ in range(wa.N)]
+        outs_b = [torch.empty(pb.S, dtype=torch.float32, device=DEV) for _ in range(wb.N)]
+
+        def check(plan, grads, outs):
+            want = [torch.empty_like(o) for o in outs]
+            tide.tide_rs_reduce(plan.handle, grads, want)
+            torch.cuda.synchronize()
+            for r, (o, x) in enumerate(zip(outs, want)):
+                assert torch.equal(o.view(torch.int32), x.view(torch.int32)), r
+
+        tide.tide_rs_reduce_noalloc(pa.handle, ga, outs_a)
+        assert pa.last_launches() == 2            # tables built, then the reduce-scatter
+        check(pa, ga, outs_a)
+        tide.tide_rs_reduce_noalloc(pa.handle, ga, outs_a)
+        assert pa.last_launches() == 1            # nothing changed: the reduce-scatter only
+        check(pa, ga, outs_a)
+        fresh = _device_grads(wa, 3002)           # new data behind the same pointers
+        for g, f in zip(ga, fresh):
+            g.copy_(f)
+        tide.tide_rs_reduce_noalloc(pa.handle, ga, outs_a)
+        assert pa.last_launches() == 1
+        check(pa, ga, outs_a)
+        tide.tide_rs_reduce_noalloc(pa.handle, ga, outs_a2)   # new shard pointers only
+        assert pa.last_launches() == 1
+        check(pa, ga, outs_a2)
+        for _ in range(2):                        # two plans taking turns on one array
+            tide.tide_rs_reduce_noalloc(pb.handle, gb, outs_b)
+            assert pb.last_launches() == 2
+            check(pb, gb, outs_b)
+            tide.tide_rs_reduce_noalloc(pa.handle, ga, outs_a)
+            assert pa.last_launches() == 2
+            check(pa, ga, outs_a)
