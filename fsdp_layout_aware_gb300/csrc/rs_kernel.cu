@@ -135,18 +135,16 @@ __device__ __forceinline__ void reduce_unaligned(const uint16_t* const* src, int
 // item, issued one item ahead so its latency is hidden): the work balances
 // whatever the items' sizes, and at any moment the CTAs are on neighbouring
 // items, so the contributors are read in nearly address order across the GPU.
-// Without a counter (noalloc entry point) CTA b takes items b, b+G, b+2G, ...
 template <int L, bool kBatched>
 __global__ void __launch_bounds__(kRsThreads, 4) rs_fused_kernel(const __grid_constant__ RsArgs a) {
   __shared__ const uint16_t* src[kMaxN];
   __shared__ long long next_item[2];
-  unsigned long long* counter = a.counter;
-  if (threadIdx.x == 0) next_item[0] = counter ? take_item(counter, a.n_items) : (long long)blockIdx.x;
+  if (threadIdx.x == 0) next_item[0] = take_item(a.counter, a.n_items);
   __syncthreads();
   int slot = 0;
   for (int64_t it = next_item[0]; it < a.n_items; it = next_item[slot]) {
     slot ^= 1;
-    if (threadIdx.x == 0) next_item[slot] = counter ? take_item(counter, a.n_items) : (long long)(it + gridDim.x);
+    if (threadIdx.x == 0) next_item[slot] = take_item(a.counter, a.n_items);
     const RsItem item = a.items[it];
     float* dst = a.shard_tab[item.r] + item.dst_off;
     if (item.kind == RS_PAD) {

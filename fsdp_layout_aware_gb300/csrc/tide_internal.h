@@ -125,7 +125,7 @@ struct RsArgs {
   const RsItem* items;
   int64_t n_items;
   unsigned long long* counter;      // next item to take: zero at launch, and the kernel leaves it
-                                    // zero (see take_item); NULL: round-robin
+                                    // zero (see take_item)
   const uint16_t* const* grad_tab;  // [P][N]: contributor src's gradient of p
   float* const* shard_tab;          // [N]
   const uint8_t* uniform_phase;     // [P]: 1 if all N gradients of p share addr mod 16
