@@ -9,8 +9,9 @@
 //   * a ring of S stages; a stage holds, for one tile of T = 8*V outputs of one
 //     item, the aligned 16-byte window of every contributor (N windows of at
 //     most 16*V bytes, with V = 256 / M vectors per tile);
-//   * the producer walks the CTA's items (round-robin over the grid, as in
-//     rs_fused) and, per tile, arms the stage's "full" mbarrier with the
+//   * the producer walks the CTA's items (round-robin over the grid: the
+//     consumers follow the producer's order without a shared counter) and,
+//     per tile, arms the stage's "full" mbarrier with the
 //     expected byte count and issues one cp.async.bulk per contributor;
 //   * consumer thread t < V*M takes source node j = t / V and vector
 //     v = t % V of the tile: it sums the node's L contributions from shared memory
