@@ -304,10 +304,17 @@ __device__ __forceinline__ float2 epilogue_v(float2 v, const float* d, int flags
 // 13.54 / 15.93 vs 16.69; float2 on wan22dit 9.646 vs 9.770 / 10.95 vs
 // 11.94.  The M = 1 and float2 instances take 40 registers (6 CTAs per SM);
 // at 32 they spilled.
-template <bool kBatched, int kGroup, class V>
-__global__ void __launch_bounds__(256, kBatched ? 5 : ((kGroup == 1 || sizeof(V) == 8) ? 6 : 8)) rs_land_vec_kernel(const __grid_constant__ RsArgs a) {
+//
+// kVecs = 8 is the instance for landing grids too small to fill the GPU (the
+// pages' 4 landing CTAs per GPU): with at most a CTA or two per SM, the bytes
+// each thread keeps in flight set the speed, and registers are plentiful.
+// Against kVecs = 2 on one box, alternating (whole staged reduce-scatter with
+// 16 + 4 CTAs): llama70b 10.28 vs 15.69 ms, qwen3moe 6.49 vs 10.21, wan22dit
+// 9.86 vs 10.94, uneven 2.49 vs 2.77.
+template <bool kBatched, int kGroup, class V, int kVecs>
+__global__ void __launch_bounds__(256, kVecs > 2 ? 1 : (kBatched ? 5 : ((kGroup == 1 || sizeof(V) == 8) ? 6 : 8)))
+    rs_land_vec_kernel(const __grid_constant__ RsArgs a) {
   constexpr int W = (int)(sizeof(V) / 4);
-  constexpr int kVecs = 2;
   __shared__ const float* part[kMaxM];
   const int M = a.M, L = a.L;
   const int64_t S = a.S, B = a.slice_len;
@@ -405,16 +412,17 @@ __global__ void __launch_bounds__(256, kBatched ? 5 : ((kGroup == 1 || sizeof(V)
 
 using LandKernel = void (*)(RsArgs);
 
-template <class V>
+template <class V, int kVecs>
 LandKernel land_vec_kernel_for(int M, int L) {
-  if (M > L) return rs_land_vec_kernel<true, 1, V>;
-  return M == 1 ? rs_land_vec_kernel<false, 1, V> : rs_land_vec_kernel<false, 2, V>;
+  if (M > L) return rs_land_vec_kernel<true, 1, V, kVecs>;
+  return M == 1 ? rs_land_vec_kernel<false, 1, V, kVecs> : rs_land_vec_kernel<false, 2, V, kVecs>;
 }
 
-// vec: vector width of the landing (4, 2, or 0 for 4-byte accesses)
-LandKernel land_kernel_for(int M, int L, int vec) {
-  if (vec == 4) return land_vec_kernel_for<float4>(M, L);
-  if (vec == 2) return land_vec_kernel_for<float2>(M, L);
+// vec: vector width of the landing (4, 2, or 0 for 4-byte accesses); wide:
+// the landing grid is too small to fill the GPU (8 vectors per thread).
+LandKernel land_kernel_for(int M, int L, int vec, bool wide) {
+  if (vec == 4) return wide ? land_vec_kernel_for<float4, 8>(M, L) : land_vec_kernel_for<float4, 2>(M, L);
+  if (vec == 2) return wide ? land_vec_kernel_for<float2, 8>(M, L) : land_vec_kernel_for<float2, 2>(M, L);
   if (M > L) return rs_land_kernel<true>;
   return M == 1 ? rs_land_kernel<false> : rs_land_grouped_kernel<false, 2>;
 }
@@ -429,7 +437,7 @@ int launch_sum_t(const RsArgs& a, int grid, cudaStream_t s) {
 
 TIDE_BOUNDS_COUNTER(rs_staged_bounds)
 
-int launch_rs_staged(const RsArgs& a, int sum_grid, int land_grid_x, int land_vec, void* stream) {
+int launch_rs_staged(const RsArgs& a, int sum_grid, int land_grid_x, int land_vec, bool land_wide, void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
   int err = (int)cudaErrorInvalidValue;
   switch (a.L) {
@@ -443,13 +451,15 @@ int launch_rs_staged(const RsArgs& a, int sum_grid, int land_grid_x, int land_ve
     case 8: err = launch_sum_t<8>(a, sum_grid, s); break;
   }
   if (err != cudaSuccess) return err;
-  land_kernel_for(a.M, a.L, land_vec)<<<dim3(land_grid_x, a.N), 256, 0, s>>>(a);
+  land_kernel_for(a.M, a.L, land_vec, land_wide)<<<dim3(land_grid_x, a.N), 256, 0, s>>>(a);
   return (int)cudaGetLastError();
 }
 
 int rs_land_blocks_per_sm(int M, int L, int vec) {
   int n = 0;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, land_kernel_for(M, L, vec), 256, 0) == cudaSuccess ? n : 0;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, land_kernel_for(M, L, vec, false), 256, 0) == cudaSuccess
+             ? n
+             : 0;
 }
 
 }  // namespace tide

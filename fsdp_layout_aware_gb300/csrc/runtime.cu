@@ -642,8 +642,9 @@ tide_status tide_rs_staged(tide_plan* pl, const void* const* grads, float* const
   const int land_per_sm = std::max(1, rs_land_blocks_per_sm(pl->M, pl->L, land_vec));  // resident landing CTAs per SM
   const int land_x =
       landing_ctas_per_rank > 0 ? landing_ctas_per_rank : std::max(1, pl->num_sms * land_per_sm / pl->N);
+  const bool land_wide = land_vec != 0 && (int64_t)land_x * pl->N < 2 * (int64_t)pl->num_sms;
   pl->last_launches = 2;
-  return finish(slot, launch_rs_staged(a, (int)sum_grid, land_x, land_vec, stream), (cudaStream_t)stream, "rs_staged launch");
+  return finish(slot, launch_rs_staged(a, (int)sum_grid, land_x, land_vec, land_wide, stream), (cudaStream_t)stream, "rs_staged launch");
 }
 
 tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const* params, int32_t elem_bytes,
