@@ -643,8 +643,10 @@ tide_status tide_rs_staged(tide_plan* pl, const void* const* grads, float* const
   const int land_x =
       landing_ctas_per_rank > 0 ? landing_ctas_per_rank : std::max(1, pl->num_sms * land_per_sm / pl->N);
   const bool land_wide = land_vec != 0 && (int64_t)land_x * pl->N < 2 * (int64_t)pl->num_sms;
+  // a summing grid below the full one that fits one wave at 2 CTAs per SM
+  const bool sum_wide = sum_grid < pl->rs_grid && sum_grid <= 2 * (int64_t)pl->num_sms;
   pl->last_launches = 2;
-  return finish(slot, launch_rs_staged(a, (int)sum_grid, land_x, land_vec, land_wide, stream), (cudaStream_t)stream, "rs_staged launch");
+  return finish(slot, launch_rs_staged(a, (int)sum_grid, sum_wide, land_x, land_vec, land_wide, stream), (cudaStream_t)stream, "rs_staged launch");
 }
 
 tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const* params, int32_t elem_bytes,

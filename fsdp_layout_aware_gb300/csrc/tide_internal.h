@@ -170,8 +170,9 @@ int ag_bulk_smem_bytes();
 int launch_rs_bulk(const RsArgs& args, int grid, void* stream);
 // land_vec: vector width of the landing, 4 or 2 floats (slice length a
 // multiple of it, inbox and shards aligned to it), or 0 for 4-byte accesses;
-// land_wide: the landing grid cannot fill the GPU (more bytes per thread).
-int launch_rs_staged(const RsArgs& args, int sum_grid, int land_grid_x, int land_vec, bool land_wide,
+// sum_wide / land_wide: the summing / landing grid cannot fill the GPU (more
+// bytes in flight per thread).
+int launch_rs_staged(const RsArgs& args, int sum_grid, bool sum_wide, int land_grid_x, int land_vec, bool land_wide,
                      void* stream);
 int rs_land_blocks_per_sm(int M, int L, int vec);  // resident landing CTAs per SM (0 on error)
 BulkLayout rs_bulk_layout(int N, int M, int L, int smem_budget);

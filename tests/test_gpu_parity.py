@@ -358,6 +358,39 @@ def test_full_size_every_rail_all_gather(cfg, exchange):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("cfg", [2, 3], ids=["llama70b_rows16", "qwen3moe_rows16"])
+@pytest.mark.parametrize("budget", [(16, 4), (16, 0), (0, 4)], ids=["pages_16_4", "sum16", "land4"])
+def test_rs_staged_small_grids(cfg, budget):
+    """Budgets whose grids cannot fill the GPU take the wide summing and
+    landing instances (16 summing CTAs per rank on 8 or 16 ranks, 4 landing
+    CTAs per rank), on groups with thousands of work items: the shards must
+    equal tide_rs_reduce's bit for bit, and sampled elements the oracle."""
+    w = configs.scaled(configs.get(cfg), row_div=16)
+    geo = O.geometry(w.shapes, w.N)
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        assert len(plan.items(0)) > 4 * 152   # more items than the full grid has CTAs
+        grads = device_grads(w)
+        flat = tide.pointer_array([grads[r][p] for r in range(w.N) for p in range(w.P)])
+        want = [torch.empty(geo.S, dtype=torch.float32, device=DEV) for _ in range(w.N)]
+        got = [torch.full((geo.S,), float("nan"), dtype=torch.float32, device=DEV) for _ in range(w.N)]
+        inbox = torch.empty(tide.tide_plan_inbox_elems(plan.handle), dtype=torch.float32, device=DEV)
+        plan.rs_reduce(flat, tide.pointer_array(want))
+        tide.tide_rs_staged(plan.handle, flat, tide.pointer_array(got), inbox, *budget)
+        plan.check()
+        for r in range(w.N):
+            assert torch.equal(got[r].view(torch.int32), want[r].view(torch.int32)), r
+        rng = np.random.default_rng(50 + cfg)
+
+        def grad_at(src, p, idx):
+            return w.grad_values(src, p, idx.astype(np.uint64))
+
+        for r, x in _sample_positions(rng, geo, w.N, 300):
+            expect = O.rs_element(geo, w.M, w.L, r, x, grad_at)
+            assert np.float32(got[r][x].item()).view(np.uint32) == np.float32(expect).view(np.uint32), (r, x)
+        del grads, want, got, inbox
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------- kernel choice and waits
 
 @pytest.mark.parametrize("w", [SMALL[0], SMALL[2], SMALL[4], SMALL[5], SMALL[6]], ids=lambda w: w.name)
