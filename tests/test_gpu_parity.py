@@ -603,21 +603,31 @@ def _vec_cases():
 @pytest.mark.parametrize("w", _vec_cases(), ids=lambda w: w.name)
 @pytest.mark.parametrize("aligned", [True, False], ids=["16B", "offset"])
 @pytest.mark.parametrize("budget", [(0, 0), (16, 4)], ids=["fill", "pages_16_4"])
-def test_rs_staged_vector_landing(w, aligned, budget):
+@pytest.mark.parametrize("variant", ["sum", "average_accumulate"])
+def test_rs_staged_vector_landing(w, aligned, budget, variant):
     """With the inbox and every shard on a 16-byte boundary the landing runs
     on 16-byte (slice length a multiple of 4) or 8-byte (slice length 2 mod 4)
-    loads and stores; one element off, it runs the 4-byte kernels.  All give
-    the oracle's bits and leave the guard bands alone."""
+    loads and stores, 8 vectors per thread when its grid cannot fill the GPU
+    (the pages' 4 landing CTAs per rank); one element off, it runs the 4-byte
+    kernels.  All give the oracle's bits, also averaged and accumulated into
+    the previous shard, and leave the guard bands alone."""
     grads = host_grads(w)
-    geo, expect = oracle_rs(w, grads)
+    geo, sums = oracle_rs(w, grads)
     assert O.slice_len(geo.S, w.L) % 4 == (0 if w.name.startswith("vec4") else 2)
+    variants = variant == "average_accumulate"
+    old = [((np.arange(geo.S, dtype=np.float32) % 19) - 9.0) * np.float32(0.25) for _ in range(w.N)]
+    expect = O.rs_finish(geo, sums, average=variants, old=old if variants else None)
     lead = 32 if aligned else 33     # elements before each output: 128 or 132 bytes
     with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        plan.set_option(tide.TIDE_OPT_RS_AVERAGE, int(variants))
+        plan.set_option(tide.TIDE_OPT_RS_ACCUMULATE, int(variants))
         dev = [[to_dev_u16(grads[r][p])[0] for p in range(w.P)] for r in range(w.N)]
         n_inbox = tide.tide_plan_inbox_elems(plan.handle)
         inbox_back = torch.full((n_inbox + 8,), float("nan"), dtype=torch.float32, device=DEV)
         inbox = inbox_back[0 if aligned else 1:][:n_inbox]
         outs = [f32_guarded(geo.S, lead, 29) for _ in range(w.N)]
+        for r in range(w.N):
+            outs[r][0].copy_(torch.from_numpy(old[r]))
         flat = [dev[r][p] for r in range(w.N) for p in range(w.P)]
         tide.tide_rs_staged(plan.handle, flat, [o[0] for o in outs], inbox, *budget)
         plan.check()
