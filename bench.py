@@ -723,8 +723,15 @@ def run_variants(args, local_rank):
                             ("ag_sm", tide.TIDE_AG_SM)):
         plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, transport)
         timed(name, lambda: plan.ag_place(ap, pp, 2, stream), nb["ag_bytes"])
+    # copy engines with the shards as rows of one buffer: one strided copy per parameter
+    ag_rows = torch.empty((N, S), dtype=torch.int16, device=dev)
+    for r in range(N):
+        ag_rows[r].copy_(ag_in[r])
+    rows_p = tide.pointer_array([ag_rows[r] for r in range(N)])
+    plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, tide.TIDE_AG_COPY_ENGINES)
+    timed("ag_copy_engines_rows", lambda: plan.ag_place(rows_p, pp, 2, stream), nb["ag_bytes"])
     plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, tide.TIDE_AG_SM)
-    del params, pp
+    del params, pp, ag_rows
     # Slot-Reuse: every rank's slot is its N*S-element all-gather destination
     slots = [torch.empty(N * S, dtype=torch.int16, device=dev) for _ in range(N)]
     slp = tide.pointer_array(slots)

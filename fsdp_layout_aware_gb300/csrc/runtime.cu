@@ -675,9 +675,34 @@ tide_status tide_ag_place(tide_plan* pl, const void* const* shards, void* const*
   }
   cudaStream_t s = (cudaStream_t)stream;
   if (pl->ag_transport == TIDE_AG_COPY_ENGINES) {
-    // The pages' transport: one copy-engine copy per (parameter, rank) piece,
-    // straight to its final address; no kernel, no device state.
+    // The pages' transport: copy-engine copies straight to the final
+    // addresses; no kernel, no device state.  When the N shards lie at one
+    // constant stride (rows of one buffer), parameter p's N pieces can go as
+    // one strided copy: row r from shards[0] + r*stride + op to
+    // params[p] + r*e_p.  That replaces N host calls by one, which is what
+    // limits small pieces; pieces above kCeStridedMaxPiece go one by one, as
+    // plain copies move large rows faster.  Measured with the shards as rows
+    // of one buffer, against every piece on its own: qwen3moe 2.41 / 25.6 ms,
+    // uneven 1.20 / 45.1 ms, wan22dit 0.74 / 3.30 ms, llama70b 0.67 / 0.76 ms
+    // (its 17-58 MB pieces one by one; all strided it took 0.95 ms).
+    constexpr size_t kCeStridedMaxPiece = size_t(4) << 20;
+    int64_t stride = pl->N > 1 ? (int64_t)((intptr_t)shards[1] - (intptr_t)shards[0]) : 0;
+    bool strided = !pl->ag_unpadded && pl->N > 1 && stride >= pl->S * elem_bytes;
+    for (int32_t r = 2; strided && r < pl->N; ++r)
+      strided = (int64_t)((intptr_t)shards[r] - (intptr_t)shards[0]) == r * stride;
+    if (strided) {
+      int dev = -1, max_pitch = 0;
+      strided = cudaGetDevice(&dev) == cudaSuccess &&
+                cudaDeviceGetAttribute(&max_pitch, cudaDevAttrMaxPitch, dev) == cudaSuccess && stride <= max_pitch;
+    }
     for (int32_t p = 0; p < pl->P; ++p) {
+      const size_t width = (size_t)pl->e[p] * elem_bytes;
+      if (strided && width > 0 && width <= kCeStridedMaxPiece) {
+        TIDE_CUDA(cudaMemcpy2DAsync(params[p], width, (const unsigned char*)shards[0] + (size_t)pl->o[p] * elem_bytes,
+                                    (size_t)stride, width, (size_t)pl->N, cudaMemcpyDeviceToDevice, s),
+                  "all-gather strided copy");
+        continue;
+      }
       for (int32_t r = 0; r < pl->N; ++r) {
         const int64_t n = pl->ag_unpadded ? std::min(pl->Rp[p], std::max<int64_t>(0, pl->rows[p] - r * pl->Rp[p])) *
                                                 pl->Kp[p]

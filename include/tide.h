@@ -206,8 +206,12 @@ typedef enum tide_option {
  * all-gather uses no SM threads ([Richland] "What shipped").
  *   TIDE_AG_SM            (default) one kernel over the work list, every
  *                         thread copying 16-byte words;
- *   TIDE_AG_COPY_ENGINES  one copy-engine copy per (parameter, rank) piece:
- *                         no kernel, N*P host calls per call;
+ *   TIDE_AG_COPY_ENGINES  copy-engine copies, no kernel: one per (parameter,
+ *                         rank) piece, or, when the N shards lie at one
+ *                         constant stride (rows of one buffer) and the
+ *                         unpadded option is off, one strided 2-D copy per
+ *                         parameter whose pieces are at most 4 MiB (larger
+ *                         pieces still go one by one);
  *   TIDE_AG_BULK          bf16 only: one thread per SM moves each piece's
  *                         16-byte aligned middle global -> shared -> global
  *                         with bulk copies (TMA), the SM kernel the rest

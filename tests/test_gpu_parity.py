@@ -637,6 +637,50 @@ def test_rs_staged_vector_landing(w, aligned, budget, variant):
             assert torch.isnan(back[:lead]).all() and torch.isnan(back[lead + geo.S:]).all(), r
 
 
+CE_MIXED = configs.Workload("ce_mixed_pieces", 4, 2, 2, [(4400, 2048), (9, 33), (4, 1024)], [gen.UNIFORM] * 3,
+                            seed=811)   # one 4.5 MB bf16 piece per rank (copied piece by piece), two small ones
+
+
+@pytest.mark.parametrize("w", [SMALL[0], SMALL[3], SMALL[5], CE_MIXED], ids=lambda w: w.name)
+@pytest.mark.parametrize("elem_bytes", [2, 4])
+@pytest.mark.parametrize("layout", ["rows", "padded_rows", "separate", "uneven_spacing", "rows_unpadded"])
+def test_ag_copy_engine_layouts(w, elem_bytes, layout):
+    """The copy-engine all-gather: shards at one constant stride (rows of one
+    buffer, with or without padding between rows) go as one strided copy per
+    parameter whose pieces are at most 4 MiB, larger pieces one by one;
+    separate buffers, unequal spacing and the unpadded destination go piece by
+    piece.  Every layout lands the oracle's bits."""
+    geo = O.geometry(w.shapes, w.N)
+    N, S = w.N, geo.S
+    dt, tdt = (np.uint16, torch.int16) if elem_bytes == 2 else (np.uint32, torch.int32)
+    rng = np.random.default_rng(41)
+    shards_h = [rng.integers(0, np.iinfo(dt).max, S, dtype=dt) for _ in range(N)]
+    unpadded = layout == "rows_unpadded"
+    expect = O.ag_place_unpadded(geo, shards_h) if unpadded else O.ag_place(geo, shards_h)
+    host = [torch.from_numpy(x.view(np.int16 if elem_bytes == 2 else np.int32)) for x in shards_h]
+    if layout in ("rows", "rows_unpadded", "padded_rows"):
+        back = torch.zeros((N, S + (5 if layout == "padded_rows" else 0)), dtype=tdt, device=DEV)
+        shards = [back[r, :S] for r in range(N)]
+    elif layout == "uneven_spacing":
+        back = torch.zeros((N + 1, S + 8), dtype=tdt, device=DEV)
+        shards = [back[r if r < N - 1 else N, :S] for r in range(N)]
+    else:
+        shards = [torch.zeros(S, dtype=tdt, device=DEV) for _ in range(N)]
+    for r in range(N):
+        shards[r].copy_(host[r])
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, tide.TIDE_AG_COPY_ENGINES)
+        plan.set_option(tide.TIDE_OPT_AG_UNPADDED, int(unpadded))
+        sizes = [(geo.rows[p] * geo.Kp[p]) if unpadded else N * geo.e[p] for p in range(w.P)]
+        params = [torch.full((max(1, n) + 16,), -7, dtype=tdt, device=DEV) for n in sizes]
+        plan.ag_place(shards, [x[:n] for x, n in zip(params, sizes)], elem_bytes)
+        torch.cuda.synchronize()
+        for p in range(w.P):
+            got = params[p].cpu().numpy().view(dt)
+            assert np.array_equal(got[:sizes[p]], expect[p]), (layout, p)
+            assert (got[sizes[p]:] == np.array(-7).astype(dt)).all(), (layout, p)   # nothing past the block
+
+
 # --------------------------------------------------------------- variants
 
 @pytest.mark.parametrize("w", [SMALL[0], SMALL[4], SMALL[5], SMALL[6]], ids=lambda w: w.name)
