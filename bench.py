@@ -631,7 +631,8 @@ def run_rd_ag(args, local_rank):
     import fsdp_layout_aware_gb300 as tide
     w, plan, stream, dev, _, ag_in = _setup_inputs(args, local_rank, need_grads=False)
     M, L, S = w.M, w.L, plan.S
-    stages = [torch.empty(M * S, dtype=torch.int16, device=dev) for _ in range(M)]
+    stage_rows = torch.empty((M, M * S), dtype=torch.int16, device=dev)   # rows of one buffer
+    stages = [stage_rows[n] for n in range(M)]
     params = [torch.empty(w.N * plan.e[p], dtype=torch.int16, device=dev) for p in range(w.P)]
     pp = tide.pointer_array(params)
 
@@ -644,7 +645,8 @@ def run_rd_ag(args, local_rank):
 
     # Every rail at once (the rails run concurrently on the pages): one stage
     # init launch, the rounds of all rails, one placement from the slots.
-    all_stages = [torch.empty(M * S, dtype=torch.int16, device=dev) for _ in range(L * M)]
+    all_rows = torch.empty((L * M, M * S), dtype=torch.int16, device=dev)
+    all_stages = [all_rows[i] for i in range(L * M)]
     sh_p, st_p = tide.pointer_array(ag_in), tide.pointer_array(all_stages)
     slot_p = tide.pointer_array(tide.stage_shard_pointers(all_stages, 0, M, L, S, 2))
 

@@ -407,8 +407,10 @@ int32_t tide_rd_send_count(int32_t M, int32_t d);
  *               hold node n's own shard.  Slots 1..M-1 are overwritten.
  *   elem_bytes  2 or 4
  * Every round is one device-to-device copy per node (copy engines, as the
- * pages' transport), enqueued on `stream` in round order; with
- * TIDE_OPT_RD_EXCHANGE = 1 every round is one SM kernel launch instead.
+ * pages' transport), enqueued on `stream` in round order; when the M stage
+ * buffers lie at one constant stride (rows of one buffer) and a round's
+ * copies are at most 16 MiB each, the round is two strided copies instead.
+ * With TIDE_OPT_RD_EXCHANGE = 1 every round is one SM kernel launch.
  * Errors: INVALID_ARG (null or aliasing buffers), CUDA, OUT_OF_MEMORY and
  * DEVICE_MISMATCH (SM exchange: first call's set-up). */
 tide_status tide_ag_rd_exchange(tide_plan* plan, void* const* stages, int32_t elem_bytes, void* stream);
@@ -448,7 +450,9 @@ tide_status tide_ag_stage_init(tide_plan* plan, const void* const* shards, void*
 /* tide_ag_rd_exchange on every rail: afterwards slot k of stages[l*M + n]
  * holds rank ((n + k) mod M)*L + l's shard, for every l and n.  With
  * TIDE_OPT_RD_EXCHANGE = 1 each round is one SM kernel launch covering all
- * rails; with copy engines (default) each round is L*M copies.
+ * rails; with copy engines (default) each round is L*M copies, or two
+ * strided copies per rail when the L*M buffers lie at one constant stride and
+ * the round's copies are at most 16 MiB each.
  *   stages      host array [L*M] of device pointers, slot 0 already filled
  *               (tide_ag_stage_init); slots 1..M-1 are overwritten
  * Errors: INVALID_ARG (null or repeated buffers; with

@@ -255,7 +255,8 @@ def test_full_size_relative_order_sampled():
 
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
 @pytest.mark.parametrize("exchange", [0, 1], ids=["copy_engines", "sm_kernel"])
-def test_all_rails_exchange_with_many_nodes(w, exchange):
+@pytest.mark.parametrize("stage_layout", ["separate", "rows"])
+def test_all_rails_exchange_with_many_nodes(w, exchange, stage_layout):
     """The every-rail exchange with up to 32 nodes (5 rounds, the last one
     sending fewer pieces than it holds when M is not a power of two): every
     stage slot holds the shard the slot rule names, and placement from the
@@ -268,7 +269,11 @@ def test_all_rails_exchange_with_many_nodes(w, exchange):
     shards = [torch.from_numpy(x.view(np.int16)).to(DEV) for x in shards_h]
     with tide.TidePlan(w.shapes, w.N, M, L) as plan:
         plan.set_option(tide.TIDE_OPT_RD_EXCHANGE, exchange)
-        stages = [torch.full((M * S,), -9, dtype=torch.int16, device=DEV) for _ in range(L * M)]
+        if stage_layout == "rows":   # one buffer: the copy engines take strided copies
+            back = torch.full((L * M, M * S), -9, dtype=torch.int16, device=DEV)
+            stages = [back[i] for i in range(L * M)]
+        else:
+            stages = [torch.full((M * S,), -9, dtype=torch.int16, device=DEV) for _ in range(L * M)]
         tide.tide_ag_stage_init(plan.handle, shards, stages, 2)
         tide.tide_ag_rd_exchange_rails(plan.handle, stages, 2)
         torch.cuda.synchronize()

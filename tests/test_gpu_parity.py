@@ -484,7 +484,8 @@ def test_host_buffers_through_the_c_abi():
 @pytest.mark.parametrize("w", [SMALL[0], SMALL[3], SMALL[4], SMALL[5]], ids=lambda w: w.name)
 @pytest.mark.parametrize("elem_bytes", [2, 4])
 @pytest.mark.parametrize("exchange", [0, 1], ids=["copy_engines", "sm_kernel"])
-def test_ag_by_recursive_doubling_matches_direct_landing(w, elem_bytes, exchange):
+@pytest.mark.parametrize("stage_layout", ["separate", "rows"])
+def test_ag_by_recursive_doubling_matches_direct_landing(w, elem_bytes, exchange, stage_layout):
     """All-gather the pages' way -- per rail, recursive-doubling exchange
     between the nodes' stage buffers, then the strided stage placement --
     must land every piece exactly where the direct all-gather does, with the
@@ -501,7 +502,11 @@ def test_ag_by_recursive_doubling_matches_direct_landing(w, elem_bytes, exchange
         for node in sorted({0, M - 1}):
             params = [torch.full((w.N * geo.e[p],), -5, dtype=tdt, device=DEV) for p in range(w.P)]
             for rail in range(L):
-                stages = [torch.full((M * S,), -9, dtype=tdt, device=DEV) for _ in range(M)]
+                if stage_layout == "rows":   # one buffer: the copy engines take strided copies
+                    back = torch.full((M, M * S + 3), -9, dtype=tdt, device=DEV)
+                    stages = [back[n, :M * S] for n in range(M)]
+                else:
+                    stages = [torch.full((M * S,), -9, dtype=tdt, device=DEV) for _ in range(M)]
                 for n in range(M):
                     stages[n][:S].copy_(shards[n * L + rail])
                 tide.tide_ag_rd_exchange(plan.handle, stages, elem_bytes)
@@ -519,7 +524,8 @@ def test_ag_by_recursive_doubling_matches_direct_landing(w, elem_bytes, exchange
 @pytest.mark.parametrize("w", [SMALL[0], SMALL[3], SMALL[4], SMALL[5]], ids=lambda w: w.name)
 @pytest.mark.parametrize("elem_bytes", [2, 4])
 @pytest.mark.parametrize("exchange", [0, 1], ids=["copy_engines", "sm_kernel"])
-def test_ag_by_recursive_doubling_all_rails(w, elem_bytes, exchange):
+@pytest.mark.parametrize("stage_layout", ["separate", "rows"])
+def test_ag_by_recursive_doubling_all_rails(w, elem_bytes, exchange, stage_layout):
     """The same all-gather with every rail at once: stage init, the exchange
     of all rails, then tide_ag_place reading the stage slots.  Every stage
     slot must hold the shard the slot rule names, and every piece must land
@@ -533,7 +539,11 @@ def test_ag_by_recursive_doubling_all_rails(w, elem_bytes, exchange):
     shards = [torch.from_numpy(x.view(np.int16 if elem_bytes == 2 else np.int32)).to(DEV) for x in shards_h]
     with tide.TidePlan(w.shapes, w.N, M, L) as plan:
         plan.set_option(tide.TIDE_OPT_RD_EXCHANGE, exchange)
-        stages = [torch.full((M * S,), -9, dtype=tdt, device=DEV) for _ in range(L * M)]
+        if stage_layout == "rows":   # one buffer: the copy engines take strided copies
+            back = torch.full((L * M, M * S + 3), -9, dtype=tdt, device=DEV)
+            stages = [back[i, :M * S] for i in range(L * M)]
+        else:
+            stages = [torch.full((M * S,), -9, dtype=tdt, device=DEV) for _ in range(L * M)]
         tide.tide_ag_stage_init(plan.handle, shards, stages, elem_bytes)
         assert plan.last_launches() == (1 if S else 0)
         tide.tide_ag_rd_exchange_rails(plan.handle, stages, elem_bytes)
