@@ -24,6 +24,8 @@
 // a plan's work list is uploaded, and every launch leaves it at zero.  Two
 // calls whose work overlaps on the GPU (different streams, no ordering
 // between them) race on the array; issue them on one stream or order them.
+// A call on a stream that is being captured is refused: a captured launch
+// would keep reading whatever a later call leaves in the array.
 
 #include <cuda_runtime.h>
 
@@ -39,13 +41,18 @@ namespace {
 
 // Largest static scratch: work items (32 bytes each), the caller's pointer
 // array, the transposed gradient table, the shard table and the phase flags.
-// The five measured workloads need at most 3.2 MiB.
+// The five measured workloads need at most 5.3 MiB (wan22dit: 172,166 items
+// of 32 bytes are 5.25 MiB of it).
 constexpr size_t kNoallocScratchBytes = size_t(8) << 20;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-std::mutex g_setup_mutex;  // guards the per-device records below
+// One lock per device guards that device's record below, so callers on
+// different devices never wait for one another; callers on one device are
+// serialised, including the waits for their streams that the uploads from
+// pageable memory can bring.
+std::mutex g_device_mutex[kMaxDevices];
 unsigned char* g_scratch_addr[kMaxDevices] = {};
 
 // What the array on a device holds: the plan whose work list and counter are
@@ -112,11 +119,20 @@ extern "C" tide_status tide_rs_reduce_noalloc(const tide_plan* pl, const void* c
                                           " bytes of static scratch; tide_rs_reduce_noalloc is limited to " +
                                           std::to_string(kNoallocScratchBytes) + " bytes (use tide_rs_reduce)");
 
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t err = cudaStreamIsCapturing(s, &cap);
+  if (err != cudaSuccess) return cuda_status(err, "cudaStreamIsCapturing");
+  if (cap != cudaStreamCaptureStatusNone)
+    return fail(TIDE_ERR_INVALID_ARG,
+                "tide_rs_reduce_noalloc called on a stream under capture (its tables live in one shared array "
+                "that later calls rewrite; use tide_rs_reduce in graphs)");
+
   int dev = -1;
-  cudaError_t err = cudaGetDevice(&dev);
+  err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return cuda_status(err, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(TIDE_ERR_INVALID_ARG, "device ordinal beyond 63");
-  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  std::lock_guard<std::mutex> lock(g_device_mutex[dev]);
   if (!g_scratch_addr[dev]) {
     // First call on this device: where the module loader put the array on
     // this device (the address differs per device).
@@ -129,7 +145,6 @@ extern "C" tide_status tide_rs_reduce_noalloc(const tide_plan* pl, const void* c
   DeviceRecord& rec = g_record[dev];
   const std::vector<const void*> gv(grads, grads + n_ptr);
   const std::vector<const void*> sv((const void* const*)shards, (const void* const*)shards + pl->N);
-  cudaStream_t s = (cudaStream_t)stream;
   int launches = 0;
   // On any failure below the record is cleared, so the next call uploads everything.
   auto cuda_fail_rec = [&](cudaError_t e, const char* what) {

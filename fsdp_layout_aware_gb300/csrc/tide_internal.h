@@ -47,8 +47,9 @@ static_assert(sizeof(AgItem) == 32, "AgItem layout");
 // Work-list chunking.  A valid RS chunk covers at most rs_chunk_elems(N)
 // elements and starts on a multiple of it in contributor-index space, so
 // interior chunks are whole, 16-byte aligned runs of every contributor; padding
-// chunks only write, so they are larger.  AG chunks are kAgChunkBytes of
-// payload.
+// chunks only write, so they are larger.  AG chunks are kAgChunkBytes / 2
+// elements whatever the element size: 64 KiB of bf16 payload, 128 KiB when
+// the all-gather moves 4-byte elements.
 constexpr int kRsThreads = 256;
 // An RS item reads 2*N bytes per element.  Items of about 128-256 KB of reads
 // were fastest in a sweep of 1024-32768 elements on the four full-size

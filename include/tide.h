@@ -49,8 +49,8 @@
  *     every replay re-uploads that fixed table, so it uses the pointers
  *     given at capture (the data behind them may change between replays).
  *     A ninth captured call returns TIDE_ERR_INVALID_ARG.  The plan must
- *     outlive its graphs.  tide_rs_reduce_noalloc cannot be captured (it
- *     copies from pageable memory).
+ *     outlive its graphs.  tide_rs_reduce_noalloc returns
+ *     TIDE_ERR_INVALID_ARG on a stream under capture.
  *   - Outputs must not overlap inputs or each other (undefined results
  *     otherwise; TIDE_OPT_CHECK_OVERLAP turns on a host-side check).
  */
@@ -325,7 +325,11 @@ tide_status tide_ag_place(tide_plan* plan, const void* const* shards, void* cons
  *   plan, grads, shards, stream: as for tide_rs_reduce.  The plan's own
  *   device state is not used or created.
  * The first call on a device looks up the array's address on that device;
- * make that first call before any CUDA graph capture.  The array is shared by
+ * make that first call before any CUDA graph capture.  A call on a stream
+ * that is being captured returns TIDE_ERR_INVALID_ARG before touching the
+ * array: a captured launch would keep reading tables that later calls
+ * rewrite.  Host threads calling on one device are serialised (one lock per
+ * device, held across the uploads).  The array is shared by
  * all calls on a device and keeps the last call's contents; the library
  * remembers, per device, which plan's work list it holds and which pointer
  * arrays its tables were built from, and a call copies into it (from

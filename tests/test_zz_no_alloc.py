@@ -103,3 +103,32 @@ def test_noalloc_reuses_what_the_array_holds():
             tide.tide_rs_reduce_noalloc(pa.handle, ga, outs_a)
             assert pa.last_launches() == 2
             check(pa, ga, outs_a)
+
+
+def test_noalloc_refuses_a_stream_under_capture():
+    """A captured launch would keep reading the shared array after later
+    calls rewrote it, so a call on a capturing stream is refused before it
+    touches the array; the next ordinary call is still exact."""
+    w = WORKLOADS[0]
+    with tide.TidePlan(w.shapes, w.N, w.M, w.L) as plan:
+        grads = _device_grads(w, 4000)
+        got = [torch.full((plan.S,), float("nan"), dtype=torch.float32, device=DEV) for _ in range(w.N)]
+        want = [torch.empty(plan.S, dtype=torch.float32, device=DEV) for _ in range(w.N)]
+        tide.tide_rs_reduce_noalloc(plan.handle, grads, got)   # set-up outside any capture
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        status = None
+        with torch.cuda.graph(g, stream=s):
+            try:
+                tide.tide_rs_reduce_noalloc(plan.handle, grads, got, s)
+            except tide.TideError as err:
+                status = err.status
+        assert status == 1
+        for o in got:
+            o.fill_(float("nan"))
+        tide.tide_rs_reduce_noalloc(plan.handle, grads, got)
+        tide.tide_rs_reduce(plan.handle, grads, want)
+        torch.cuda.synchronize()
+        for r in range(w.N):
+            assert torch.equal(got[r].view(torch.int32), want[r].view(torch.int32)), r
