@@ -5,15 +5,19 @@ One step = tide_rs_reduce (bf16 gradients of all N emulated ranks -> N packed
 fp32 shards) + tide_ag_place (N packed bf16 shards -> P parameter-major
 blocks) over one synthetic parameter group, everything resident in HBM.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama70b]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload wan22dit]
     python bench.py --impl reference ...   # the CPU oracle, timed on host cores
 
 Prints one JSON line.  `value` is the effective HBM bandwidth of the step in
 GB/s of algorithmic bytes: reduce-scatter 2*N*G (every contributor's real bf16
 element read once) + 4*N*S (every fp32 shard element written once), all-gather
-2*2*N*S (every bf16 piece read once and written once).  Under torchrun each
-rank runs its own replica on its own GPU (no data-path collective), `value`
-sums all ranks' bytes over the slowest rank's time.
+2*2*N*S (every bf16 piece read once and written once).  The headline workload
+is the largest group, the Wan2.2 DiT block (N = 64); the same step is then
+timed on the other three measured groups (Llama-3.1-70B layer, Qwen3-30B-A3B
+MoE layer, the uneven padding group), one after another with each group's
+buffers freed before the next, and reported under `per_config`.  Under
+torchrun each rank runs its own replica on its own GPU (no data-path
+collective), `value` sums all ranks' bytes over the slowest rank's time.
 """
 
 import argparse
@@ -33,7 +37,10 @@ if ROOT not in sys.path:
 
 METRIC = "RS/AG effective HBM GB/s and % of GB300 HBM peak (1 GPU); elements/s"
 FALLBACK_HBM_GBS = 6800.0
-DEFAULT_WORKLOAD = "llama70b"
+DEFAULT_WORKLOAD = "wan22dit"
+# The four full-size groups the step is measured on; the default run times
+# the headline workload, then the other three under `per_config`.
+MEASURED_GROUPS = ("wan22dit", "llama70b", "qwen3moe", "uneven")
 CLOCK_QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
                "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
                "clocks_event_reasons.sw_power_cap")
@@ -57,9 +64,21 @@ def parse_args(argv=None):
                     help="regroup the workload's N ranks as this many nodes of N / nodes GPUs (e.g. 16 for "
                          "wan22dit as 16 x 4: more nodes than GPUs per node)")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    help="llama70b (default), qwen3moe, wan22dit, uneven or tiny")
+                    help="wan22dit (default), llama70b, qwen3moe, uneven or tiny")
+    ap.add_argument("--per-config", default="auto",
+                    help="groups also timed after the headline, under per_config: 'auto' (the other measured "
+                         "groups when the headline is one of them), 'none', or a comma-separated list")
     ap.add_argument("--row-div", type=int, default=1,
                     help="divide every parameter's rows (a smaller case of the same layer, for profiling)")
+    ap.add_argument("--staged-budget", choices=["both", "fill", "pages"], default="both",
+                    help="staged-rs: CTA budgets timed (fill the GPU, the pages' 16 + 4 per rank, or both)")
+    ap.add_argument("--inbox-offset", type=int, default=0,
+                    help="staged-rs: place the inbox this many floats past a 256-byte boundary (1 forces the "
+                         "4-byte landing kernels)")
+    ap.add_argument("--rd-exchange", choices=["both", "copy-engines", "sm"], default="both",
+                    help="rd-ag: exchange transports timed")
+    ap.add_argument("--rd-mode", choices=["both", "rails", "per-rail"], default="both",
+                    help="rd-ag: every rail at once, rail by rail, or both")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -122,22 +141,42 @@ def kernel_source_digest(name):
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def profiled_traffic(summary_name, kernel_file):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel source
-    it was taken on is the current one; otherwise None."""
-    path = os.path.join(ROOT, "profiles", summary_name)
+def profile_fields(summary_name):
+    """The `key: value` lines of a committed ncu summary under profiles/."""
+    fields = {}
+    with open(os.path.join(ROOT, "profiles", summary_name)) as f:
+        for line in f:
+            if ":" in line and not line.startswith(" "):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+    return fields
+
+
+def profiled_traffic(summary_name, kernel_file, alg_read_full, alg_write_full):
+    """DRAM traffic of one full-size launch, from a committed ncu summary of a
+    smaller capture of the same kernel (a rows/k case of the same group), if
+    the kernel source it was taken on is the current one; otherwise None.
+
+    Reads grow with the contributor bytes, so the captured DRAM reads are
+    scaled by (full-size algorithmic reads / captured algorithmic reads).
+    Writes are not scaled: at the end of a launch part of them is still dirty
+    in L2 (tens of MB whatever the size), so a scaled capture would credit
+    that residue many times over; the full launch's algorithmic writes stand
+    in for them."""
     try:
-        fields = {}
-        with open(path) as f:
-            for line in f:
-                if ":" in line and not line.startswith(" "):
-                    k, v = line.split(":", 1)
-                    fields[k.strip()] = v.strip()
-        if fields.get("kernel_source_sha256") != kernel_source_digest(kernel_file):
+        f = profile_fields(summary_name)
+        if f.get("kernel_source_sha256") != kernel_source_digest(kernel_file):
             return None
-        return float(fields["dram_bytes_per_full_launch"])
+        reads, writes = float(f["dram_bytes_read"]), float(f["dram_bytes_write"])
+        alg_r, alg_w = float(f["algorithmic_read_bytes_captured"]), float(f["algorithmic_write_bytes_captured"])
     except (OSError, KeyError, ValueError):
         return None
+    scale = alg_read_full / alg_r
+    return {"bytes": round(reads * scale + alg_write_full),
+            "source": (f"{f.get('workload_captured', 'a smaller capture')}: DRAM reads x {scale:g} "
+                       f"+ the full launch's algorithmic writes ({summary_name})"),
+            "captured_dram_read_over_algorithmic": round(reads / alg_r, 4),
+            "captured_dram_write_over_algorithmic": round(writes / alg_w, 4)}
 
 
 class ClockSampler:
@@ -163,7 +202,9 @@ class ClockSampler:
             self.proc = None
         return self
 
-    def stop(self, t0, t1):
+    def stop(self, windows):
+        """Median SM clock and the throttle reasons seen in samples taken
+        inside any of the (t0, t1) wall-clock windows (all samples if none)."""
         if self.proc is None:
             return None
         time.sleep(max(0.0, self.t_start + self.MIN_RUN_S - time.time()))
@@ -185,7 +226,7 @@ class ClockSampler:
                 except ValueError:
                     continue
         os.unlink(self.path)
-        inside = [r for r in rows if t0 <= r[0] <= t1] or rows
+        inside = [r for r in rows if any(t0 <= r[0] <= t1 for t0, t1 in windows)] or rows
         if not inside:
             return None
         reasons = sorted({REASON_NAMES[i] for r in inside for i, v in enumerate(r[3]) if v == "Active"})
@@ -207,27 +248,24 @@ def get_workload(args):
     return w
 
 
-def run_ours(args, rank, world, local_rank):
-    import numpy as np
+def per_config_groups(args):
+    """Groups timed after the headline one, under per_config."""
+    if args.per_config == "none":
+        return []
+    if args.per_config == "auto":
+        if args.workload not in MEASURED_GROUPS or args.nodes:
+            return []
+        return [g for g in MEASURED_GROUPS if g != args.workload]
+    return [g.strip() for g in args.per_config.split(",") if g.strip()]
+
+
+def allocate_group(w, plan, dev, stream):
+    """Every rank's bf16 gradients and bf16 packed all-gather shards, filled
+    in HBM by the seeded generator, plus the outputs of both calls."""
     import torch
 
-    import fsdp_layout_aware_gb300 as tide
-    from synth import configs, device, gen
-
-    torch.cuda.set_device(local_rank)
-    init_dist(world, "nccl")
-    dev = torch.device("cuda", local_rank)
-    w = get_workload(args)
-    plan = tide.TidePlan(w.shapes, w.N, w.M, w.L)
-    plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, {"sm": tide.TIDE_AG_SM, "bulk": tide.TIDE_AG_BULK,
-                                                 "copy-engines": tide.TIDE_AG_COPY_ENGINES}[args.ag_transport])
-    geo = plan
-    nbytes = algorithmic_bytes(w, geo)
+    from synth import device, gen
     S = plan.S
-    stream = torch.cuda.Stream(device=dev)
-
-    # Inputs resident in HBM before timing: every rank's bf16 gradients and
-    # bf16 packed parameter shards, from the seeded generator.
     with torch.cuda.stream(stream):
         grads = []
         for r in range(w.N):
@@ -243,25 +281,34 @@ def run_ours(args, rank, world, local_rank):
             ag_in.append(t)
         ag_out = [torch.empty(w.N * plan.e[p], dtype=torch.int16, device=dev) for p in range(w.P)]
     stream.synchronize()
+    return grads, rs_out, ag_in, ag_out
 
+
+def time_group(args, w, world, dev, stream, windows, keep=False):
+    """Warm-up, then K timed steps of one group: one tide_rs_reduce and one
+    tide_ag_place per step on one stream, CUDA events around every call and
+    around the K steps, a barrier and a device synchronisation on both sides.
+    Appends the timed wall-clock window to `windows`."""
+    import torch
+
+    import fsdp_layout_aware_gb300 as tide
+    plan = tide.TidePlan(w.shapes, w.N, w.M, w.L)
+    plan.set_option(tide.TIDE_OPT_AG_TRANSPORT, {"sm": tide.TIDE_AG_SM, "bulk": tide.TIDE_AG_BULK,
+                                                 "copy-engines": tide.TIDE_AG_COPY_ENGINES}[args.ag_transport])
+    nbytes = algorithmic_bytes(w, plan)
+    grads, rs_out, ag_in, ag_out = allocate_group(w, plan, dev, stream)
     # Device addresses marshalled once, as a caller reusing its buffers would.
-    grads_p, rs_out_p = tide.pointer_array(grads), tide.pointer_array(rs_out)
-    ag_in_p, ag_out_p = tide.pointer_array(ag_in), tide.pointer_array(ag_out)
-
-    def step():
-        plan.rs_reduce(grads_p, rs_out_p, stream)
-        plan.ag_place(ag_in_p, ag_out_p, 2, stream)
+    ptrs = (tide.pointer_array(grads), tide.pointer_array(rs_out), tide.pointer_array(ag_in),
+            tide.pointer_array(ag_out))
 
     for _ in range(args.warmup):
-        step()
+        plan.rs_reduce(ptrs[0], ptrs[1], stream)
+        plan.ag_place(ptrs[2], ptrs[3], 2, stream)
     stream.synchronize()
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local_rank).start() if rank == 0 else None
-    if sampler:
-        time.sleep(0.4)   # let nvidia-smi come up before the timed region
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.time()
@@ -269,37 +316,89 @@ def run_ours(args, rank, world, local_rank):
     start.record(stream)
     for k in range(K):
         ev[k][0].record(stream)
-        plan.rs_reduce(grads_p, rs_out_p, stream)
+        plan.rs_reduce(ptrs[0], ptrs[1], stream)
         launches[0] += plan.last_launches()
         ev[k][1].record(stream)
-        plan.ag_place(ag_in_p, ag_out_p, 2, stream)
+        plan.ag_place(ptrs[2], ptrs[3], 2, stream)
         launches[1] += plan.last_launches()
         ev[k][2].record(stream)
     stop.record(stream)
     torch.cuda.synchronize()
-    t_wall1 = time.time()
+    windows.append((t_wall0, time.time()))
     barrier(world)
-    clocks = sampler.stop(t_wall0, t_wall1) if sampler else None
+    plan.check()
 
     local_s = start.elapsed_time(stop) / 1e3
-    rs_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
-    ag_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    rs_ms = statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for k in range(K))
+    ag_ms = statistics.mean(ev[k][1].elapsed_time(ev[k][2]) for k in range(K))
     step_bytes = nbytes["rs_bytes"] + nbytes["ag_bytes"]
     max_s, total_bytes = aggregate(local_s, float(step_bytes * K), world, device=dev)
     _, total_elems = aggregate(local_s, float((nbytes["rs_elems"] + nbytes["ag_elems"]) * K), world, device=dev)
+    res = {"w": w, "plan": plan, "nbytes": nbytes, "max_s": max_s, "total_bytes": total_bytes,
+           "total_elems": total_elems, "rs_ms": rs_ms, "ag_ms": ag_ms, "launches": launches}
+    if keep:
+        res["buffers"] = (grads, rs_out, ag_in, ag_out, ptrs)
+    else:
+        plan.close()
+        del grads, rs_out, ag_in, ag_out, ptrs
+        torch.cuda.empty_cache()
+    return res
 
+
+def call_stats(nbytes, rs_ms, ag_ms, peak):
+    rs_gbs = nbytes["rs_bytes"] / rs_ms / 1e6
+    ag_gbs = nbytes["ag_bytes"] / ag_ms / 1e6
+    return ({"ms": round(rs_ms, 4), "GB_s": round(rs_gbs, 2), "frac": round(rs_gbs / peak, 4),
+             "elements_per_s": round(nbytes["rs_elems"] / rs_ms * 1e3, 1)},
+            {"ms": round(ag_ms, 4), "GB_s": round(ag_gbs, 2), "frac": round(ag_gbs / peak, 4),
+             "elements_per_s": round(nbytes["ag_elems"] / ag_ms * 1e3, 1)})
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    torch.cuda.set_device(local_rank)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(device=dev)
+    peak, peak_kind = measured_hbm_peak()
+    K = args.steps
+    windows = []
+    sampler = ClockSampler(local_rank).start() if rank == 0 else None
+    if sampler:
+        time.sleep(0.4)   # let nvidia-smi come up before the first timed region
+
+    head = time_group(args, get_workload(args), world, dev, stream, windows, keep=True)
+    w, plan, nbytes = head["w"], head["plan"], head["nbytes"]
+    grads, rs_out, ag_in, ag_out, ptrs = head.pop("buffers")
     e2e = None if args.no_e2e else run_e2e(args, plan, w, nbytes, grads, rs_out, ag_in, ag_out, stream, world, dev,
-                                            (grads_p, rs_out_p, ag_in_p, ag_out_p))
+                                            ptrs)
+    plan.close()
+    del grads, rs_out, ag_in, ag_out, ptrs, head["plan"]
+    torch.cuda.empty_cache()
+
+    per_config = {}
+    for name in per_config_groups(args):
+        sub = argparse.Namespace(**{**vars(args), "workload": name, "nodes": 0})
+        g = time_group(args, get_workload(sub), world, dev, stream, windows)
+        rs, ag = call_stats(g["nbytes"], g["rs_ms"], g["ag_ms"], peak)
+        step_gbs = g["total_bytes"] / g["max_s"] / 1e9
+        per_config[name] = {
+            "workload": f"{g['w'].name}: {g['w'].notes}", "N": g["w"].N, "M": g["w"].M, "L": g["w"].L,
+            "P": g["w"].P, "rs_bytes_per_step": g["nbytes"]["rs_bytes"],
+            "ag_bytes_per_step": g["nbytes"]["ag_bytes"], "ms_per_step": round(g["max_s"] / K * 1e3, 4),
+            "GB_s": round(step_gbs, 2), "frac": round(step_gbs / peak, 4), "rs": rs, "ag": ag,
+            "gpu_launches": g["launches"][0] + g["launches"][1]}
+    clocks = sampler.stop(windows) if sampler else None
 
     if rank != 0:
         return None
-    peak, peak_kind = measured_hbm_peak()
-    value = total_bytes / max_s / 1e9
-    rs_avg = statistics.mean(rs_ms) / 1e3
-    ag_avg = statistics.mean(ag_ms) / 1e3
-    rs_gbs = nbytes["rs_bytes"] / rs_avg / 1e9
-    ag_gbs = nbytes["ag_bytes"] / ag_avg / 1e9
-    traffic = profiled_traffic(f"rs_fused_{w.name}.txt", "rs_kernel.cu")
+    max_s, launches = head["max_s"], head["launches"]
+    value = head["total_bytes"] / max_s / 1e9
+    rs, ag = call_stats(nbytes, head["rs_ms"], head["ag_ms"], peak)
+    traffic = profiled_traffic(f"rs_fused_{w.name}.txt", "rs_kernel.cu", 2 * nbytes["rs_elems"],
+                               4 * w.N * nbytes["S"])
+    step_bytes = nbytes["rs_bytes"] + nbytes["ag_bytes"]
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -314,27 +413,32 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "f32",
         "data": "synthetic (seeded SplitMix64 bf16; shapes of the named layer)",
         "config": {"workload": f"{w.name}: {w.notes}", "N": w.N, "M": w.M, "L": w.L, "P": w.P,
-                   "G_elems": nbytes["G"], "S_elems": S, "rs_bytes_per_step": nbytes["rs_bytes"],
+                   "G_elems": nbytes["G"], "S_elems": nbytes["S"], "rs_bytes_per_step": nbytes["rs_bytes"],
                    "ag_bytes_per_step": nbytes["ag_bytes"],
                    "l2": "no flush: %.1f GB of inputs per step >> 129 MB L2" % (step_bytes / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "pct_of_hbm_peak": round(100 * value / peak, 2),
-        "elements_per_s": round(total_elems / max_s, 1),
-        "rs": {"ms": round(rs_avg * 1e3, 4), "GB_s": round(rs_gbs, 2), "frac": round(rs_gbs / peak, 4),
-               "elements_per_s": round(nbytes["rs_elems"] / rs_avg, 1)},
-        "ag": {"ms": round(ag_avg * 1e3, 4), "GB_s": round(ag_gbs, 2), "frac": round(ag_gbs / peak, 4),
-               "elements_per_s": round(nbytes["ag_elems"] / ag_avg, 1)},
-        "roofline": {"kernel": "rs_fused", "bound": "hbm", "achieved": round(rs_gbs, 2), "peak": peak,
-                     "peak_source": peak_kind, "unit": "GB/s", "frac": round(rs_gbs / peak, 4),
-                     "traffic": traffic, "algorithmic_bytes_per_launch": nbytes["rs_bytes"]},
+        "elements_per_s": round(head["total_elems"] / max_s, 1),
+        "rs": rs,
+        "ag": ag,
+        "roofline": {"kernel": "rs_fused", "bound": "hbm", "achieved": rs["GB_s"], "peak": peak,
+                     "peak_source": peak_kind, "unit": "GB/s", "frac": rs["frac"],
+                     "traffic": traffic["bytes"] if traffic else None,
+                     "traffic_source": traffic["source"] if traffic else None,
+                     "algorithmic_bytes_per_launch": nbytes["rs_bytes"]},
+        "per_config": per_config,
         "gpu_launches": launches[0] + launches[1],
         "kernels_per_step": {"rs": launches[0] / K, "ag": launches[1] / K},
         "ag_transport": args.ag_transport,
         "clocks": clocks,
         "e2e": e2e,
     }
+    if traffic:
+        line["roofline"]["traffic_captured_ratios"] = {
+            "dram_read_over_algorithmic": traffic["captured_dram_read_over_algorithmic"],
+            "dram_write_over_algorithmic": traffic["captured_dram_write_over_algorithmic"]}
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(configs.get(args.workload), args.cpu_seconds)
+        line["cpu_baseline"], line["cpu_baseline_all_cores"] = cpu_baselines(args.workload, args.cpu_seconds)
     return line
 
 
@@ -394,8 +498,9 @@ def run_e2e(args, plan, w, nbytes, grads, rs_out, ag_in, ag_out, stream, world, 
     Inputs (every rank's gradients and packed shards) live in pinned host
     memory and outputs are written to pinned host memory.  On GB300 a pinned
     host address is a valid device address, so the library's kernels read the
-    inputs and write the results across NVLink-C2C themselves (15.4 GB in and
-    5.1 GB out per llama70b step); the link is the bound.  For context the
+    inputs and write the results across NVLink-C2C themselves (45.7 GB in and
+    2.1 GB out per wan22dit step, 15.4 GB in and 5.1 GB out per llama70b
+    step); the link is the bound.  For context the
     same step is also timed with explicit staging: copy every input to device
     buffers, run on the device, copy every output back.
     """
@@ -453,26 +558,25 @@ def run_e2e(args, plan, w, nbytes, grads, rs_out, ag_in, ag_out, stream, world, 
 
 # ---------------------------------------------------------------- CPU oracle
 
-def oracle_sample(workload_name, row_div):
+# Row divisors of the CPU samples: every large parameter keeps whole per-rank
+# pieces (wan22dit rows/80: one row of every 5120-row parameter per rank).
+SAMPLE_ROW_DIV = {"llama70b": 64, "qwen3moe": 16, "wan22dit": 80, "uneven": 8, "tiny": 1}
+
+
+def oracle_sample(workload_name):
     """A row subset of the workload (same row lengths, N, M, L) for CPU timing."""
-    import numpy as np
+    from synth import configs
+    div = SAMPLE_ROW_DIV.get(workload_name, 16)
+    w = configs.get(workload_name)
+    return (configs.scaled(w, row_div=div, name=f"{w.name}_rows{div}") if div > 1 else w), div
+
+
+def rank_bytes(w, geo, ranks):
+    """Algorithmic bytes of the reduce-scatter and all-gather work of the
+    given destination ranks (summed over all ranks: 2*N*G + 4*N*S + 4*N*S)."""
     import oracle.tide_oracle as O
-    from synth import configs, gen
-    w = configs.scaled(configs.get(workload_name), row_div=row_div)
-    grads = [[gen.bf16_tensor(w.grad_key(r, p), w.numel(p), w.dists[p], w.sigma) for p in range(w.P)]
-             for r in range(w.N)]
-    geo = O.geometry(w.shapes, w.N)
-    ag_in = [gen.bf16_values(w.ag_key(r), np.arange(geo.S, dtype=np.uint64), gen.UNIFORM) for r in range(w.N)]
-    return w, geo, grads, ag_in
-
-
-def oracle_step(w, geo, grads, ag_in):
-    import oracle.tide_oracle as O
-    O.rs_reduce(geo, grads, w.M, w.L)
-    O.ag_place(geo, ag_in)
-
-
-SAMPLE_ROW_DIV = {"llama70b": 64, "qwen3moe": 16, "wan22dit": 64, "uneven": 8, "tiny": 1}
+    return sum(2 * w.N * sum(O.valid_elems(geo, p, r) for p in range(geo.P)) + 4 * geo.S + 4 * geo.S
+               for r in ranks)
 
 
 def host_info():
@@ -490,44 +594,60 @@ def host_info():
     return {"machine": platform.machine(), "nproc": os.cpu_count(), "cpu": model}
 
 
-def cpu_baseline(w, seconds):
-    """The oracle as it stands, single-threaded, over repeated passes of a row
-    subset of the same workload until `seconds` of CPU time are spent."""
-    div = SAMPLE_ROW_DIV.get(w.name, 16)
-    ws, geo, grads, ag_in = oracle_sample(w.name, div)
+def usable_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def cpu_baselines(name, seconds):
+    """The oracle as it stands, timed on a row sample of the workload: on one
+    host core (every destination rank in one process), and on all host cores
+    (the destination ranks dealt to one process per core, each running the
+    same oracle functions on its own ranks; oracle.parallel).  Each leg runs
+    whole passes until `seconds` have gone by."""
+    import oracle.parallel as OP
+    import oracle.tide_oracle as O
+    ws, div = oracle_sample(name)
+    geo = O.geometry(ws.shapes, ws.N)
     nb = algorithmic_bytes(ws, geo)
-    passes, t0 = 0, time.perf_counter()
-    while True:
-        oracle_step(ws, geo, grads, ag_in)
-        passes += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    gbs = (nb["rs_bytes"] + nb["ag_bytes"]) * passes / el / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "host": host_info(),
-            "sample": f"{w.name} rows/{div} (N={ws.N}, G={nb['G']}, S={nb['S']}): {passes} passes of RS+AG "
-                      f"in {el:.1f} s on one host core (numpy)",
-            "elements_per_s": round((nb["rs_elems"] + nb["ag_elems"]) * passes / el, 1)}
+    host = host_info()
+    one = OP.run(ws, 1, passes=None, seconds=seconds, warmup=1)
+    el, passes = one["seconds"][0], one["passes"][0]
+    single = {"value": round((nb["rs_bytes"] + nb["ag_bytes"]) * passes / el / 1e9, 4), "unit": "GB/s",
+              "cores": 1, "kind": "oracle", "host": host,
+              "sample": f"{name} rows/{div} (N={ws.N}, G={nb['G']}, S={nb['S']}): {passes} passes of RS+AG "
+                        f"in {el:.1f} s in one process (numpy)",
+              "elements_per_s": round((nb["rs_elems"] + nb["ag_elems"]) * passes / el, 1)}
+    cores = usable_cores()
+    mt = OP.run(ws, cores, passes=None, seconds=seconds, warmup=1)
+    done = sum(rank_bytes(ws, geo, ranks) * n for ranks, n in zip(mt["ranks"], mt["passes"]))
+    multi = {"value": round(done / mt["wall"] / 1e9, 4), "unit": "GB/s", "cores": mt["workers"],
+             "kind": "oracle, destination ranks split over one process per core", "host": host,
+             "sample": f"{name} rows/{div}: {mt['workers']} processes, {min(mt['passes'])}-{max(mt['passes'])} "
+                       f"passes each over their ranks in {mt['wall']:.1f} s (numpy)",
+             "speedup_over_one_core": None}
+    multi["speedup_over_one_core"] = round(multi["value"] / single["value"], 2) if single["value"] else None
+    return single, multi
 
 
 def run_reference(args, rank, world):
     """The CPU oracle as the reference arm: rank 0 times K steps, each one
-    RS+AG pass over a row subset of the workload, on one host core."""
+    RS+AG pass over a row subset of the workload, in one process on one host
+    core, after W untimed passes."""
     if rank != 0:
         return None
-    from synth import configs
-    w = configs.get(args.workload)
-    div = SAMPLE_ROW_DIV.get(w.name, 16)
-    ws, geo, grads, ag_in = oracle_sample(w.name, div)
+    import oracle.parallel as OP
+    import oracle.tide_oracle as O
+    ws, div = oracle_sample(args.workload)
+    geo = O.geometry(ws.shapes, ws.N)
     nb = algorithmic_bytes(ws, geo)
-    for _ in range(args.warmup):
-        oracle_step(ws, geo, grads, ag_in)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_step(ws, geo, grads, ag_in)
-    el = time.perf_counter() - t0
+    res = OP.run(ws, 1, passes=max(1, args.steps), warmup=args.warmup)
+    el = res["seconds"][0]
     value = (nb["rs_bytes"] + nb["ag_bytes"]) * args.steps / el / 1e9
-    sample = f"{w.name} rows/{div} (N={ws.N}, G={nb['G']}, S={nb['S']}) per step, one host core (numpy)"
+    sample = f"{args.workload} rows/{div} (N={ws.N}, G={nb['G']}, S={nb['S']}) per step, one host core (numpy)"
+    w = get_workload(args)
     return {
         "impl": "reference",
         "metric": METRIC,
@@ -602,21 +722,26 @@ def run_staged_rs(args, local_rank):
     w, plan, stream, dev, grads, _ = _setup_inputs(args, local_rank, need_ag=False)
     nb = algorithmic_bytes(w, plan)
     shards = [torch.empty(plan.S, dtype=torch.float32, device=dev) for _ in range(w.N)]
-    inbox = torch.empty(tide.tide_plan_inbox_elems(plan.handle), dtype=torch.float32, device=dev)
+    inbox_store = torch.empty(tide.tide_plan_inbox_elems(plan.handle) + args.inbox_offset, dtype=torch.float32,
+                              device=dev)
+    inbox = inbox_store[args.inbox_offset:]
     gp, sp = tide.pointer_array(grads), tide.pointer_array(shards)
     inbox_bytes = 8 * w.M * w.N * plan.S
     out = {"path": "staged-rs", "metric": METRIC, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
            "warmup": args.warmup, "dtype": "f32", "data": "synthetic",
            "config": {"workload": f"{w.name}: {w.notes}", "N": w.N, "M": w.M, "L": w.L,
-                      "rs_bytes_per_step": nb["rs_bytes"], "inbox_extra_bytes_per_step": inbox_bytes}}
-    for name, budget in (("fill", (0, 0)), ("pages_16_4", (16, 4))):
+                      "rs_bytes_per_step": nb["rs_bytes"], "inbox_extra_bytes_per_step": inbox_bytes,
+                      "inbox_offset_floats": args.inbox_offset}}
+    budgets = [("fill", (0, 0)), ("pages_16_4", (16, 4))]
+    budgets = [b for b in budgets if args.staged_budget == "both" or b[0].startswith(args.staged_budget)]
+    for name, budget in budgets:
         t = _event_time(lambda: tide.tide_rs_staged(plan.handle, gp, sp, inbox, *budget, stream=stream),
                         args.steps, args.warmup, stream)
         out[name] = {"ms": round(t * 1e3, 4), "GB_s_algorithmic": round(nb["rs_bytes"] / t / 1e9, 1),
                      "GB_s_with_inbox": round((nb["rs_bytes"] + inbox_bytes) / t / 1e9, 1)}
     t = _event_time(lambda: plan.rs_reduce(gp, sp, stream), args.steps, args.warmup, stream)
     out["fused_ms"] = round(t * 1e3, 4)
-    out["value"] = out["fill"]["GB_s_algorithmic"]
+    out["value"] = out[budgets[0][0]]["GB_s_algorithmic"]
     return out
 
 
@@ -662,22 +787,27 @@ def run_rd_ag(args, local_rank):
     exch_bytes = L * M * (M - 1) * S * 2 * 2
     moved = init_bytes + place_bytes + exch_bytes
     res, res_rails = {}, {}
+    picked = {"both": ("copy_engines", "sm_kernel"), "copy-engines": ("copy_engines",), "sm": ("sm_kernel",)}
+    transports = [(n, m) for n, m in (("copy_engines", 0), ("sm_kernel", 1)) if n in picked[args.rd_exchange]]
     with torch.cuda.stream(stream):
-        for name, mode in (("copy_engines", 0), ("sm_kernel", 1)):
+        for name, mode in transports:
             plan.set_option(tide.TIDE_OPT_RD_EXCHANGE, mode)
-            t = _event_time(step, max(1, args.steps // 8), args.warmup, stream)
-            res[name] = {"ms_per_step": round(t * 1e3, 4), "GB_s": round(moved / t / 1e9, 1)}
-            t = _event_time(step_rails, args.steps, args.warmup, stream)
-            res_rails[name] = {"ms_per_step": round(t * 1e3, 4), "GB_s": round(moved / t / 1e9, 1)}
+            if args.rd_mode in ("both", "per-rail"):
+                t = _event_time(step, max(1, args.steps // 8), args.warmup, stream)
+                res[name] = {"ms_per_step": round(t * 1e3, 4), "GB_s": round(moved / t / 1e9, 1)}
+            if args.rd_mode in ("both", "rails"):
+                t = _event_time(step_rails, args.steps, args.warmup, stream)
+                res_rails[name] = {"ms_per_step": round(t * 1e3, 4), "GB_s": round(moved / t / 1e9, 1)}
         ta = _event_time(lambda: plan.ag_place(tide.pointer_array(ag_in), pp, 2, stream), args.steps, args.warmup,
                          stream)
     plan.check()
+    head = (res_rails or res)[transports[0][0]]
     return {"path": "rd-ag", "metric": METRIC, "unit": "GB/s", "n_gpus": 1, "dtype": "bf16 copy", "data": "synthetic",
             "config": {"workload": f"{w.name}: {w.notes}", "N": w.N, "M": M, "L": L,
                        "rounds": tide.tide_rd_rounds(M)},
             "stage_init_bytes": init_bytes, "placement_bytes": place_bytes, "exchange_bytes": exch_bytes,
             "exchange": res, "exchange_all_rails": res_rails,
-            "ms_per_step": res_rails["copy_engines"]["ms_per_step"], "value": res_rails["copy_engines"]["GB_s"],
+            "ms_per_step": head["ms_per_step"], "value": head["GB_s"],
             "direct_landing_ms": round(ta * 1e3, 4)}
 
 

@@ -218,17 +218,19 @@ def _node_partial(grad_slice_of, n_src, L, count):
     return acc1
 
 
-def rs_reduce(geo, grads, M, L, order=LANDING):
+def rs_reduce(geo, grads, M, L, order=LANDING, ranks=None):
     """Reduce-scatter of grads[rank][p] (uint16 bf16 bits, R_p*Kp row-major).
 
     Returns N float32 arrays of S elements: rank r's packed fp32 gradient shard.
-    ``order`` picks the level-2 reading (R5 or R14).
+    ``order`` picks the level-2 reading (R5 or R14).  ``ranks`` (default: all)
+    restricts the result to those destination ranks, in the order given; each
+    rank's shard is computed exactly as in the full call.
     """
     N = geo.N
     if N != M * L:
         raise ValueError("N must equal M * L")
     shards = []
-    for r in range(N):
+    for r in (range(N) if ranks is None else ranks):
         n_dest = r // L
         out = np.empty(geo.S, dtype=np.float32)
         for p in range(geo.P):
@@ -289,19 +291,21 @@ def rs_element(geo, M, L, r, x, grad_at, order=LANDING):
 # [Abstract] Figure 1 and Figure 5(b).
 # --------------------------------------------------------------------------
 
-def ag_place(geo, shards):
+def ag_place(geo, shards, ranks=None, out=None):
     """All-gather of N packed shards (1-D arrays of S elements, any dtype).
 
     Returns P arrays: parameter p as its padded N*Rp x Kp block, flattened
-    (Reading R9; the parameter proper is its first R_p rows).
+    (Reading R9; the parameter proper is its first R_p rows).  ``out``
+    (default: fresh arrays) receives the blocks instead; ``ranks`` (default:
+    all) places only those ranks' pieces, leaving the rest of ``out`` as it is.
     """
-    params = []
+    params = out if out is not None else [np.empty(geo.N * geo.e[p], dtype=shards[0].dtype)
+                                          for p in range(geo.P)]
     for p in range(geo.P):
         e_p, o_p = geo.e[p], geo.o[p]
-        block = np.empty(geo.N * e_p, dtype=shards[0].dtype)
-        for r in range(geo.N):
+        block = params[p]
+        for r in (range(geo.N) if ranks is None else ranks):
             block[r * e_p:(r + 1) * e_p] = shards[r][o_p:o_p + e_p]
-        params.append(block)
     return params
 
 

@@ -43,6 +43,15 @@ def test_default_line_has_every_contract_key():
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(rec["clocks"] or {})
     assert rec["gpu_launches"] == 2 * K   # one reduce-scatter and one all-gather kernel per step
+    mt = rec["cpu_baseline_all_cores"]
+    assert mt["cores"] >= 1 and mt["value"] > 0 and mt["sample"]
+    # the other three measured groups, at the same row divisor, each with its own calls' figures
+    assert set(rec["per_config"]) == {"wan22dit", "qwen3moe", "uneven"}
+    for name, g in rec["per_config"].items():
+        assert g["gpu_launches"] == 2 * K and g["GB_s"] > 0, name
+        for call in ("rs", "ag"):
+            assert g[call]["frac"] == pytest.approx(g[call]["GB_s"] / roof["peak"], rel=1e-3), (name, call)
+        assert g["rs"]["GB_s"] == pytest.approx(g["rs_bytes_per_step"] / g["rs"]["ms"] / 1e6, rel=1e-3)
 
 
 @pytest.mark.parametrize("path", ["staged-rs", "rd-ag", "variants"])
