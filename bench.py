@@ -53,11 +53,14 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--path", choices=["fused", "staged-rs", "rd-ag", "variants"], default="fused",
+    ap.add_argument("--path", choices=["fused", "staged-rs", "rd-ag", "variants", "ag-ceiling"], default="fused",
                     help="fused: the hot path (RS + AG per step); staged-rs: the two-stage reduce-scatter "
                          "through an inbox; rd-ag: the all-gather by recursive-doubling exchange and stage "
                          "placement; variants: bulk-copy RS kernel, averaging / accumulating RS, "
-                         "Slot-Reuse pack + RS from slots, unpadded AG, AG transports")
+                         "Slot-Reuse pack + RS from slots, unpadded AG, AG transports; ag-ceiling: "
+                         "tide_ag_place against a plain device copy of the same bytes, each after an L2 flush")
+    ap.add_argument("--variants", default="all",
+                    help="variants: comma-separated subset of the timed variants (default all)")
     ap.add_argument("--ag-transport", choices=["sm", "bulk", "copy-engines"], default="sm",
                     help="how tide_ag_place moves the pieces (default: the SM kernel)")
     ap.add_argument("--nodes", type=int, default=0,
@@ -830,7 +833,11 @@ def run_variants(args, local_rank):
     pp = tide.pointer_array(params)
     res = {}
 
+    picked = None if args.variants == "all" else {v.strip() for v in args.variants.split(",")}
+
     def timed(name, fn, nbytes, setup=None):
+        if picked is not None and name not in picked:
+            return
         with torch.cuda.stream(stream):
             t = _event_time(fn, args.steps, args.warmup, stream)
         res[name] = {"ms": round(t * 1e3, 4), "bytes": nbytes, "GB_s": round(nbytes / t / 1e9, 1)}
@@ -870,10 +877,71 @@ def run_variants(args, local_rank):
     timed("slot_pack", lambda: tide.tide_slot_pack(plan.handle, gp, slp, stream), 4 * N * G)
     timed("rs_from_slots", lambda: tide.tide_rs_reduce_slots(plan.handle, slp, sp, stream), nb["rs_bytes"])
     plan.check()
+    head = res.get("rs_average_accumulate") or next(iter(res.values()), {"GB_s": None})
     return {"path": "variants", "metric": METRIC, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "dtype": "f32 sums of bf16", "data": "synthetic",
             "config": {"workload": f"{w.name}: {w.notes}", "N": N, "M": w.M, "L": w.L, "G": G, "S": S},
-            "value": res["rs_average_accumulate"]["GB_s"], "variants": res}
+            "value": head["GB_s"], "variants": res}
+
+
+def run_ag_ceiling(args, local_rank):
+    """The all-gather against the copy ceiling at its own size: for each
+    group, tide_ag_place and a plain device-to-device copy (torch copy_) of
+    the same bytes (N*S bf16 read and written), each timed alone with CUDA
+    events right after a 512 MiB fill that flushes L2, median of K."""
+    import torch
+
+    import fsdp_layout_aware_gb300 as tide
+    from synth import device, gen
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    peak, _ = measured_hbm_peak()
+
+    def median_ms(fn):
+        ts = []
+        for _ in range(max(1, args.steps)):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    groups = [args.workload] + (per_config_groups(args) if args.workload in MEASURED_GROUPS else [])
+    out = {}
+    for name in groups:
+        sub = argparse.Namespace(**{**vars(args), "workload": name, "nodes": 0})
+        w = get_workload(sub)
+        plan = tide.TidePlan(w.shapes, w.N, w.M, w.L)
+        shards = []
+        for r in range(w.N):
+            t = torch.empty(plan.S, dtype=torch.int16, device=dev)
+            device.fill_bf16(t, w.ag_key(r), gen.UNIFORM)
+            shards.append(t)
+        params = [torch.empty(w.N * plan.e[p], dtype=torch.int16, device=dev) for p in range(w.P)]
+        sp, pp = tide.pointer_array(shards), tide.pointer_array(params)
+        src = torch.empty(w.N * plan.S, dtype=torch.int16, device=dev)
+        dst = torch.empty_like(src)
+        for _ in range(max(1, args.warmup)):
+            plan.ag_place(sp, pp, 2, stream)
+            dst.copy_(src)
+        nbytes = 4 * w.N * plan.S
+        ag = median_ms(lambda: plan.ag_place(sp, pp, 2, stream))
+        cp = median_ms(lambda: dst.copy_(src))
+        plan.check()
+        out[name] = {"bytes_read_plus_written": nbytes, "ag_ms": round(ag, 4), "copy_ms": round(cp, 4),
+                     "ag_frac": round(nbytes / ag / 1e6 / peak, 4), "copy_frac": round(nbytes / cp / 1e6 / peak, 4),
+                     "ag_over_copy": round(cp / ag, 4)}
+        plan.close()
+        del shards, params, src, dst
+        torch.cuda.empty_cache()
+    return {"path": "ag-ceiling", "metric": "all-gather and same-size copy, fraction of measured copy bandwidth",
+            "unit": "fraction", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "data": "synthetic",
+            "value": out[groups[0]]["ag_over_copy"], "groups": out}
 
 
 def main(argv=None):
@@ -887,6 +955,8 @@ def main(argv=None):
         line = run_rd_ag(args, local_rank) if rank == 0 else None
     elif args.path == "variants":
         line = run_variants(args, local_rank) if rank == 0 else None
+    elif args.path == "ag-ceiling":
+        line = run_ag_ceiling(args, local_rank) if rank == 0 else None
     else:
         line = run_ours(args, rank, world, local_rank)
     if line is not None:

@@ -6,21 +6,25 @@
 // shared-memory ring, not by registers:
 //
 //   * one CTA per SM, a producer warp and 8 consumer warps;
-//   * a ring of S stages; a stage holds, for one tile of T = 8*V outputs of one
-//     item, the aligned 16-byte window of every contributor (N windows of at
-//     most 16*V bytes, with V = 256 / M vectors per tile);
+//   * a ring of S stages; a stage holds, for one tile of T = 8*V = 2048
+//     outputs of one item and one source node, the aligned 16-byte windows of
+//     that node's L contributors (L windows of at most 4 KiB), so a tile
+//     takes M stages;
 //   * the producer walks the CTA's items (round-robin over the grid: the
 //     consumers follow the producer's order without a shared counter) and,
-//     per tile, arms the stage's "full" mbarrier with the
-//     expected byte count and issues one cp.async.bulk per contributor;
-//   * consumer thread t < V*M takes source node j = t / V and vector
-//     v = t % V of the tile: it sums the node's L contributions from shared memory
-//     (level 1, l ascending) and writes the 8 fp32 partials to a transposition
-//     buffer; after a consumer barrier, thread t produces outputs t, t+256, ...
-//     by adding the M partials of each in the Latin-square landing order
-//     (level 2) and stores them (consecutive threads, consecutive addresses);
+//     per tile, fills one stage per source node in the tile's level-2 order
+//     (the Latin-square landing order of its slice): it arms the stage's
+//     "full" mbarrier with the expected byte count and issues one
+//     cp.async.bulk per contributor.  Every request moves a whole window, so
+//     the request count per byte does not grow with the number of nodes;
+//   * consumer thread v owns vector v (outputs 8v .. 8v+7) of every tile: per
+//     stage it sums the node's L contributions from shared memory (level 1,
+//     l ascending) and adds the partial to its running level-2 sum in
+//     registers (batches of L nodes when M > L); after the tile's last node
+//     it stores its 8 finished outputs (16-byte stores, realigned across
+//     lanes when the shard is not 16-byte aligned there);
 //   * a consumer warp releases the stage ("empty" mbarrier) as soon as its
-//     level-1 loads are done, so the producer refills it while level 2 runs.
+//     level-1 loads are done, so the producer refills it while the sums run.
 //
 // Padding ranges are zero-filled by the consumers; parameters whose N
 // gradients do not share an address phase mod 16 (bulk copies need 16-byte
@@ -56,6 +60,8 @@ struct TileDesc {
   int32_t p;         // DIRECT: parameter
   uint32_t ord_lo;   // level-2 source-node order, one byte per node: nodes 0..3
   uint32_t ord_hi;   //   and 4..7 (M <= 8)
+  int32_t k;         // BULK: the stage holds the windows of the k-th node in the level-2 order
+  int32_t pad_;
 };
 
 __device__ __forceinline__ void consumer_barrier() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
@@ -71,11 +77,9 @@ __device__ __forceinline__ uint4 lds16(const unsigned char* p) {
 // Shared-memory carve-up, computed on the host (rs_bulk_layout).
 struct Smem {
   unsigned char* stages;
-  float* part;           // 2 x V*PS transposition buffers
   TileDesc* desc;        // [S]
   uint64_t* full;        // [S]
   uint64_t* empty;       // [S]
-  const uint16_t** src;  // [kMaxN] DIRECT tiles
   int* ctl;              // [0] abort flag, [1 + s] rounds issued on stage s,
                          // [1 + kMaxBulkStages + s] consumers' wait result for stage s
 };
@@ -83,11 +87,9 @@ struct Smem {
 __device__ __forceinline__ Smem carve(unsigned char* base, const RsArgs& a) {
   Smem m;
   m.stages = base;
-  m.part = reinterpret_cast<float*>(base + a.bulk.off_part);
   m.desc = reinterpret_cast<TileDesc*>(base + a.bulk.off_desc);
   m.full = reinterpret_cast<uint64_t*>(base + a.bulk.off_bar);
   m.empty = m.full + a.bulk.stages;
-  m.src = reinterpret_cast<const uint16_t**>(base + a.bulk.off_src);
   m.ctl = reinterpret_cast<int*>(base + a.bulk.off_ctl);
   return m;
 }
@@ -176,39 +178,47 @@ __device__ void producer(const RsArgs& a, const Smem& m) {
       advance();
       continue;
     }
+    // Lane c holds contributor c's pointer (g0) and contributor c + 32's (g1).
     const uint16_t* g0 = lane < N ? a.grad_tab[(int64_t)item.p * N + lane] + item.src_off : nullptr;
     const uint16_t* g1 = lane + 32 < N ? a.grad_tab[(int64_t)item.p * N + lane + 32] + item.src_off : nullptr;
     const uintptr_t first = __shfl_sync(0xffffffffu, (unsigned long long)(uintptr_t)g0, 0);
     const int ph0 = (int)((first >> 1) & 7);
-    for (int e = 0; e < item.n;) {
+    for (int e = 0; ok && e < item.n;) {
       const int ph = e == 0 ? ph0 : 0;
       const int nt = min(item.n - e, T - ph);
       const uint32_t bytes = (uint32_t)((2 * (ph + nt) + 15) & ~15);
-      if (!(ok = acquire())) break;
-      unsigned char* sbuf = m.stages + (size_t)stage * a.bulk.stage_bytes;
-      const bool drop = tile == a.bulk.test_drop_tile;
-      if (lane == 0) {
-        TileDesc d;
-        d.dst = dst + e;
-        d.src_off = 0;
-        d.n = nt;
-        d.ph = ph;
-        d.kind = TILE_BULK;
-        d.p = item.p;
-        d.ord_lo = ord_lo;
-        d.ord_hi = ord_hi;
-        m.desc[stage] = d;
-        if (!drop) {
-          mbar_arrive_expect_tx(&m.full[stage], bytes * (uint32_t)N);
-          m.ctl[1 + stage] = (int)round + 1;
+      for (int k = 0; k < a.M; ++k) {
+        if (!(ok = acquire())) break;
+        // the k-th node of the level-2 order; lane l < L loads its contributor node*L + l
+        const int node = (int)(((k < 4 ? ord_lo >> (8 * k) : ord_hi >> (8 * (k - 4)))) & 0xFFu);
+        const int c = node * L + (lane < L ? lane : 0);
+        const uintptr_t p0 = __shfl_sync(0xffffffffu, (unsigned long long)(uintptr_t)g0, c & 31);
+        const uintptr_t p1 = __shfl_sync(0xffffffffu, (unsigned long long)(uintptr_t)g1, c & 31);
+        const uint16_t* gsrc = reinterpret_cast<const uint16_t*>(c < 32 ? p0 : p1);
+        unsigned char* sbuf = m.stages + (size_t)stage * a.bulk.stage_bytes;
+        const bool drop = tile == a.bulk.test_drop_tile;
+        if (lane == 0) {
+          TileDesc d;
+          d.dst = dst + e;
+          d.src_off = 0;
+          d.n = nt;
+          d.ph = ph;
+          d.kind = TILE_BULK;
+          d.p = item.p;
+          d.ord_lo = ord_lo;
+          d.ord_hi = ord_hi;
+          d.k = k;
+          d.pad_ = 0;
+          m.desc[stage] = d;
+          if (!drop) {
+            mbar_arrive_expect_tx(&m.full[stage], bytes * (uint32_t)L);
+            m.ctl[1 + stage] = (int)round + 1;
+          }
         }
+        __syncwarp();
+        if (!drop && lane < L) bulk_load(sbuf + (size_t)lane * 16 * V, gsrc + e - ph, bytes, &m.full[stage]);
+        advance();
       }
-      __syncwarp();
-      if (!drop) {
-        if (g0) bulk_load(sbuf + (size_t)lane * 16 * V, g0 + e - ph, bytes, &m.full[stage]);
-        if (g1) bulk_load(sbuf + (size_t)(lane + 32) * 16 * V, g1 + e - ph, bytes, &m.full[stage]);
-      }
-      advance();
       e += nt;
     }
   }
@@ -227,14 +237,18 @@ __device__ void consumers(const RsArgs& a, const Smem& m) {
   const int lane = tid & 31;
   const int M = a.M;
   const int V = a.bulk.V;
-  const int PS = a.bulk.PS;
   volatile int* abort_flag = m.ctl;
   uint32_t stage = 0, round = 0;
-  int pb = 0;
+  // Level-2 state of this thread's vector, carried across the M stages of a
+  // tile: the running batch sum and the running total.
+  float acc2[8], bsum[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc2[i] = bsum[i] = 0.f;
   for (;;) {
     // The consumer warps decide as one (a named barrier must never lose a
     // participant): thread 0 waits, publishes the answer in this stage's slot,
-    // and every thread then acquires the completed phase itself.
+    // and every thread then acquires the completed phase itself.  (Every warp
+    // waiting on the mbarrier by itself measured 3-5% slower.)
     if (tid == 0) m.ctl[1 + kMaxBulkStages + stage] = wait_phase(&m.full[stage], round & 1, abort_flag, a) ? 1 : 0;
     consumer_barrier();
     if (!m.ctl[1 + kMaxBulkStages + stage]) break;
@@ -244,26 +258,32 @@ __device__ void consumers(const RsArgs& a, const Smem& m) {
     if (d.kind == TILE_BULK) {
       const unsigned char* sbuf = m.stages + (size_t)stage * a.bulk.stage_bytes;
       const int nvec = (d.ph + d.n + 7) >> 3;
-      if (M == 1) {
-        // One node: the level-1 sum is the result.  Thread v stores its 8
-        // outputs (16-byte stores, realigned across lanes when needed).
-        float acc2[8];
+      if (tid < nvec) {
+        // level 1: the node's L contributions, l ascending
+        float acc1[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc2[i] = 0.f;
-        if (tid < nvec) {
-          float acc1[8];
+        for (int i = 0; i < 8; ++i) acc1[i] = 0.f;
+        uint4 x[L];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc1[i] = 0.f;
-          uint4 x[L];
+        for (int l = 0; l < L; ++l) x[l] = lds16(sbuf + (size_t)l * 16 * V + 16 * tid);
 #pragma unroll
-          for (int l = 0; l < L; ++l) x[l] = lds16(sbuf + (size_t)l * 16 * V + 16 * tid);
+        for (int l = 0; l < L; ++l) add_bf16x8(acc1, x[l]);
+        // level 2: this node is the d.k-th of the tile's order; a batch of L
+        // ends after every L-th node and at the last
 #pragma unroll
-          for (int l = 0; l < L; ++l) add_bf16x8(acc1, x[l]);
+        for (int i = 0; i < 8; ++i) bsum[i] = __fadd_rn(bsum[i], acc1[i]);
+        if ((d.k + 1) % L == 0 || d.k + 1 == M) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc2[i] = __fadd_rn(acc2[i], acc1[i]);
+          for (int i = 0; i < 8; ++i) {
+            acc2[i] = __fadd_rn(acc2[i], bsum[i]);
+            bsum[i] = 0.f;
+          }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&m.empty[stage]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m.empty[stage]);  // this warp is done reading the stage
+      if (d.k + 1 == M) {
+        // the tile's last node: thread v holds the finished sums of its 8 outputs
         if (tid - lane < nvec) {  // warp-uniform: the shuffles need every lane
           const int delta = (int)(((unsigned)d.ph - (unsigned)((uintptr_t)d.dst >> 2)) & 3u);
           const int e0 = tid * 8 - d.ph;
@@ -273,49 +293,8 @@ __device__ void consumers(const RsArgs& a, const Smem& m) {
           else
             store8_shifted(d.dst, e0, d.n, delta, lane, acc2);
         }
-      } else {
-        float* part = m.part + pb * V * PS;
-        if (tid < V * M) {
-          // consecutive threads take consecutive vectors of one node, so a
-          // warp's 16-byte loads hit consecutive shared-memory addresses
-          const int j = tid / V, v = tid - (tid / V) * V;
-          if (v < nvec) {
-            float acc1[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc1[i] = 0.f;
-            uint4 x[L];
-#pragma unroll
-            for (int l = 0; l < L; ++l) x[l] = lds16(sbuf + (size_t)(j * L + l) * 16 * V + 16 * v);
-#pragma unroll
-            for (int l = 0; l < L; ++l) add_bf16x8(acc1, x[l]);
-            float4* o = reinterpret_cast<float4*>(part + v * PS + j * 8);
-            o[0] = make_float4(acc1[0], acc1[1], acc1[2], acc1[3]);
-            o[1] = make_float4(acc1[4], acc1[5], acc1[6], acc1[7]);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&m.empty[stage]);  // this warp is done reading the stage
-        consumer_barrier();
-#pragma unroll 4
-        for (int e = tid; e < d.n; e += kConsumers) {
-          const int x = e + d.ph;
-          const float* pv = part + (x >> 3) * PS + (x & 7);
-          float acc2 = 0.f, bsum = 0.f;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t node = (k < 4 ? d.ord_lo >> (8 * k) : d.ord_hi >> (8 * (k - 4))) & 0xFFu;
-            if (k < M) {
-              bsum = __fadd_rn(bsum, pv[node * 8]);
-              if ((k + 1) % L == 0 || k + 1 == M) {  // end of a batch of L sources
-                acc2 = __fadd_rn(acc2, bsum);
-                bsum = 0.f;
-              }
-            }
-          }
-          if (store_ok(d.dst + e, 4, d.dst, d.dst + d.n))
-            __stcs(d.dst + e, epilogue1(acc2, d.dst + e, a.epilogue, a.N));
-        }
-        pb ^= 1;
+        for (int i = 0; i < 8; ++i) acc2[i] = bsum[i] = 0.f;
       }
     } else if (d.kind == TILE_PAD) {
       __syncwarp();
@@ -324,14 +303,12 @@ __device__ void consumers(const RsArgs& a, const Smem& m) {
     } else {  // TILE_DIRECT: contributors at different address phases
       __syncwarp();
       if (lane == 0) mbar_arrive(&m.empty[stage]);
-      consumer_barrier();  // previous DIRECT tile's readers of src[] are done
-      if (tid < a.N) m.src[tid] = a.grad_tab[(int64_t)d.p * a.N + tid] + d.src_off;
-      consumer_barrier();
+      const uint16_t* const* gtab = a.grad_tab + (int64_t)d.p * a.N;
       for (int e0 = tid * 8; e0 < d.n; e0 += kConsumers * 8) {
         const int cnt = min(8, d.n - e0);
-        float acc2[8], bsum[8];
+        float sum2[8], bs[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc2[i] = bsum[i] = 0.f;
+        for (int i = 0; i < 8; ++i) sum2[i] = bs[i] = 0.f;
         for (int k = 0; k < M; ++k) {
           const int node = (int)(((k < 4 ? d.ord_lo >> (8 * k) : d.ord_hi >> (8 * (k - 4)))) & 0xFFu);
           float acc1[8];
@@ -339,25 +316,25 @@ __device__ void consumers(const RsArgs& a, const Smem& m) {
           for (int i = 0; i < 8; ++i) acc1[i] = 0.f;
 #pragma unroll
           for (int l = 0; l < L; ++l) {
-            const uint16_t* s = m.src[node * L + l] + e0;
+            const uint16_t* src = gtab[node * L + l] + d.src_off + e0;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              if (i < cnt) acc1[i] = __fadd_rn(acc1[i], __uint_as_float((uint32_t)__ldcs(s + i) << 16));
+              if (i < cnt) acc1[i] = __fadd_rn(acc1[i], __uint_as_float((uint32_t)__ldcs(src + i) << 16));
           }
 #pragma unroll
-          for (int i = 0; i < 8; ++i) bsum[i] = __fadd_rn(bsum[i], acc1[i]);
+          for (int i = 0; i < 8; ++i) bs[i] = __fadd_rn(bs[i], acc1[i]);
           if ((k + 1) % L == 0 || k + 1 == M) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              acc2[i] = __fadd_rn(acc2[i], bsum[i]);
-              bsum[i] = 0.f;
+              sum2[i] = __fadd_rn(sum2[i], bs[i]);
+              bs[i] = 0.f;
             }
           }
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           if (i < cnt && store_ok(d.dst + e0 + i, 4, d.dst, d.dst + d.n))
-            __stcs(d.dst + e0 + i, epilogue1(acc2[i], d.dst + e0 + i, a.epilogue, a.N));
+            __stcs(d.dst + e0 + i, epilogue1(sum2[i], d.dst + e0 + i, a.epilogue, a.N));
       }
     }
     if (++stage == (uint32_t)a.bulk.stages) {
@@ -419,21 +396,18 @@ TIDE_BOUNDS_COUNTER(rs_bulk_bounds)
 
 BulkLayout rs_bulk_layout(int N, int M, int L, int smem_budget) {
   BulkLayout b{};
-  b.V = 256 / M;
-  b.PS = 8 * M + (M % 2 == 0 ? 8 : 0);
-  b.stage_bytes = 16 * N * b.V;
-  const int part_bytes = 2 * b.V * b.PS * 4;
-  const int fixed = part_bytes + 1024 + kMaxN * 8 + 4 * 64;
+  b.V = 256;
+  b.stage_bytes = 16 * L * b.V;
+  const int fixed = kMaxBulkStages * (int)sizeof(TileDesc) + 2 * kMaxBulkStages * 8 + (1 + 2 * kMaxBulkStages) * 4 + 256;
   int stages = (smem_budget - fixed) / b.stage_bytes;
   stages = stages < 2 ? 2 : (stages > kMaxBulkStages ? kMaxBulkStages : stages);
   b.stages = stages;
-  b.off_part = stages * b.stage_bytes;
-  b.off_desc = b.off_part + part_bytes;
+  b.off_desc = stages * b.stage_bytes;
   b.off_bar = b.off_desc + kMaxBulkStages * (int)sizeof(TileDesc);
-  b.off_src = b.off_bar + 2 * kMaxBulkStages * 8;
-  b.off_ctl = b.off_src + kMaxN * 8;
+  b.off_ctl = b.off_bar + 2 * kMaxBulkStages * 8;
   b.smem_bytes = b.off_ctl + (1 + 2 * kMaxBulkStages) * 4;
-  (void)L;
+  (void)N;
+  (void)M;
   return b;
 }
 

@@ -112,14 +112,13 @@ struct UnitStart {
 constexpr int kMaxBulkStages = 16;
 constexpr int TIDE_DEVICE_TIMEOUT = 1;  // status-word bit: a kernel gave up waiting
 struct BulkLayout {
-  int32_t V;            // 8-element vectors per tile (256 / M)
-  int32_t PS;           // floats per vector row of the transposition buffer
-  int32_t stage_bytes;  // 16 * N * V
+  int32_t V;            // 8-element vectors per tile (256: 2048 outputs, 4 KiB windows)
+  int32_t stage_bytes;  // 16 * L * V: one node's L windows of one tile
   int32_t stages;
-  int32_t off_part, off_desc, off_bar, off_src, off_ctl, smem_bytes;
+  int32_t off_desc, off_bar, off_ctl, smem_bytes;
   int* status;              // plan's device status word
   uint64_t wait_limit_ns;   // bound on every wait
-  int64_t test_drop_tile;   // tile whose data the producer withholds (tests); -1: none
+  int64_t test_drop_tile;   // stage fill whose data the producer withholds (tests); -1: none
 };
 
 struct RsArgs {
@@ -199,10 +198,10 @@ struct tide_plan {
   int64_t S = 0;
   std::vector<tide::RsItem> rs_items;
   std::vector<tide::AgItem> ag_items;
-  std::vector<tide::AgItem> ag_items_unpadded;
+  std::vector<tide::AgItem> ag_items_unpadded;   // ag_items restricted to real rows
   // Bulk-copy all-gather split of ag_items (bf16, 16-byte aligned bases):
   // the aligned middles in chunks of at most kAgBulkChunkElems, and the rest.
-  std::vector<tide::AgItem> ag_bulk_items, ag_rest_items;  // ag_items restricted to real rows
+  std::vector<tide::AgItem> ag_bulk_items, ag_rest_items;
   std::vector<tide::AgItem> pack_items;         // Slot-Reuse: r = grad index r*P+p, p = slot rank
   std::vector<const void*> slot_grads;          // tide_rs_reduce_slots' pointer array (host)
   std::vector<int64_t> ag_prefix;  // all-gather cost prefix sums (load balance)

@@ -171,7 +171,8 @@ tide_status tide_plan_level2_order(const tide_plan* plan, int32_t n_dest, int32_
  *   TIDE_OPT_SUM_ORDER     the level-2 addition order (tide_sum_order,
  *                          below); default TIDE_SUM_LANDING.
  *   TIDE_OPT_TEST_DROP_TILE  test hook: the bulk reduce-scatter's producer
- *                          withholds the given tile, and the bulk
+ *                          withholds the given stage fill (one source
+ *                          node's windows of one tile), and the bulk
  *                          all-gather skips the given chunk's load (both
  *                          counted per CTA from 0), so a bounded wait runs
  *                          out; -1 (default) disables.

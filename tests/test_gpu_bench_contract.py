@@ -54,7 +54,20 @@ def test_default_line_has_every_contract_key():
         assert g["rs"]["GB_s"] == pytest.approx(g["rs_bytes_per_step"] / g["rs"]["ms"] / 1e6, rel=1e-3)
 
 
-@pytest.mark.parametrize("path", ["staged-rs", "rd-ag", "variants"])
+@pytest.mark.parametrize("path", ["staged-rs", "rd-ag", "variants", "ag-ceiling"])
 def test_other_paths_print_one_line(path):
     rec = _run("--path", path, *SMALL, "--steps", "2", "--warmup", "1")
     assert rec["path"] == path and rec["value"] > 0
+
+
+def test_path_options_select_what_is_timed():
+    rec = _run("--path", "variants", "--variants", "rs_bulk,ag_sm", *SMALL, "--steps", "2", "--warmup", "1")
+    assert set(rec["variants"]) == {"rs_bulk", "ag_sm"}
+    rec = _run("--path", "staged-rs", "--staged-budget", "pages", "--inbox-offset", "1", *SMALL, "--steps", "2",
+               "--warmup", "1")
+    assert "pages_16_4" in rec and "fill" not in rec and rec["config"]["inbox_offset_floats"] == 1
+    rec = _run("--path", "rd-ag", "--rd-exchange", "sm", "--rd-mode", "rails", *SMALL, "--steps", "2", "--warmup", "1")
+    assert set(rec["exchange_all_rails"]) == {"sm_kernel"} and rec["exchange"] == {}
+    rec = _run("--path", "ag-ceiling", "--per-config", "none", *SMALL, "--steps", "3", "--warmup", "1")
+    g = rec["groups"]["llama70b"]
+    assert set(rec["groups"]) == {"llama70b"} and g["ag_ms"] > 0 and g["copy_ms"] > 0
