@@ -3,13 +3,14 @@
 // Same result as rs_fused (bit for bit: identical fp32 addition order) but the
 // contributors' bf16 data reach the SM through the Tensor Memory Accelerator
 // instead of per-thread loads, so the bytes in flight per SM are set by the
-// shared-memory ring, not by registers:
+// shared-memory rings, not by registers:
 //
-//   * one CTA per SM, a producer warp and 8 consumer warps;
-//   * a ring of S stages; a stage holds, for one tile of T = 8*V = 2048
-//     outputs of one item and one source node, the aligned 16-byte windows of
-//     that node's L contributors (L windows of at most 4 KiB), so a tile
-//     takes M stages;
+//   * two CTAs per SM (two independent pipelines), each a producer warp and 8
+//     consumer warps;
+//   * per CTA a ring of S stages (3 of 32 KiB with L = 8); a stage holds,
+//     for one tile of T = 8*V = 2048 outputs of one item and one source
+//     node, the aligned 16-byte windows of that node's L contributors (L
+//     windows of at most 4 KiB), so a tile takes M stages;
 //   * the producer walks the CTA's items (round-robin over the grid: the
 //     consumers follow the producer's order without a shared counter) and,
 //     per tile, fills one stage per source node in the tile's level-2 order
@@ -345,7 +346,7 @@ __device__ void consumers(const RsArgs& a, const Smem& m) {
 }
 
 template <int L>
-__global__ void __launch_bounds__(kConsumers + 32, 1) rs_bulk_kernel(const __grid_constant__ RsArgs a) {
+__global__ void __launch_bounds__(kConsumers + 32, kBulkCtasPerSm) rs_bulk_kernel(const __grid_constant__ RsArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Smem m = carve(smem, a);
   if (threadIdx.x == 0) {
@@ -386,6 +387,14 @@ int launch_t(const RsArgs& a, int grid, cudaStream_t s) {
 }
 
 template <int L>
+int occupancy_t(int smem_bytes) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, rs_bulk_kernel<L>, kConsumers + 32, smem_bytes) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+template <int L>
 int setup_t(int smem_bytes) {
   return (int)cudaFuncSetAttribute(rs_bulk_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
@@ -423,6 +432,20 @@ int rs_bulk_setup(int L, int smem_bytes) {
     case 8: return setup_t<8>(smem_bytes);
   }
   return (int)cudaErrorInvalidValue;
+}
+
+int rs_bulk_blocks_per_sm(int L, int smem_bytes) {
+  switch (L) {
+    case 1: return occupancy_t<1>(smem_bytes);
+    case 2: return occupancy_t<2>(smem_bytes);
+    case 3: return occupancy_t<3>(smem_bytes);
+    case 4: return occupancy_t<4>(smem_bytes);
+    case 5: return occupancy_t<5>(smem_bytes);
+    case 6: return occupancy_t<6>(smem_bytes);
+    case 7: return occupancy_t<7>(smem_bytes);
+    case 8: return occupancy_t<8>(smem_bytes);
+  }
+  return 0;
 }
 
 int launch_rs_bulk(const RsArgs& a, int grid, void* stream) {

@@ -110,6 +110,7 @@ struct UnitStart {
 // Bulk-copy pipeline of the reduce-scatter (rs_bulk.cu): tile geometry and
 // shared-memory carve-up, fixed per plan when it is set up on a device.
 constexpr int kMaxBulkStages = 16;
+constexpr int kBulkCtasPerSm = 2;  // bulk-copy reduce-scatter pipelines per SM
 constexpr int TIDE_DEVICE_TIMEOUT = 1;  // status-word bit: a kernel gave up waiting
 struct BulkLayout {
   int32_t V;            // 8-element vectors per tile (256: 2048 outputs, 4 KiB windows)
@@ -177,6 +178,7 @@ int launch_rs_staged(const RsArgs& args, int sum_grid, bool sum_wide, int land_g
 int rs_land_blocks_per_sm(int M, int L, int vec);  // resident landing CTAs per SM (0 on error)
 BulkLayout rs_bulk_layout(int N, int M, int L, int smem_budget);
 int rs_bulk_setup(int L, int smem_bytes);  // raises the kernel's dynamic shared-memory limit
+int rs_bulk_blocks_per_sm(int L, int smem_bytes);  // resident bulk CTAs per SM with that much shared memory
 // Resident CTAs per SM of each kernel (occupancy), for grid sizing.
 int rs_blocks_per_sm(int L);
 // Store-check counters of the kernels' translation units (check.cuh); 0 in
