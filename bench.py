@@ -37,6 +37,7 @@ if ROOT not in sys.path:
 
 METRIC = "RS/AG effective HBM GB/s and % of GB300 HBM peak (1 GPU); elements/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, vendor figure (context beside the measured peak)
 DEFAULT_WORKLOAD = "wan22dit"
 # The four full-size groups the step is measured on; the default run times
 # the headline workload, then the other three under `per_config`.
@@ -332,13 +333,15 @@ def time_group(args, w, world, dev, stream, windows, keep=False):
     plan.check()
 
     local_s = start.elapsed_time(stop) / 1e3
-    rs_ms = statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for k in range(K))
-    ag_ms = statistics.mean(ev[k][1].elapsed_time(ev[k][2]) for k in range(K))
+    rs_all = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    ag_all = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    rs_ms, ag_ms = statistics.mean(rs_all), statistics.mean(ag_all)
     step_bytes = nbytes["rs_bytes"] + nbytes["ag_bytes"]
     max_s, total_bytes = aggregate(local_s, float(step_bytes * K), world, device=dev)
     _, total_elems = aggregate(local_s, float((nbytes["rs_elems"] + nbytes["ag_elems"]) * K), world, device=dev)
     res = {"w": w, "plan": plan, "nbytes": nbytes, "max_s": max_s, "total_bytes": total_bytes,
-           "total_elems": total_elems, "rs_ms": rs_ms, "ag_ms": ag_ms, "launches": launches}
+           "total_elems": total_elems, "rs_ms": rs_ms, "ag_ms": ag_ms, "launches": launches,
+           "rs_ms_median": statistics.median(rs_all), "ag_ms_median": statistics.median(ag_all)}
     if keep:
         res["buffers"] = (grads, rs_out, ag_in, ag_out, ptrs)
     else:
@@ -348,13 +351,17 @@ def time_group(args, w, world, dev, stream, windows, keep=False):
     return res
 
 
-def call_stats(nbytes, rs_ms, ag_ms, peak):
-    rs_gbs = nbytes["rs_bytes"] / rs_ms / 1e6
-    ag_gbs = nbytes["ag_bytes"] / ag_ms / 1e6
-    return ({"ms": round(rs_ms, 4), "GB_s": round(rs_gbs, 2), "frac": round(rs_gbs / peak, 4),
-             "elements_per_s": round(nbytes["rs_elems"] / rs_ms * 1e3, 1)},
-            {"ms": round(ag_ms, 4), "GB_s": round(ag_gbs, 2), "frac": round(ag_gbs / peak, 4),
-             "elements_per_s": round(nbytes["ag_elems"] / ag_ms * 1e3, 1)})
+def call_stats(g, peak):
+    """Per-call figures of a timed group: mean over the K timed calls (what
+    GB/s and frac use) and the median beside it."""
+    nbytes = g["nbytes"]
+    out = []
+    for call in ("rs", "ag"):
+        ms = g[call + "_ms"]
+        gbs = nbytes[call + "_bytes"] / ms / 1e6
+        out.append({"ms": round(ms, 4), "ms_median": round(g[call + "_ms_median"], 4), "GB_s": round(gbs, 2),
+                    "frac": round(gbs / peak, 4), "elements_per_s": round(nbytes[call + "_elems"] / ms * 1e3, 1)})
+    return out[0], out[1]
 
 
 def run_ours(args, rank, world, local_rank):
@@ -384,7 +391,7 @@ def run_ours(args, rank, world, local_rank):
     for name in per_config_groups(args):
         sub = argparse.Namespace(**{**vars(args), "workload": name, "nodes": 0})
         g = time_group(args, get_workload(sub), world, dev, stream, windows)
-        rs, ag = call_stats(g["nbytes"], g["rs_ms"], g["ag_ms"], peak)
+        rs, ag = call_stats(g, peak)
         step_gbs = g["total_bytes"] / g["max_s"] / 1e9
         per_config[name] = {
             "workload": f"{g['w'].name}: {g['w'].notes}", "N": g["w"].N, "M": g["w"].M, "L": g["w"].L,
@@ -398,7 +405,7 @@ def run_ours(args, rank, world, local_rank):
         return None
     max_s, launches = head["max_s"], head["launches"]
     value = head["total_bytes"] / max_s / 1e9
-    rs, ag = call_stats(nbytes, head["rs_ms"], head["ag_ms"], peak)
+    rs, ag = call_stats(head, peak)
     traffic = profiled_traffic(f"rs_fused_{w.name}.txt", "rs_kernel.cu", 2 * nbytes["rs_elems"],
                                4 * w.N * nbytes["S"])
     step_bytes = nbytes["rs_bytes"] + nbytes["ag_bytes"]
@@ -428,7 +435,8 @@ def run_ours(args, rank, world, local_rank):
                      "peak_source": peak_kind, "unit": "GB/s", "frac": rs["frac"],
                      "traffic": traffic["bytes"] if traffic else None,
                      "traffic_source": traffic["source"] if traffic else None,
-                     "algorithmic_bytes_per_launch": nbytes["rs_bytes"]},
+                     "algorithmic_bytes_per_launch": nbytes["rs_bytes"],
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": round(rs["GB_s"] / NOMINAL_HBM_GBS, 4)},
         "per_config": per_config,
         "gpu_launches": launches[0] + launches[1],
         "kernels_per_step": {"rs": launches[0] / K, "ag": launches[1] / K},
