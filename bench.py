@@ -342,6 +342,8 @@ def time_group(args, w, world, dev, stream, windows, keep=False):
     res = {"w": w, "plan": plan, "nbytes": nbytes, "max_s": max_s, "total_bytes": total_bytes,
            "total_elems": total_elems, "rs_ms": rs_ms, "ag_ms": ag_ms, "launches": launches,
            "rs_ms_median": statistics.median(rs_all), "ag_ms_median": statistics.median(ag_all)}
+    res["rs_ms_uploading"], res["ag_ms_uploading"] = time_table_uploads(plan, w, dev, stream, grads, ag_in, ptrs,
+                                                                        min(K, 10))
     if keep:
         res["buffers"] = (grads, rs_out, ag_in, ag_out, ptrs)
     else:
@@ -349,6 +351,34 @@ def time_group(args, w, world, dev, stream, windows, keep=False):
         del grads, rs_out, ag_in, ag_out, ptrs
         torch.cuda.empty_cache()
     return res
+
+
+def time_table_uploads(plan, w, dev, stream, grads, ag_in, ptrs, K):
+    """Mean time of a call that must upload its pointer table: calls
+    alternate between the timed output buffers and a second set, so each
+    call's table differs from the one before (outside the timed region of
+    the step; the steady state of the step reuses its tables)."""
+    import torch
+
+    import fsdp_layout_aware_gb300 as tide
+    rs_out2 = [torch.empty(plan.S, dtype=torch.float32, device=dev) for _ in range(w.N)]
+    ag_out2 = [torch.empty(w.N * plan.e[p], dtype=torch.int16, device=dev) for p in range(w.P)]
+    rs_sets = [ptrs[1], tide.pointer_array(rs_out2)]
+    ag_sets = [ptrs[3], tide.pointer_array(ag_out2)]
+    out = []
+    for call in (lambda k: plan.rs_reduce(ptrs[0], rs_sets[k % 2], stream),
+                 lambda k: plan.ag_place(ptrs[2], ag_sets[k % 2], 2, stream)):
+        call(1)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for k in range(K):
+            call(k)
+            ev[k + 1].record(stream)
+        torch.cuda.synchronize()
+        out.append(statistics.mean(ev[k].elapsed_time(ev[k + 1]) for k in range(K)))
+    del rs_out2, ag_out2
+    return out[0], out[1]
 
 
 def call_stats(g, peak):
@@ -360,7 +390,8 @@ def call_stats(g, peak):
         ms = g[call + "_ms"]
         gbs = nbytes[call + "_bytes"] / ms / 1e6
         out.append({"ms": round(ms, 4), "ms_median": round(g[call + "_ms_median"], 4), "GB_s": round(gbs, 2),
-                    "frac": round(gbs / peak, 4), "elements_per_s": round(nbytes[call + "_elems"] / ms * 1e3, 1)})
+                    "frac": round(gbs / peak, 4), "elements_per_s": round(nbytes[call + "_elems"] / ms * 1e3, 1),
+                    "ms_uploading_pointer_table": round(g[call + "_ms_uploading"], 4)})
     return out[0], out[1]
 
 

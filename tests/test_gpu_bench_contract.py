@@ -39,7 +39,7 @@ def test_default_line_has_every_contract_key():
     assert roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"], rel=1e-3)
     assert roof["frac_of_nominal"] == pytest.approx(roof["achieved"] / roof["nominal_peak"], rel=1e-3)
     for call in ("rs", "ag"):
-        assert rec[call]["ms_median"] > 0 and rec[call]["ms"] > 0
+        assert rec[call]["ms_median"] > 0 and rec[call]["ms"] > 0 and rec[call]["ms_uploading_pointer_table"] > 0
     cpu = rec["cpu_baseline"]
     assert cpu["kind"] == "oracle" and cpu["cores"] == 1 and cpu["value"] > 0 and cpu["sample"]
     e2e = rec["e2e"]
