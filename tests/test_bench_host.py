@@ -7,6 +7,7 @@ import socket
 import subprocess
 import sys
 
+import pytest
 import torch.multiprocessing as mp
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -81,3 +82,62 @@ def test_reference_arm_only_rank0_prints(monkeypatch):
     assert bench.run_reference(args, rank=1, world=2) is None
     rec = bench.run_reference(args, rank=0, world=2)
     assert rec["n_gpus"] == 2 and rec["impl"] == "reference"
+
+
+def test_per_config_groups_selection():
+    pick = lambda *argv: bench.per_config_groups(bench.parse_args(list(argv)))
+    assert pick() == ["llama70b", "qwen3moe", "uneven"]                      # headline wan22dit
+    assert pick("--workload", "uneven") == ["wan22dit", "llama70b", "qwen3moe"]
+    assert pick("--workload", "tiny") == []                                   # not a measured group
+    assert pick("--nodes", "16") == []                                        # a regrouped headline
+    assert pick("--per-config", "none") == []
+    assert pick("--per-config", "uneven, llama70b") == ["uneven", "llama70b"]
+
+
+def test_rank_bytes_sum_to_the_algorithmic_bytes():
+    for name in ("tiny", "uneven"):
+        w, _ = bench.oracle_sample(name)
+        geo = O.geometry(w.shapes, w.N)
+        nb = bench.algorithmic_bytes(w, geo)
+        assert bench.rank_bytes(w, geo, range(w.N)) == nb["rs_bytes"] + nb["ag_bytes"]
+        half = list(range(0, w.N, 2))
+        rest = list(range(1, w.N, 2))
+        assert bench.rank_bytes(w, geo, half) + bench.rank_bytes(w, geo, rest) == nb["rs_bytes"] + nb["ag_bytes"]
+
+
+def test_profiled_traffic_scales_reads_and_adds_algorithmic_writes(tmp_path, monkeypatch):
+    """Reads of the captured launch scale by the ratio of contributor bytes;
+    writes are the full launch's algorithmic writes; a summary taken on other
+    kernel source gives None."""
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "fsdp_layout_aware_gb300" / "csrc").mkdir(parents=True)
+    src = tmp_path / "fsdp_layout_aware_gb300" / "csrc" / "k.cu"
+    src.write_bytes(b"kernel source")
+    import hashlib
+    digest = hashlib.sha256(b"kernel source").hexdigest()
+    (tmp_path / "profiles" / "p.txt").write_text(
+        f"workload_captured: g rows/4\nkernel_source_sha256: {digest}\n"
+        "algorithmic_read_bytes_captured: 1000\nalgorithmic_write_bytes_captured: 100\n"
+        "dram_bytes_read: 1010\ndram_bytes_write: 90\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    t = bench.profiled_traffic("p.txt", "k.cu", 4000, 400)
+    assert t["bytes"] == 1010 * 4 + 400
+    assert t["captured_dram_read_over_algorithmic"] == 1.01 and t["captured_dram_write_over_algorithmic"] == 0.9
+    assert "g rows/4" in t["source"] and "x 4" in t["source"]
+    src.write_bytes(b"changed source")
+    assert bench.profiled_traffic("p.txt", "k.cu", 4000, 400) is None
+    assert bench.profiled_traffic("missing.txt", "k.cu", 4000, 400) is None
+
+
+def test_committed_headline_traffic_covers_the_algorithmic_bytes():
+    """The committed rs_fused summaries give a full-launch traffic at least the
+    algorithmic bytes (nothing is read less than once) for every measured group
+    whose summary matches the current kernel source."""
+    for name in ("wan22dit", "llama70b", "qwen3moe", "uneven"):
+        w = configs.get(name)
+        geo = O.geometry(w.shapes, w.N)
+        nb = bench.algorithmic_bytes(w, geo)
+        t = bench.profiled_traffic(f"rs_fused_{name}.txt", "rs_kernel.cu", 2 * nb["rs_elems"], 4 * w.N * geo.S)
+        if t is None:
+            pytest.skip(f"profiles/rs_fused_{name}.txt was taken on other kernel source (bench reports null)")
+        assert nb["rs_bytes"] <= t["bytes"] <= 1.01 * nb["rs_bytes"], name
