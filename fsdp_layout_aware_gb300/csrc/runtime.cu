@@ -152,7 +152,7 @@ tide_status ensure_device(tide_plan* pl) {
     // Bulk-copy pipeline (M <= 8 only): kBulkCtasPerSm CTAs per SM, each with
     // as many stages as its share of the SM's shared memory allows (a little
     // is left for the per-block reservation and the static allocations).
-    // Two independent pipelines per SM measured 9-31% faster than one with
+    // Two independent pipelines per SM measured 10-31% faster than one with
     // twice the ring, three 1-3% slower than two.
     int optin = 0, per_sm = 0;
     if ((err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
