@@ -34,6 +34,7 @@ def test_default_line_has_every_contract_key():
     assert rec["n_gpus"] == 1 and rec["steps"] == K and rec["warmup"] == W and rec["value"] > 0
     assert rec["higher_is_better"] is True and rec["scaling"] == "weak" and rec["vs_baseline"] is None
     assert "workload" in rec["config"]
+    assert rec["config"]["l2"].startswith("L2 flushed")   # llama70b rows/64 moves 320 MB per step
     roof = rec["roofline"]
     assert roof["bound"] == "hbm" and roof["unit"] == "GB/s" and roof["peak"] > 0
     assert roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"], rel=1e-3)
