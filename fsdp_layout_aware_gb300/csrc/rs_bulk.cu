@@ -5,12 +5,12 @@
 // instead of per-thread loads, so the bytes in flight per SM are set by the
 // shared-memory rings, not by registers:
 //
-//   * two CTAs per SM (two independent pipelines), each a producer warp and 8
-//     consumer warps;
-//   * per CTA a ring of S stages (3 of 32 KiB with L = 8); a stage holds,
-//     for one tile of T = 8*V = 2048 outputs of one item and one source
+//   * four CTAs per SM (four independent pipelines), each a producer warp and
+//     4 consumer warps;
+//   * per CTA a ring of S stages (3 of 16 KiB with L = 8); a stage holds,
+//     for one tile of T = 8*V = 1024 outputs of one item and one source
 //     node, the aligned 16-byte windows of that node's L contributors (L
-//     windows of at most 4 KiB), so a tile takes M stages;
+//     windows of at most 2 KiB), so a tile takes M stages;
 //   * the producer walks the CTA's items (round-robin over the grid: the
 //     consumers follow the producer's order without a shared counter) and,
 //     per tile, fills one stage per source node in the tile's level-2 order
@@ -47,7 +47,7 @@
 namespace tide {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 4;
 constexpr int kConsumers = kConsumerWarps * 32;
 
 enum TileKind : int32_t { TILE_BULK = 0, TILE_PAD = 1, TILE_DIRECT = 2, TILE_END = 3 };
@@ -405,7 +405,7 @@ TIDE_BOUNDS_COUNTER(rs_bulk_bounds)
 
 BulkLayout rs_bulk_layout(int N, int M, int L, int smem_budget) {
   BulkLayout b{};
-  b.V = 256;
+  b.V = 128;
   b.stage_bytes = 16 * L * b.V;
   const int fixed = kMaxBulkStages * (int)sizeof(TileDesc) + 2 * kMaxBulkStages * 8 + (1 + 2 * kMaxBulkStages) * 4 + 256;
   int stages = (smem_budget - fixed) / b.stage_bytes;

@@ -152,8 +152,11 @@ tide_status ensure_device(tide_plan* pl) {
     // Bulk-copy pipeline (M <= 8 only): kBulkCtasPerSm CTAs per SM, each with
     // as many stages as its share of the SM's shared memory allows (a little
     // is left for the per-block reservation and the static allocations).
-    // Two independent pipelines per SM measured 10-31% faster than one with
-    // twice the ring, three 1-3% slower than two.
+    // Independent pipelines per SM set the speed: one CTA of 8 consumer
+    // warps with a 6-stage ring of 32 KiB reached 0.76-0.95 of the copy
+    // bandwidth, two such CTAs with 3 stages each 0.99-1.04, four CTAs of 4
+    // consumer warps with 3 stages of 16 KiB each 1.015-1.067 (kept); five
+    // spill registers and are 3-4% slower.
     int optin = 0, per_sm = 0;
     if ((err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
       return bail(err, "cudaDeviceGetAttribute(smem)");

@@ -110,10 +110,10 @@ struct UnitStart {
 // Bulk-copy pipeline of the reduce-scatter (rs_bulk.cu): tile geometry and
 // shared-memory carve-up, fixed per plan when it is set up on a device.
 constexpr int kMaxBulkStages = 16;
-constexpr int kBulkCtasPerSm = 2;  // bulk-copy reduce-scatter pipelines per SM
+constexpr int kBulkCtasPerSm = 4;  // bulk-copy reduce-scatter pipelines per SM
 constexpr int TIDE_DEVICE_TIMEOUT = 1;  // status-word bit: a kernel gave up waiting
 struct BulkLayout {
-  int32_t V;            // 8-element vectors per tile (256: 2048 outputs, 4 KiB windows)
+  int32_t V;            // 8-element vectors per tile (128: 1024 outputs, 2 KiB windows)
   int32_t stage_bytes;  // 16 * L * V: one node's L windows of one tile
   int32_t stages;
   int32_t off_desc, off_bar, off_ctl, smem_bytes;
