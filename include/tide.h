@@ -152,9 +152,11 @@ tide_status tide_plan_level2_order(const tide_plan* plan, int32_t n_dest, int32_
  *                          producer warp streams the contributors into shared
  *                          memory with bulk copies (TMA).  Both add in the
  *                          same order and give bit-identical results; the
- *                          bulk path pays one copy request per contributor
- *                          window, so it suits groups with few ranks; it
- *                          takes at most 8 nodes (UNIMPLEMENTED beyond).
+ *                          bulk path stages one source node's windows (up
+ *                          to 2 KiB per contributor) per step of its
+ *                          shared-memory ring, whatever the number of
+ *                          ranks; it takes at most 8 nodes (UNIMPLEMENTED
+ *                          beyond).
  *   TIDE_OPT_WAIT_LIMIT_NS bound, in nanoseconds, on every wait inside the
  *                          bulk-copy kernels (default 2e9).  A kernel that runs
  *                          out records TIDE_ERR_TIMEOUT for tide_plan_check,
