@@ -262,7 +262,12 @@ def per_config_groups(args):
         if args.workload not in MEASURED_GROUPS or args.nodes:
             return []
         return [g for g in MEASURED_GROUPS if g != args.workload]
-    return [g.strip() for g in args.per_config.split(",") if g.strip()]
+    from synth import configs
+    names = [g.strip() for g in args.per_config.split(",") if g.strip()]
+    unknown = [g for g in names if g not in configs.BY_NAME]
+    if unknown:
+        raise SystemExit(f"--per-config: unknown group(s) {', '.join(unknown)} (known: {', '.join(configs.BY_NAME)})")
+    return names
 
 
 def allocate_group(w, plan, dev, stream):

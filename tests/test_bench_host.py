@@ -92,6 +92,8 @@ def test_per_config_groups_selection():
     assert pick("--nodes", "16") == []                                        # a regrouped headline
     assert pick("--per-config", "none") == []
     assert pick("--per-config", "uneven, llama70b") == ["uneven", "llama70b"]
+    with pytest.raises(SystemExit):
+        pick("--per-config", "llama70b,nosuchgroup")
 
 
 def test_rank_bytes_sum_to_the_algorithmic_bytes():
