@@ -422,6 +422,7 @@ def call_stats(g, peak):
 def run_ours(args, rank, world, local_rank):
     import torch
 
+    groups = per_config_groups(args)   # validated before any GPU work
     torch.cuda.set_device(local_rank)
     init_dist(world, "nccl")
     dev = torch.device("cuda", local_rank)
@@ -443,7 +444,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.empty_cache()
 
     per_config = {}
-    for name in per_config_groups(args):
+    for name in groups:
         sub = argparse.Namespace(**{**vars(args), "workload": name, "nodes": 0})
         g = time_group(args, get_workload(sub), world, dev, stream, windows)
         rs, ag = call_stats(g, peak)
